@@ -1,0 +1,142 @@
+"""CPU oracle for the paged-KV hot path -- TEST INFRASTRUCTURE.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product (the CUDA library and its Python binding) never imports, links or
+calls it, and shares none of its code.
+
+Numeric routines live in ``pa_oracle.c`` (plain C, double precision); the
+block bookkeeping lives in ``blocks.py``.  The wrappers below take numpy
+arrays (host memory) and return numpy arrays.  Element types: "f32",
+"bf16", "f16"; 16-bit buffers are passed as raw uint16 bit patterns.
+
+Pinned functions (see tests/test_oracle_pins.py): slot translation, write,
+block copy, gather, attention, and the block bookkeeping.  None is unpinned.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import blocks  # noqa: F401  (re-exported)
+from .build import build as _build
+
+DTYPES = {"f32": 0, "bf16": 1, "f16": 2}
+ELT = {"f32": 4, "bf16": 2, "f16": 2}
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build()
+        L = ctypes.CDLL(path)
+        vp = ctypes.c_void_p
+        i32, i64 = ctypes.c_int32, ctypes.c_int64
+        L.oracle_slot_mapping.argtypes = [vp, i32, vp, vp, i64, i32, vp]
+        L.oracle_slot_mapping.restype = None
+        L.oracle_write_kv.argtypes = [vp, vp, vp, i64, vp, vp, i64]
+        L.oracle_write_kv.restype = None
+        L.oracle_copy_blocks.argtypes = [vp, vp, i32, vp, i32, i64]
+        L.oracle_copy_blocks.restype = None
+        L.oracle_gather.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
+        L.oracle_gather.restype = None
+        L.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
+                                             ctypes.c_float, ctypes.c_int, ctypes.c_int, vp, ctypes.c_int]
+        L.oracle_paged_attention.restype = None
+        L.oracle_decode.argtypes = [vp, i64, ctypes.c_int, vp]
+        L.oracle_decode.restype = None
+        L.oracle_max_threads.argtypes = []
+        L.oracle_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return ctypes.c_void_p(a.ctypes.data) if a is not None else ctypes.c_void_p(0)
+
+
+def _c(a, dtype=None):
+    a = np.ascontiguousarray(a if dtype is None else np.asarray(a, dtype=dtype))
+    return a
+
+
+def max_threads() -> int:
+    return lib().oracle_max_threads()
+
+
+def decode(raw, dtype: str) -> np.ndarray:
+    """Raw element buffer (float32 array or uint16 bit patterns) -> float64."""
+    raw = _c(raw)
+    out = np.empty(raw.shape, dtype=np.float64)
+    lib().oracle_decode(_ptr(raw), raw.size, DTYPES[dtype], _ptr(out))
+    return out
+
+
+def slot_mapping(block_tables, seq_idx, positions, block_size: int) -> np.ndarray:
+    bt = _c(block_tables, np.int32)
+    si = _c(seq_idx, np.int32)
+    pos = _c(positions, np.int64)
+    out = np.empty(pos.shape[0], dtype=np.int64)
+    lib().oracle_slot_mapping(_ptr(bt), bt.shape[1], _ptr(si), _ptr(pos), pos.shape[0], block_size, _ptr(out))
+    return out
+
+
+def write_kv(k, v, slot_mapping_, k_cache, v_cache) -> None:
+    """In-place row scatter into numpy caches [NB, bs, Hkv, hd] (any element type)."""
+    k, v = _c(k), _c(v)
+    sm = _c(slot_mapping_, np.int64)
+    assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
+    row_bytes = k.nbytes // max(k.shape[0], 1) if k.shape[0] else 0
+    lib().oracle_write_kv(_ptr(k), _ptr(v), _ptr(sm), sm.shape[0], _ptr(k_cache), _ptr(v_cache), row_bytes)
+
+
+def copy_blocks(k_caches, v_caches, block_pairs) -> None:
+    """In-place whole-block copies over every layer's numpy caches."""
+    pairs = _c(block_pairs, np.int64).reshape(-1, 2)
+    n = len(k_caches)
+    for c in list(k_caches) + list(v_caches):
+        assert c.flags.c_contiguous
+    block_bytes = k_caches[0].nbytes // k_caches[0].shape[0]
+    kp = (ctypes.c_void_p * n)(*[c.ctypes.data for c in k_caches])
+    vp = (ctypes.c_void_p * n)(*[c.ctypes.data for c in v_caches])
+    lib().oracle_copy_blocks(kp, vp, n, _ptr(pairs), pairs.shape[0], block_bytes)
+
+
+def gather(cache, block_table, seq_len: int, dtype: str) -> np.ndarray:
+    """First seq_len tokens of one sequence, [seq_len, Hkv, hd] float64."""
+    cache = _c(cache)
+    nb, bs, hkv, hd = cache.shape
+    bt = _c(block_table, np.int32)
+    out = np.empty((seq_len, hkv, hd), dtype=np.float64)
+    lib().oracle_gather(_ptr(cache), _ptr(bt), seq_len, bs, hkv, hd, DTYPES[dtype], _ptr(out))
+    return out
+
+
+def paged_attention(q, k_cache, v_cache, block_tables, seq_lens, query_start_loc, scale: float,
+                    dtype: str, causal: bool = True, seq_select=None, num_threads: int = 0) -> np.ndarray:
+    """Varlen paged causal attention, float64 output [total_q, Hq, hd]."""
+    q = _c(q)
+    kc, vc = _c(k_cache), _c(v_cache)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    total_q, hq, hd = q.shape
+    nb, bs, hkv, hd2 = kc.shape
+    assert hd2 == hd and hq % hkv == 0
+    sel = None if seq_select is None else _c(seq_select, np.uint8)
+    out = np.full((total_q, hq, hd), np.nan, dtype=np.float64)
+    lib().oracle_paged_attention(_ptr(out), _ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl),
+                                 _ptr(qsl), sl.shape[0], hq, hkv, hd, bs, ctypes.c_float(scale),
+                                 1 if causal else 0, DTYPES[dtype], _ptr(sel), num_threads)
+    return out
+
+
+def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: float, dtype: str,
+                     seq_select=None, num_threads: int = 0) -> np.ndarray:
+    """One query per sequence: the num_new = 1 case of paged_attention."""
+    s = np.asarray(context_lens).shape[0]
+    qsl = np.arange(s + 1, dtype=np.int32)
+    return paged_attention(q, k_cache, v_cache, block_tables, context_lens, qsl, scale, dtype, True,
+                           seq_select, num_threads)

@@ -1,0 +1,251 @@
+/*
+ * pa_oracle.c -- CPU oracle for the paged-KV hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file: only the tests, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py do.  It shares no code, header,
+ * table or helper with the CUDA library.
+ *
+ * Every routine is the plain definition written out with loops, in the
+ * order the pages give the steps, accumulating in double precision:
+ *
+ *   - slot translation: "分页 KV Cache" (ai-infra handbook), §块表与 slot
+ *     mapping and the slot_mapping_for helper of its paged.py listing;
+ *     "PagedAttention：分页内存管理" (mini-vllm step 12), §block_table
+ *     translation formula.
+ *   - write: "分页 KV Cache", paged.py PagedKVCache.write (row scatter, in
+ *     index order).
+ *   - block copy: "分页 KV Cache", exercise 2 answer (copy-on-write copies
+ *     the old block's content into the new block); "KV cache：容量推导、分页与
+ *     回收", kv_cache.py Sequence.append (allocate(copy of data)).
+ *   - attention: "分页 KV Cache", paged.py paged_attention (gather the
+ *     first seq_len tokens through the block table, repeat KV heads with
+ *     repeat_interleave, scores = q.k * scale, causal mask
+ *     tril(diagonal = seq_len - num_new), softmax, P.V).
+ *
+ * Element types: 0 = fp32, 1 = bf16, 2 = fp16.  Inputs are decoded to double
+ * exactly from their bit patterns; results are returned in double.  The
+ * page's reference casts the softmax probabilities back to the query dtype
+ * before P.V; this oracle keeps them in double (the exact value).
+ *
+ * Build: gcc -O2 -std=c11 -fopenmp -shared -fPIC (oracle/build.py).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- element decoding (IEEE 754 binary32 / bfloat16 / binary16) ---------- */
+
+static double dec_f32(uint32_t bits) {
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* bfloat16 is the upper half of a binary32 with the same sign/exponent. */
+static double dec_bf16(uint16_t bits) { return dec_f32((uint32_t)bits << 16); }
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double dec_f16(uint16_t bits) {
+    int sign = (bits >> 15) & 1;
+    int e = (bits >> 10) & 0x1f;
+    int frac = bits & 0x3ff;
+    double mag;
+    if (e == 0)
+        mag = ldexp((double)frac, -24); /* subnormal: frac * 2^-14 * 2^-10 */
+    else if (e == 31)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp(1.0 + frac / 1024.0, e - 15);
+    return sign ? -mag : mag;
+}
+
+static size_t elt_size(int dtype) { return dtype == 0 ? 4 : 2; }
+
+static double load_elt(const void* base, int64_t i, int dtype) {
+    if (dtype == 0) {
+        uint32_t b;
+        memcpy(&b, (const char*)base + 4 * i, 4);
+        return dec_f32(b);
+    }
+    uint16_t h;
+    memcpy(&h, (const char*)base + 2 * i, 2);
+    return dtype == 1 ? dec_bf16(h) : dec_f16(h);
+}
+
+/* Decode n consecutive elements to double (used by tests to read buffers). */
+void oracle_decode(const void* src, int64_t n, int dtype, double* dst) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = load_elt(src, i, dtype);
+}
+
+/* ---- slot translation ---------------------------------------------------- */
+
+/* Position p lives in logical block p // block_size at offset p % block_size;
+ * the block table maps the logical block to a physical one, and the slot is
+ * physical_block * block_size + offset. */
+int64_t oracle_slot(const int32_t* block_table, int64_t pos, int32_t block_size) {
+    int64_t logical = pos / block_size;
+    int64_t offset = pos % block_size;
+    return (int64_t)block_table[logical] * block_size + offset;
+}
+
+/* One slot per new token: token i belongs to sequence seq_idx[i] (row of the
+ * padded [num_seqs, max_blocks] table) at position positions[i].  A negative
+ * position marks a padding token and yields slot -1. */
+void oracle_slot_mapping(const int32_t* block_tables, int32_t max_blocks,
+                         const int32_t* seq_idx, const int64_t* positions, int64_t n,
+                         int32_t block_size, int64_t* slot_out) {
+    for (int64_t i = 0; i < n; ++i) {
+        if (positions[i] < 0) {
+            slot_out[i] = -1;
+            continue;
+        }
+        const int32_t* table = block_tables + (int64_t)seq_idx[i] * max_blocks;
+        slot_out[i] = oracle_slot(table, positions[i], block_size);
+    }
+}
+
+/* ---- write ---------------------------------------------------------------- */
+
+/* The cache viewed as [num_blocks * block_size, row] rows; token i's row goes
+ * to row slot_mapping[i], tokens taken in index order.  A negative slot is a
+ * padding token and is skipped. */
+void oracle_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n,
+                     void* k_cache, void* v_cache, int64_t row_bytes) {
+    for (int64_t i = 0; i < n; ++i) {
+        int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        memcpy((char*)k_cache + s * row_bytes, (const char*)k + i * row_bytes, (size_t)row_bytes);
+        memcpy((char*)v_cache + s * row_bytes, (const char*)v + i * row_bytes, (size_t)row_bytes);
+    }
+}
+
+/* ---- copy-on-write block copy -------------------------------------------- */
+
+/* For every layer and every (src, dst) pair in order: the whole dst block of K
+ * and of V receives the content of the src block. */
+void oracle_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                        const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes) {
+    for (int32_t l = 0; l < num_layers; ++l) {
+        for (int32_t p = 0; p < num_pairs; ++p) {
+            int64_t src = block_pairs[2 * p], dst = block_pairs[2 * p + 1];
+            memcpy((char*)k_caches[l] + dst * block_bytes, (const char*)k_caches[l] + src * block_bytes,
+                   (size_t)block_bytes);
+            memcpy((char*)v_caches[l] + dst * block_bytes, (const char*)v_caches[l] + src * block_bytes,
+                   (size_t)block_bytes);
+        }
+    }
+}
+
+/* ---- gather --------------------------------------------------------------- */
+
+/* The first seq_len tokens of one sequence in logical order, as double
+ * [seq_len, num_kv_heads, head_dim]: blocks = table[:ceil(seq_len/bs)], the
+ * blocks' rows concatenated, truncated to seq_len. */
+void oracle_gather(const void* cache, const int32_t* block_table, int32_t seq_len,
+                   int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                   double* out) {
+    int64_t row = (int64_t)num_kv_heads * head_dim;
+    int32_t nblk = (seq_len + block_size - 1) / block_size;
+    int64_t t = 0;
+    for (int32_t b = 0; b < nblk; ++b) {
+        int64_t phys = block_table[b];
+        for (int32_t o = 0; o < block_size && t < seq_len; ++o, ++t) {
+            int64_t src_row = phys * block_size + o;
+            for (int64_t e = 0; e < row; ++e) out[t * row + e] = load_elt(cache, src_row * row + e, dtype);
+        }
+    }
+}
+
+/* ---- attention ------------------------------------------------------------ */
+
+/*
+ * Varlen paged attention, request by request:
+ *   q, out:           [total_q, num_heads, head_dim]  (q in `dtype`, out double)
+ *   k_cache, v_cache: [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables:     [num_seqs, max_blocks] int32
+ *   seq_lens:         [num_seqs]  total context after this step
+ *   query_start_loc:  [num_seqs + 1]  request i owns q rows [qsl[i], qsl[i+1])
+ * New token j of request i sits at position seq_len - num_new + j.  With
+ * causal != 0 it sees positions <= that; with causal == 0 it sees all seq_len.
+ * Query head h reads KV head h / (num_heads / num_kv_heads).
+ * seq_select (may be NULL): only requests with seq_select[i] != 0 are
+ * computed; the rows of the others are left untouched.
+ */
+void oracle_paged_attention(double* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int32_t max_blocks,
+                            const int32_t* seq_lens, const int32_t* query_start_loc,
+                            int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size, float scale, int causal,
+                            int dtype, const uint8_t* seq_select, int num_threads) {
+    const int32_t rep = num_heads / num_kv_heads;
+    const double sc = (double)scale;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        if (seq_select && !seq_select[i]) continue;
+        const int32_t seq_len = seq_lens[i];
+        const int32_t start = query_start_loc[i], end = query_start_loc[i + 1];
+        const int32_t num_new = end - start;
+        if (seq_len <= 0 || num_new <= 0) continue;
+        const int32_t* table = block_tables + (int64_t)i * max_blocks;
+        const int64_t row = (int64_t)num_kv_heads * head_dim;
+        double* k = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
+        double* v = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
+        double* p = (double*)malloc(sizeof(double) * (size_t)seq_len);
+        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+        oracle_gather(k_cache, table, seq_len, block_size, num_kv_heads, head_dim, dtype, k);
+        oracle_gather(v_cache, table, seq_len, block_size, num_kv_heads, head_dim, dtype, v);
+        for (int32_t j = 0; j < num_new; ++j) {
+            const int64_t qrow = start + j;
+            const int64_t pos = (int64_t)seq_len - num_new + j;
+            const int32_t visible = causal ? (int32_t)(pos + 1) : seq_len;
+            for (int32_t h = 0; h < num_heads; ++h) {
+                const int32_t kvh = h / rep;
+                for (int32_t d = 0; d < head_dim; ++d) qv[d] = load_elt(q, (qrow * num_heads + h) * head_dim + d, dtype);
+                /* scores over the visible keys */
+                double m = -INFINITY;
+                for (int32_t s = 0; s < visible; ++s) {
+                    double dot = 0.0;
+                    for (int32_t d = 0; d < head_dim; ++d) dot += qv[d] * k[s * row + (int64_t)kvh * head_dim + d];
+                    p[s] = dot * sc;
+                    if (p[s] > m) m = p[s];
+                }
+                /* softmax */
+                double denom = 0.0;
+                for (int32_t s = 0; s < visible; ++s) {
+                    p[s] = exp(p[s] - m);
+                    denom += p[s];
+                }
+                /* P . V */
+                double* o = out + (qrow * num_heads + h) * head_dim;
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    double acc = 0.0;
+                    for (int32_t s = 0; s < visible; ++s) acc += p[s] * v[s * row + (int64_t)kvh * head_dim + d];
+                    o[d] = acc / denom;
+                }
+            }
+        }
+        free(k);
+        free(v);
+        free(p);
+        free(qv);
+    }
+}
+
+/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+size_t oracle_elt_size(int dtype) { return elt_size(dtype); }

@@ -1,0 +1,61 @@
+"""Shared test helpers: oracle-side caches built from a workload, and the
+attention tolerance.  Test infrastructure; the product never imports this."""
+import json
+import os
+
+import numpy as np
+
+import oracle
+from paged_kv_cache_116_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+NAN_BITS = {"bf16": 0x7FC0, "f16": 0x7E00}
+
+# Attention tolerance: |gpu - exact| <= ATOL + RTOL * |exact|.  ATOL is the
+# stated max-abs bound (1e-5 for fp32, 1e-2 for 16-bit types with fp32
+# accumulation); RTOL is the unit roundoff of the output type, the error
+# that storing the exact value in that type may add by itself.
+ATOL = {"f32": 1e-5, "bf16": 1e-2, "f16": 1e-2}
+RTOL = {"f32": 2.0 ** -24, "bf16": 2.0 ** -8, "f16": 2.0 ** -11}
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def nan_cache(w):
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    if w.dtype == "f32":
+        return np.full(shape, np.nan, dtype=np.float32)
+    return np.full(shape, NAN_BITS[w.dtype], dtype=np.uint16)
+
+
+def oracle_caches(w, after_step=True):
+    """Oracle K/V caches of a workload: NaN everywhere, the cached rows
+    written through the pre-step tables, then (after_step) the step's block
+    copies and new rows."""
+    kc, vc = nan_cache(w), nan_cache(w)
+    slots = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
+    oracle.write_kv(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), slots, kc, vc)
+    if after_step:
+        if w.cow_pairs.shape[0]:
+            oracle.copy_blocks([kc], [vc], w.cow_pairs)
+        slots = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
+        oracle.write_kv(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), slots, kc, vc)
+    return kc, vc
+
+
+def oracle_attention(w, kc=None, vc=None, seq_select=None, causal=None):
+    if kc is None:
+        kc, vc = oracle_caches(w)
+    return oracle.paged_attention(W.raw_numpy(w.q), kc, vc, w.block_tables, w.seq_lens, w.query_start_loc,
+                                  w.scale, w.dtype, w.causal if causal is None else causal,
+                                  seq_select=seq_select)
+
+
+def within_tol(got, exact, dtype):
+    err = np.abs(got - exact)
+    bound = ATOL[dtype] + RTOL[dtype] * np.abs(exact)
+    return bool(np.all(err <= bound)), float(np.nanmax(err)) if err.size else 0.0
