@@ -1,0 +1,205 @@
+/*
+ * pa.h -- C ABI of the GB300 (sm_103a) paged-KV attention library (libpa.so).
+ *
+ * The operations are those of vLLM-style paged attention as the source pages
+ * define them:
+ *   - the K/V pool: per layer one K and one V tensor of shape
+ *     [num_blocks, block_size, num_kv_heads, head_dim], row-major
+ *     ("分页 KV Cache", §实现 and the PagedKVCache class of its paged.py);
+ *   - a token at position p of a request lives in logical block
+ *     p / block_size at offset p % block_size; the request's block table maps
+ *     the logical block to a physical one, and the token's slot is
+ *     physical_block * block_size + offset ("分页 KV Cache", §块表与 slot
+ *     mapping; "PagedAttention：分页内存管理", §block_table translation);
+ *   - attention reads each request's K/V through its block table, with the
+ *     new tokens at the end of the context and a causal mask ("分页 KV
+ *     Cache", §分页注意力 and paged_attention; "aiqz.cc PagedAttention",
+ *     §工程实现要点: per-block partial softmax merged online);
+ *   - copy-on-write copies a shared block into a fresh one before a write
+ *     ("分页 KV Cache", exercise 2; "KV cache：容量推导、分页与回收",
+ *     §共享前缀后为什么需要引用计数).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named as device pointers are device memory owned by the
+ *     caller, contiguous, row-major, 16-byte aligned where noted.  The
+ *     library allocates nothing and keeps no pointer after the call returns.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) on the current device.
+ *   - Argument errors are returned synchronously, before anything is
+ *     enqueued: PA_ERR_INVALID_ARG (bad size, null pointer, misalignment),
+ *     PA_ERR_UNSUPPORTED (a valid but unsupported shape or dtype),
+ *     PA_ERR_WORKSPACE (workspace too small).  PA_ERR_CUDA reports a
+ *     launch failure.  PA_ERR_INDEX is returned only in check mode
+ *     (pa_set_check_mode), which copies the index arrays to the host and
+ *     validates them before launching; without check mode an out-of-range
+ *     block id, slot or length is undefined behaviour, as with tensor
+ *     indexing in the pages' reference code.  pa_last_error() gives a
+ *     human-readable reason for the last non-OK status of the calling thread.
+ *   - Block-table rows are padded to max_blocks; entries at or past
+ *     ceil(len / block_size) are never read.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,
+    PA_ERR_UNSUPPORTED = 2,
+    PA_ERR_INDEX = 3,
+    PA_ERR_WORKSPACE = 4,
+    PA_ERR_CUDA = 5,
+    PA_ERR_TIMEOUT = 6
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+
+/* Library options (pa_set_option).  Global to the process, not thread-safe
+ * against concurrent calls. */
+typedef enum {
+    /* 1: validate index arrays on the host before each launch (synchronises
+     * the stream).  0 (default): no validation. */
+    PA_OPT_CHECK_MODE = 0,
+    /* Decode kernel: 0 automatic (default), 1 the CUDA-core kernel, 2 the
+     * tensor-core kernel (PA_ERR_UNSUPPORTED where it does not apply). */
+    PA_OPT_DECODE_KERNEL = 1,
+    /* Number of CTAs of the tensor-core decode kernel's balanced split;
+     * 0 (default) picks one per resident slot of the device. */
+    PA_OPT_DECODE_CTAS = 2,
+    /* Varlen kernel: 0 automatic (default), 1 the CUDA-core kernel, 2 the
+     * tensor-core kernel. */
+    PA_OPT_VARLEN_KERNEL = 3
+} pa_option;
+
+PA_API const char* pa_status_string(int status);
+/* Reason for the last non-OK status returned on the calling thread. */
+PA_API const char* pa_last_error(void);
+PA_API pa_status pa_set_option(int option, int64_t value);
+PA_API int64_t pa_get_option(int option);
+/* Shorthand for pa_set_option(PA_OPT_CHECK_MODE, on). */
+PA_API pa_status pa_set_check_mode(int on);
+
+/* Device-side status word: kernels that wait on a barrier give up after a
+ * bounded number of polls, set a bit here and return (PA_ERR_TIMEOUT).
+ * Reads (and with clear != 0 resets) it for the current device; synchronises
+ * the device. */
+PA_API pa_status pa_device_status(int clear);
+
+/*
+ * pa_slot_mapping -- slot of each new token.
+ *   slot_out[i] = block_tables[seq_idx[i] * max_blocks + positions[i] / block_size]
+ *                 * block_size + positions[i] % block_size
+ * ("分页 KV Cache", slot_mapping_for; "PagedAttention：分页内存管理",
+ * translate_slot).  positions[i] < 0 marks a padding token: slot_out[i] = -1.
+ *   block_tables: device int32 [num_seqs, max_blocks]
+ *   seq_idx:      device int32 [n], 0 <= seq_idx[i] < num_seqs
+ *   positions:    device int64 [n]
+ *   slot_out:     device int64 [n] (written)
+ */
+PA_API pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks,
+                          const int32_t* seq_idx, const int64_t* positions, int64_t n,
+                          int32_t block_size, int64_t* slot_out, void* stream);
+
+/*
+ * pa_write_kv -- scatter new tokens' K and V rows into the pool.
+ * The cache viewed as [num_blocks * block_size, num_kv_heads * head_dim]
+ * rows; row slot_mapping[i] of k_cache receives k[i], of v_cache v[i]
+ * ("分页 KV Cache", PagedKVCache.write).  A negative slot skips token i
+ * (padding).  Slots must be distinct (check mode rejects duplicates).
+ *   k, v:          device [n, num_kv_heads, head_dim] of dtype, 16-byte aligned
+ *   slot_mapping:  device int64 [n]
+ *   k_cache, v_cache: device [num_blocks, block_size, num_kv_heads, head_dim]
+ * Requires num_kv_heads * head_dim * sizeof(dtype) to be a multiple of 16.
+ * Bit-exact: bytes are moved, never converted.
+ */
+PA_API pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n,
+                      void* k_cache, void* v_cache, int32_t num_blocks, int32_t block_size,
+                      int32_t num_kv_heads, int32_t head_dim, int dtype, void* stream);
+
+/*
+ * pa_copy_blocks -- copy-on-write block copies.
+ * For each layer l and pair p: block block_pairs[2p+1] of k_caches[l] and of
+ * v_caches[l] receives a copy of block block_pairs[2p] (all block_size
+ * slots).  k_caches / v_caches are HOST arrays of num_layers device
+ * pointers (1 <= num_layers <= PA_MAX_LAYERS).  A destination must not be
+ * the source or destination of another pair of the same call (check mode
+ * rejects that); otherwise the pairs run in any order.
+ *   block_pairs: device int64 [num_pairs, 2] (src, dst)
+ */
+#define PA_MAX_LAYERS 128
+PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                         const int64_t* block_pairs, int32_t num_pairs, int32_t num_blocks,
+                         int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                         void* stream);
+
+/*
+ * pa_decode -- one query per sequence over its paged context.
+ * For sequence s and query head h (KV head kv = h / (num_heads / num_kv_heads),
+ * the repeat_interleave grouping of the handbook's paged_attention):
+ *   out[s, h] = softmax(scale * q[s, h] . K_s[0:L]^T) . V_s[0:L],  L = context_lens[s]
+ * where K_s / V_s are read through block_tables[s].  This is the num_new = 1
+ * case of pa_varlen (the query is the last position, so it sees all L keys).
+ * The context is split across CTAs by a length-balanced partition and the
+ * partial softmax states are merged by their log-sum-exp; the partition
+ * depends only on the lengths, so relabelling physical blocks gives
+ * bit-identical output.  context_lens[s] == 0 gives a zero row.
+ *   out, q:       device [num_seqs, num_heads, head_dim] of dtype (16-byte aligned)
+ *   k_cache, v_cache: device [num_blocks, block_size, num_kv_heads, head_dim]
+ *   block_tables: device int32 [num_seqs, max_blocks]
+ *   context_lens: device int32 [num_seqs], each <= max_context
+ *   workspace:    device scratch of at least pa_decode_workspace_size(...) bytes
+ *                 (may be NULL when that size is 0), 16-byte aligned; its
+ *                 content on entry does not matter.
+ * Accumulation is fp32 for every dtype.
+ */
+PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int32_t max_context, int dtype);
+PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                    int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t num_blocks, int32_t block_size, int32_t max_context, float scale,
+                    int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_varlen -- the handbook's paged_attention: a batch of requests, each
+ * with seq_lens[i] tokens of context after this step of which the last
+ * n_i = cu_seqlens_q[i+1] - cu_seqlens_q[i] are new; request i's queries
+ * are rows cu_seqlens_q[i] .. cu_seqlens_q[i+1]-1 of q.  New token j of
+ * request i is at position seq_lens[i] - n_i + j and, with causal != 0,
+ * attends to positions 0..that position; with causal == 0 to all
+ * seq_lens[i] positions.  Decode rows (n_i = 1) and prefill chunks mix
+ * freely in one call.
+ *   out, q:       device [total_q, num_heads, head_dim] of dtype (16-byte aligned)
+ *   cu_seqlens_q: device int32 [num_seqs + 1], cu_seqlens_q[0] = 0,
+ *                 non-decreasing, cu_seqlens_q[num_seqs] = total_q
+ *   seq_lens:     device int32 [num_seqs], n_i <= seq_lens[i] <= max_context
+ *   max_q:        upper bound of n_i over the batch
+ *   workspace:    pa_varlen_workspace_size(...) bytes (may be NULL when 0)
+ */
+PA_API size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int32_t max_context, int dtype);
+PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                    const int32_t* cu_seqlens_q, int32_t num_seqs, int32_t total_q, int32_t max_q,
+                    int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                    int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

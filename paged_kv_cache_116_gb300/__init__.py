@@ -1,1 +1,11 @@
-"""GB300-native paged-KV attention: the binding lives in ``_binding``."""
+"""GB300-native paged-KV attention.
+
+The product is the C-ABI library ``libpa.so`` (include/pa.h); this package
+holds its CUDA sources (``csrc/``), the nvcc build (``build.py``), a ctypes
+binding with the C entry points' names (``_binding``), and seeded synthetic
+inputs (``workloads``).
+"""
+from ._binding import (  # noqa: F401
+    PA_BF16, PA_F16, PA_F32, PA_OPT_CHECK_MODE, PA_OPT_DECODE_CTAS, PA_OPT_DECODE_KERNEL, PA_OPT_VARLEN_KERNEL,
+    PAError, lib, pa_copy_blocks, pa_decode, pa_decode_workspace_size, pa_device_status, pa_get_option,
+    pa_set_check_mode, pa_set_option, pa_slot_mapping, pa_varlen, pa_varlen_workspace_size, pa_write_kv)

@@ -1,0 +1,189 @@
+"""ctypes binding of libpa.so: the C ABI's entry points under the same names.
+
+Argument marshalling only -- torch tensors become device pointers, sizes and
+the current CUDA stream; every step of the path runs in the library's CUDA
+kernels.  There is no fallback: if the library is missing the first call
+raises, and every non-OK status raises PAError with the library's reason.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libpa.so")
+
+PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_OPT_CHECK_MODE, PA_OPT_DECODE_KERNEL, PA_OPT_DECODE_CTAS, PA_OPT_VARLEN_KERNEL = 0, 1, 2, 3
+DTYPE_CODE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+
+EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
+           "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
+           "pa_decode", "pa_varlen_workspace_size", "pa_varlen")
+
+
+class PAError(RuntimeError):
+    def __init__(self, status, name, reason):
+        super().__init__("%s failed: %s (%s)" % (name, name_of(status), reason))
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (loads it on first use; raises if it is not built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libpa.so is not built (%s); run __graft_entry__.build() first" % LIB_PATH)
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    ci, cf = ctypes.c_int, ctypes.c_float
+    sig = {
+        "pa_status_string": ([ci], ctypes.c_char_p),
+        "pa_last_error": ([], ctypes.c_char_p),
+        "pa_set_option": ([ci, i64], ci),
+        "pa_get_option": ([ci], i64),
+        "pa_set_check_mode": ([ci], ci),
+        "pa_device_status": ([ci], ci),
+        "pa_slot_mapping": ([vp, i32, i32, vp, vp, i64, i32, vp, vp], ci),
+        "pa_write_kv": ([vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, ci, vp], ci),
+        "pa_copy_blocks": ([vp, vp, i32, vp, i32, i32, i32, i32, i32, ci, vp], ci),
+        "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
+        "pa_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz, vp], ci),
+        "pa_varlen_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32, ci], sz),
+        "pa_varlen": ([vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, cf, ci, ci, vp,
+                       sz, vp], ci),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+    _lib = L
+    return L
+
+
+def name_of(status):
+    return lib().pa_status_string(status).decode()
+
+
+def _check(status, name):
+    if status != 0:
+        raise PAError(status, name, lib().pa_last_error().decode())
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype(t):
+    try:
+        return DTYPE_CODE[t.dtype]
+    except KeyError:
+        raise TypeError("unsupported dtype %s" % t.dtype)
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def pa_set_option(option, value):
+    _check(lib().pa_set_option(option, value), "pa_set_option")
+
+
+def pa_get_option(option):
+    return lib().pa_get_option(option)
+
+
+def pa_set_check_mode(on):
+    _check(lib().pa_set_check_mode(1 if on else 0), "pa_set_check_mode")
+
+
+def pa_device_status(clear=True):
+    _check(lib().pa_device_status(1 if clear else 0), "pa_device_status")
+
+
+def pa_slot_mapping(block_tables, seq_idx, positions, block_size, slot_out=None, stream=None):
+    """slot_out[i] = block_tables[seq_idx[i], positions[i] // bs] * bs + positions[i] % bs (-1 for pos < 0)."""
+    if slot_out is None:
+        slot_out = torch.empty(positions.shape[0], dtype=torch.int64, device=positions.device)
+    _dev(block_tables, seq_idx, positions, slot_out)
+    st = lib().pa_slot_mapping(_ptr(block_tables), block_tables.shape[0], block_tables.shape[1], _ptr(seq_idx),
+                               _ptr(positions), positions.shape[0], block_size, _ptr(slot_out), _stream(stream))
+    _check(st, "pa_slot_mapping")
+    return slot_out
+
+
+def pa_write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None):
+    """Row scatter of k, v [N, Hkv, hd] into caches [NB, bs, Hkv, hd] at slot_mapping [N]."""
+    _dev(k, v, slot_mapping, k_cache, v_cache)
+    nb, bs, hkv, hd = k_cache.shape
+    st = lib().pa_write_kv(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0], _ptr(k_cache),
+                           _ptr(v_cache), nb, bs, hkv, hd, _dtype(k_cache), _stream(stream))
+    _check(st, "pa_write_kv")
+
+
+def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
+    """Copy block pairs [P, 2] (src, dst) in every layer's K and V cache."""
+    if isinstance(k_caches, torch.Tensor):
+        k_caches, v_caches = [k_caches], [v_caches]
+    _dev(block_pairs, *k_caches, *v_caches)
+    n = len(k_caches)
+    kp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in k_caches])
+    vp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in v_caches])
+    nb, bs, hkv, hd = k_caches[0].shape
+    st = lib().pa_copy_blocks(kp, vp, n, _ptr(block_pairs), block_pairs.shape[0], nb, bs, hkv, hd,
+                              _dtype(k_caches[0]), _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, dtype):
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else dtype
+    return lib().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, code)
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context, scale, workspace=None,
+              stream=None):
+    """One query per sequence: out, q [S, Hq, hd]; context_lens [S]; tables [S, max_blocks]."""
+    _dev(out, q, k_cache, v_cache, block_tables, context_lens, workspace)
+    nb, bs, hkv, hd = k_cache.shape
+    S, hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                         block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb, bs, max_context,
+                         float(scale), _dtype(q), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_varlen_workspace_size(num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, block_size, max_context,
+                             dtype):
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else dtype
+    return lib().pa_varlen_workspace_size(num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, block_size,
+                                          max_context, code)
+
+
+def pa_varlen(out, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, max_q, max_context, scale,
+              causal=True, workspace=None, stream=None):
+    """Mixed prefill/decode: q, out [T, Hq, hd]; cu_seqlens_q [S+1]; seq_lens [S]."""
+    _dev(out, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, workspace)
+    nb, bs, hkv, hd = k_cache.shape
+    T, hq, _ = q.shape
+    S = seq_lens.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_varlen(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                         block_tables.shape[1], _ptr(seq_lens), _ptr(cu_seqlens_q), S, T, max_q, hq, hkv, hd, nb,
+                         bs, max_context, float(scale), 1 if causal else 0, _dtype(q), _ptr(workspace), ws_bytes,
+                         _stream(stream))
+    _check(st, "pa_varlen")
+    return out

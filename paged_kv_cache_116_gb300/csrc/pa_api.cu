@@ -1,0 +1,395 @@
+// pa_api.cu -- the extern "C" entry points declared in include/pa.h:
+// argument validation, optional host-side index checking, and dispatch to
+// the kernels' launchers.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+#include <string>
+#include <unordered_set>
+#include <vector>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+int64_t g_options[4] = {0, 0, 0, 0};
+
+pa_status fail(pa_status st, const std::string& msg) {
+    g_last_error = msg;
+    return st;
+}
+
+pa_status cuda_fail(cudaError_t e, const char* where) {
+    return fail(PA_ERR_CUDA, std::string(where) + ": " + cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool valid_dtype(int d) { return d == PA_F32 || d == PA_BF16 || d == PA_F16; }
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+template <typename T>
+bool to_host(std::vector<T>& dst, const T* src, int64_t n, cudaStream_t st, pa_status* err) {
+    dst.resize((size_t)std::max<int64_t>(n, 0));
+    if (n <= 0) return true;
+    cudaError_t e = cudaMemcpyAsync(dst.data(), src, sizeof(T) * (size_t)n, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        *err = cuda_fail(e, "check mode: copying indices to the host");
+        return false;
+    }
+    return true;
+}
+
+bool check_mode() { return g_options[PA_OPT_CHECK_MODE] != 0; }
+
+// Check-mode validation of block tables against lengths.
+pa_status check_tables(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks, const std::vector<int32_t>& lens,
+                       int32_t num_blocks, int32_t block_size, int32_t max_context, cudaStream_t st) {
+    pa_status err = PA_OK;
+    std::vector<int32_t> bt;
+    if (!to_host(bt, block_tables, (int64_t)num_seqs * max_blocks, st, &err)) return err;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+        const int32_t L = lens[s];
+        if (L < 0 || L > max_context)
+            return fail(PA_ERR_INDEX, "sequence " + std::to_string(s) + ": length " + std::to_string(L) +
+                                          " outside [0, max_context=" + std::to_string(max_context) + "]");
+        const int64_t nb = ((int64_t)L + block_size - 1) / block_size;
+        if (nb > max_blocks)
+            return fail(PA_ERR_INDEX, "sequence " + std::to_string(s) + " needs " + std::to_string(nb) +
+                                          " blocks but the table holds " + std::to_string(max_blocks));
+        for (int64_t b = 0; b < nb; ++b) {
+            const int32_t id = bt[(size_t)s * max_blocks + b];
+            if (id < 0 || id >= num_blocks)
+                return fail(PA_ERR_INDEX, "sequence " + std::to_string(s) + " logical block " + std::to_string(b) +
+                                              " maps to " + std::to_string(id) + ", outside [0, num_blocks)");
+        }
+    }
+    return PA_OK;
+}
+
+pa_status check_geometry(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                         int32_t block_size, int dtype) {
+    if (!valid_dtype(dtype)) return fail(PA_ERR_INVALID_ARG, "dtype must be PA_F32, PA_BF16 or PA_F16");
+    if (num_kv_heads <= 0 || num_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "head counts, head_dim, num_blocks and block_size must be positive");
+    if (num_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_heads must be a multiple of num_kv_heads");
+    if ((int64_t)num_blocks * block_size > INT32_MAX)
+        return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size must fit in int32");
+    return PA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(int status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_INDEX: return "PA_ERR_INDEX";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_TIMEOUT: return "PA_ERR_TIMEOUT";
+        default: return "unknown pa_status";
+    }
+}
+
+const char* pa_last_error(void) { return g_last_error.c_str(); }
+
+pa_status pa_set_option(int option, int64_t value) {
+    if (option < 0 || option > PA_OPT_VARLEN_KERNEL) return fail(PA_ERR_INVALID_ARG, "unknown option");
+    if (value < 0) return fail(PA_ERR_INVALID_ARG, "option values are non-negative");
+    g_options[option] = value;
+    return PA_OK;
+}
+
+int64_t pa_get_option(int option) {
+    if (option < 0 || option > PA_OPT_VARLEN_KERNEL) return -1;
+    return g_options[option];
+}
+
+pa_status pa_set_check_mode(int on) { return pa_set_option(PA_OPT_CHECK_MODE, on ? 1 : 0); }
+
+pa_status pa_device_status(int clear) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "pa_device_status");
+    const uint32_t bits = pa::decode_tc_status(clear != 0);
+    if (bits & 1u) return fail(PA_ERR_TIMEOUT, "a kernel's bounded barrier wait ran out");
+    return PA_OK;
+}
+
+pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks, const int32_t* seq_idx,
+                          const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
+                          void* stream) {
+    if (n < 0 || num_seqs < 0 || max_blocks < 0 || block_size <= 0)
+        return fail(PA_ERR_INVALID_ARG, "sizes must be non-negative and block_size positive");
+    if (n == 0) return PA_OK;
+    if (!block_tables || !seq_idx || !positions || !slot_out) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int32_t> si;
+        std::vector<int64_t> pos;
+        if (!to_host(si, seq_idx, n, st, &err) || !to_host(pos, positions, n, st, &err)) return err;
+        for (int64_t i = 0; i < n; ++i) {
+            if (pos[i] < 0) continue;
+            if (si[i] < 0 || si[i] >= num_seqs)
+                return fail(PA_ERR_INDEX, "token " + std::to_string(i) + ": sequence index out of range");
+            if (pos[i] / block_size >= max_blocks)
+                return fail(PA_ERR_INDEX, "token " + std::to_string(i) + ": position beyond the block table");
+        }
+    }
+    cudaError_t e = pa::launch_slot_mapping(block_tables, max_blocks, seq_idx, positions, n, block_size, slot_out, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_slot_mapping launch");
+}
+
+pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_cache,
+                      void* v_cache, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim,
+                      int dtype, void* stream) {
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (n < 0) return fail(PA_ERR_INVALID_ARG, "n must be non-negative");
+    if (n == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * pa::elt_size(dtype);
+    if (row_bytes % 16 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "num_kv_heads * head_dim * element size must be a multiple of 16 bytes");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "k, v and the caches must be 16-byte aligned");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int64_t> sm;
+        if (!to_host(sm, slot_mapping, n, st, &err)) return err;
+        const int64_t slots = (int64_t)num_blocks * block_size;
+        std::unordered_set<int64_t> seen;
+        for (int64_t i = 0; i < n; ++i) {
+            if (sm[i] < 0) continue;
+            if (sm[i] >= slots)
+                return fail(PA_ERR_INDEX, "token " + std::to_string(i) + ": slot " + std::to_string(sm[i]) +
+                                              " outside the pool");
+            if (!seen.insert(sm[i]).second)
+                return fail(PA_ERR_INDEX, "slot " + std::to_string(sm[i]) + " written twice in one call");
+        }
+    }
+    cudaError_t e = pa::launch_write_kv(k, v, slot_mapping, n, k_cache, v_cache, row_bytes, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_write_kv launch");
+}
+
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* block_pairs,
+                         int32_t num_pairs, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
+                         int32_t head_dim, int dtype, void* stream) {
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs must be non-negative");
+    if (num_layers < 1 || num_layers > PA_MAX_LAYERS)
+        return fail(PA_ERR_INVALID_ARG, "num_layers must be in [1, PA_MAX_LAYERS]");
+    if (num_pairs == 0) return PA_OK;
+    if (!k_caches || !v_caches || !block_pairs) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    for (int l = 0; l < num_layers; ++l) {
+        if (!k_caches[l] || !v_caches[l]) return fail(PA_ERR_INVALID_ARG, "null cache pointer");
+        if (!aligned16(k_caches[l]) || !aligned16(v_caches[l]))
+            return fail(PA_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+    }
+    const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_dim * pa::elt_size(dtype);
+    if (block_bytes % 16 != 0) return fail(PA_ERR_UNSUPPORTED, "a block must be a multiple of 16 bytes");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int64_t> pr;
+        if (!to_host(pr, block_pairs, 2 * (int64_t)num_pairs, st, &err)) return err;
+        std::unordered_set<int64_t> dsts, srcs;
+        for (int32_t p = 0; p < num_pairs; ++p) {
+            const int64_t s = pr[2 * p], d = pr[2 * p + 1];
+            if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks)
+                return fail(PA_ERR_INDEX, "pair " + std::to_string(p) + ": block id outside [0, num_blocks)");
+            if (!dsts.insert(d).second)
+                return fail(PA_ERR_INDEX, "block " + std::to_string(d) + " is the destination of two pairs");
+            srcs.insert(s);
+        }
+        for (int32_t p = 0; p < num_pairs; ++p) {
+            const int64_t s = pr[2 * p], d = pr[2 * p + 1];
+            if (d != s && srcs.count(d))
+                return fail(PA_ERR_INDEX, "block " + std::to_string(d) + " is both a destination and a source");
+        }
+    }
+    cudaError_t e = pa::launch_copy_blocks(k_caches, v_caches, num_layers, block_pairs, num_pairs, block_bytes, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_copy_blocks launch");
+}
+
+// ------------------------------------------------------------------ decode
+
+static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, pa_status* st) {
+    const int64_t want = g_options[PA_OPT_DECODE_KERNEL];
+    const bool ok = pa::decode_tc_supported(dtype, head_dim, block_size, group);
+    *st = PA_OK;
+    if (want == 1) return false;
+    if (want == 2 && !ok) {
+        *st = fail(PA_ERR_UNSUPPORTED, "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256, "
+                                       "block_size 16 and at most 16 query heads per KV head");
+        return false;
+    }
+    return ok;
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_context, int dtype) {
+    if (num_seqs <= 0 || num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads || max_context < 0)
+        return 0;
+    pa_status st;
+    const int G = num_heads / num_kv_heads;
+    if (!use_decode_tc(dtype, head_dim, block_size, G, &st)) return 0;
+    const int grid = pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context, dtype, G,
+                                        g_options[PA_OPT_DECODE_CTAS]);
+    return pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid);
+}
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                    int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    pa_status g = check_geometry(num_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (num_seqs < 0 || max_blocks < 0 || max_context < 0)
+        return fail(PA_ERR_INVALID_ARG, "num_seqs, max_blocks and max_context must be non-negative");
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
+    if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int32_t> lens;
+        if (!to_host(lens, context_lens, num_seqs, st, &err)) return err;
+        err = check_tables(block_tables, num_seqs, max_blocks, lens, num_blocks, block_size, max_context, st);
+        if (err != PA_OK) return err;
+    }
+    pa::AttnArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.seq_lens = context_lens;
+    a.cu_seqlens_q = nullptr;
+    a.num_seqs = num_seqs;
+    a.total_q = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.scale = scale;
+    a.causal = 1;
+    a.dtype = dtype;
+
+    const int G = num_heads / num_kv_heads;
+    pa_status sel;
+    const bool tc = use_decode_tc(dtype, head_dim, block_size, G, &sel);
+    if (sel != PA_OK) return sel;
+    if (!tc) {
+        cudaError_t e = pa::launch_attn_simt(a, st);
+        return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_decode launch");
+    }
+    const int grid = pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context, dtype, G,
+                                        g_options[PA_OPT_DECODE_CTAS]);
+    const size_t need = pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid);
+    if (workspace_bytes < need || (need && !workspace))
+        return fail(PA_ERR_WORKSPACE, "workspace holds " + std::to_string(workspace_bytes) + " bytes, " +
+                                          std::to_string(need) + " needed");
+    if (!aligned16(workspace)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    const int64_t elt = pa::elt_size(dtype);
+    for (int32_t s0 = 0; s0 < num_seqs; s0 += pa::kDecodeMaxSeqsPerLaunch) {
+        pa::AttnArgs c = a;
+        const int32_t cnt = std::min(num_seqs - s0, pa::kDecodeMaxSeqsPerLaunch);
+        c.num_seqs = cnt;
+        c.total_q = cnt;
+        c.out = static_cast<uint8_t*>(out) + (int64_t)s0 * num_heads * head_dim * elt;
+        c.q = static_cast<const uint8_t*>(q) + (int64_t)s0 * num_heads * head_dim * elt;
+        c.block_tables = block_tables + (int64_t)s0 * max_blocks;
+        c.seq_lens = context_lens + s0;
+        std::string err;
+        cudaError_t e = pa::launch_decode_tc(c, num_blocks, grid, workspace, &err, st);
+        if (e != cudaSuccess)
+            return err.empty() ? cuda_fail(e, "pa_decode launch") : fail(PA_ERR_CUDA, "pa_decode: " + err);
+    }
+    return PA_OK;
+}
+
+// ------------------------------------------------------------------ varlen
+
+size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t max_context,
+                                int dtype) {
+    (void)num_seqs, (void)total_q, (void)max_q, (void)num_heads, (void)num_kv_heads, (void)head_dim,
+        (void)block_size, (void)max_context, (void)dtype;
+    return 0;
+}
+
+pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_seqlens_q, int32_t num_seqs,
+                    int32_t total_q, int32_t max_q, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t num_blocks, int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    (void)workspace, (void)workspace_bytes;
+    pa_status g = check_geometry(num_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_blocks < 0 || max_context < 0)
+        return fail(PA_ERR_INVALID_ARG, "sizes must be non-negative");
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !cu_seqlens_q)
+        return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+        return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
+    if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
+    if (g_options[PA_OPT_VARLEN_KERNEL] == 2)
+        return fail(PA_ERR_UNSUPPORTED, "no tensor-core varlen kernel in this build");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int32_t> lens, cu;
+        if (!to_host(lens, seq_lens, num_seqs, st, &err) || !to_host(cu, cu_seqlens_q, num_seqs + 1, st, &err))
+            return err;
+        if (cu[0] != 0 || cu[num_seqs] != total_q)
+            return fail(PA_ERR_INDEX, "cu_seqlens_q must start at 0 and end at total_q");
+        for (int32_t i = 0; i < num_seqs; ++i) {
+            const int32_t nn = cu[i + 1] - cu[i];
+            if (nn < 0) return fail(PA_ERR_INDEX, "cu_seqlens_q must be non-decreasing");
+            if (nn > max_q) return fail(PA_ERR_INDEX, "request " + std::to_string(i) + " has more than max_q queries");
+            if (nn > lens[i])
+                return fail(PA_ERR_INDEX, "request " + std::to_string(i) + " has more new tokens than context");
+        }
+        err = check_tables(block_tables, num_seqs, max_blocks, lens, num_blocks, block_size, max_context, st);
+        if (err != PA_OK) return err;
+    }
+    pa::AttnArgs a{};
+    a.out = out;
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.max_blocks = max_blocks;
+    a.seq_lens = seq_lens;
+    a.cu_seqlens_q = cu_seqlens_q;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.block_size = block_size;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.dtype = dtype;
+    cudaError_t e = pa::launch_attn_simt(a, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_varlen launch");
+}
+
+}  // extern "C"

@@ -1,0 +1,121 @@
+// pa_copy.cu -- the byte-moving kernels of the path: slot translation, the
+// slot-mapped K/V row write, and the copy-on-write block copy.
+//
+// All three are HBM-bound moves.  Rows and blocks are moved as 16-byte
+// vectors (rows are required to be multiples of 16 bytes), one warp per row
+// or a whole CTA per block pair, so every warp instruction touches whole
+// 32-byte sectors.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// slot = block_tables[seq][pos / block_size] * block_size + pos % block_size;
+// a negative position gives -1 ("分页 KV Cache", slot_mapping_for).
+__global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int32_t max_blocks,
+                                    const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ positions,
+                                    int64_t n, int32_t block_size, int64_t* __restrict__ slot_out) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pos = positions[i];
+        if (pos < 0) {
+            slot_out[i] = -1;
+            continue;
+        }
+        const int64_t logical = pos / block_size;
+        const int32_t phys = block_tables[(int64_t)seq_idx[i] * max_blocks + logical];
+        slot_out[i] = (int64_t)phys * block_size + (pos - logical * block_size);
+    }
+}
+
+// One warp per (token, K|V): the token's row of row_vecs 16-byte vectors goes
+// to row slot_mapping[token] of the cache ("分页 KV Cache", PagedKVCache.write).
+constexpr int kWriteWarps = 8;
+
+__global__ void __launch_bounds__(kWriteWarps * 32)
+    write_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
+                    int64_t n, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t row_vecs) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x * (int64_t)(kWriteWarps / 2) + (warp >> 1);
+    if (item >= n) return;
+    const int64_t slot = slots[item];
+    if (slot < 0) return;
+    const uint4* src = (warp & 1) ? v : k;
+    uint4* dst = (warp & 1) ? v_cache : k_cache;
+    src += item * row_vecs;
+    dst += slot * row_vecs;
+    for (int64_t e = lane; e < row_vecs; e += 32) dst[e] = ld_nc_v4(src + e);
+}
+
+// One CTA per (pair, layer); its threads stride over the K and V blocks.
+struct CopyPtrs {
+    uint4* k[PA_MAX_LAYERS_INTERNAL];
+    uint4* v[PA_MAX_LAYERS_INTERNAL];
+};
+
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(const CopyPtrs ptrs, const int64_t* __restrict__ pairs, int64_t block_vecs) {
+    const int64_t pair = blockIdx.x;
+    const int layer = blockIdx.y;
+    const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+    const uint4* ks = ptrs.k[layer] + src * block_vecs;
+    const uint4* vs = ptrs.v[layer] + src * block_vecs;
+    uint4* kd = ptrs.k[layer] + dst * block_vecs;
+    uint4* vd = ptrs.v[layer] + dst * block_vecs;
+    for (int64_t e = threadIdx.x; e < block_vecs; e += blockDim.x) {
+        const uint4 a = ld_nc_v4(ks + e);
+        const uint4 b = ld_nc_v4(vs + e);
+        kd[e] = a;
+        vd[e] = b;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_idx,
+                                const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
+                                cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = (n + threads - 1) / threads;
+    slot_mapping_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), threads, 0, stream>>>(
+        block_tables, max_blocks, seq_idx, positions, n, block_size, slot_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_cache,
+                            void* v_cache, int64_t row_bytes, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int64_t per_cta = kWriteWarps / 2;
+    const int64_t blocks = (n + per_cta - 1) / per_cta;
+    write_kv_kernel<<<(unsigned)blocks, kWriteWarps * 32, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n, static_cast<uint4*>(k_cache),
+        static_cast<uint4*>(v_cache), row_bytes / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                               const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
+                               cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    CopyPtrs ptrs;
+    for (int l = 0; l < num_layers; ++l) {
+        ptrs.k[l] = static_cast<uint4*>(k_caches[l]);
+        ptrs.v[l] = static_cast<uint4*>(v_caches[l]);
+    }
+    dim3 grid((unsigned)num_pairs, (unsigned)num_layers);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(ptrs, block_pairs, block_bytes / 16);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,631 @@
+// pa_decode_tc.cu -- paged decode attention on the tensor cores (bf16/f16).
+//
+// What it computes is the num_new = 1 case of the handbook's paged_attention
+// ("分页 KV Cache", §分页注意力): for sequence s and query head h with KV
+// head kv = h / G (G = Hq / Hkv), out = softmax(scale * q K^T) V over the L
+// keys of the sequence, K and V read through its block table.
+//
+// How, on sm_103a:
+//  * Work unit = (sequence, KV head); its keys are the sequence's logical
+//    blocks.  All units' blocks form one flat list of
+//    Hkv * sum(ceil(L/16)) blocks, cut into equal contiguous ranges, one per
+//    warp of a persistent grid, so every warp streams the same number of
+//    bytes whatever the length mix.  A unit cut between warps leaves partial
+//    softmax states (m, l, unnormalised o) that a second, tiny kernel merges
+//    by their log-sum-exp ("aiqz.cc PagedAttention", §工程实现要点: blocks
+//    computed apart and merged by the online-softmax rule).  The cut depends
+//    only on the lengths, never on physical block ids.
+//  * Each warp runs its own R-deep ring of shared-memory stages.  One lane
+//    issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle) of the
+//    K and V tiles of a 16-token block -- rows of one KV head, gathered
+//    through the block table -- completing on an mbarrier; block-table
+//    entries for the next 64 blocks sit in registers.
+//  * The G query heads of the unit are packed as the N side of
+//    mma.m16n8k16 (padded to 8 or 16): S^T = K Q^T with the 16 tokens as M,
+//    so each K/V byte is read once for the whole group; the fp32 scores get
+//    an exp2-domain online softmax; P^T is moved into B-fragment layout with
+//    movmatrix and O^T += V^T P^T accumulates in fp32 registers.
+//  * Tokens past L in a sequence's last block are masked (scores to -inf,
+//    V operand lanes to zero) so whatever the unused slots hold never leaks.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+#include <string>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ unsigned int g_decode_status;
+
+constexpr int BS = 16;  // tokens per block (one m-tile)
+
+struct TcParams {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    int32_t max_blocks;
+    const int32_t* context_lens;
+    int32_t num_seqs;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t group;
+    float scale_log2;
+    int32_t* ws_prefix;  // [num_seqs + 1] block-count prefix, written by CTA 0
+    float* ws_part;      // [total_warps][2][group][HD + 2] partial states
+};
+
+template <int HD>
+struct Geo {
+    static constexpr int CH = HD * 2 / 128;   // 128-byte chunks in one head's row
+    static constexpr int TILE = BS * HD * 2;  // bytes of a K (or V) tile
+    static constexpr int STAGE = 2 * TILE;    // K tile then V tile
+    static constexpr int KS = HD / 16;        // k-steps of K Q^T == m-tiles of V^T P^T
+};
+
+// Warps per CTA and stages per warp for each head_dim.
+template <int HD> struct Pipe;
+template <> struct Pipe<64> { static constexpr int NW = 4, R = 6; };
+template <> struct Pipe<128> { static constexpr int NW = 4, R = 3; };
+template <> struct Pipe<256> { static constexpr int NW = 2, R = 3; };
+
+template <int HD>
+constexpr size_t smem_bytes(int num_seqs) {
+    return 1024 /* alignment slack */ + (size_t)Pipe<HD>::NW * Pipe<HD>::R * (Geo<HD>::STAGE + 8) +
+           (size_t)(num_seqs + 1) * 4;
+}
+
+template <typename T, int HD, int NT>
+__global__ void __launch_bounds__(Pipe<HD>::NW * 32)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const TcParams p) {
+    using Gm = Geo<HD>;
+    constexpr int NW = Pipe<HD>::NW, R = Pipe<HD>::R, KS = Gm::KS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * Gm::STAGE);
+    int32_t* prefix = reinterpret_cast<int32_t*>(bars + NW * R);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+
+    // ---- blocks per sequence and their exclusive prefix
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+        const int L = p.context_lens[s];
+        prefix[s + 1] = L > 0 ? (L + BS - 1) / BS : 0;
+    }
+    if (threadIdx.x == 0) prefix[0] = 0;
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (S + 31) / 32;
+        const int lo = 1 + lane * per, hi = min(S + 1, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += prefix[i];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - sum;
+        for (int i = lo; i < hi; ++i) {
+            run += prefix[i];
+            prefix[i] = run;
+        }
+    }
+    __syncthreads();
+
+    const int64_t W = (int64_t)prefix[S] * Hkv;
+    if (blockIdx.x == 0)
+        for (int s = threadIdx.x; s <= S; s += blockDim.x) p.ws_prefix[s] = prefix[s];
+    // sequences with no context get a zero row
+    for (int s = blockIdx.x; s < S; s += gridDim.x) {
+        if (prefix[s + 1] == prefix[s]) {
+            T* o = static_cast<T*>(p.out) + (int64_t)s * p.num_heads * HD;
+            for (int e = threadIdx.x; e < p.num_heads * HD; e += blockDim.x) o[e] = Elt<T>::from_f(0.f);
+        }
+    }
+
+    const int64_t TW = (int64_t)gridDim.x * NW;
+    const int64_t gw = (int64_t)blockIdx.x * NW + warp;
+    const int64_t f0 = gw * W / TW, f1 = (gw + 1) * W / TW;
+    const int n = (int)(f1 - f0);
+    if (n <= 0) return;  // no block-wide barrier follows
+
+    uint64_t* wbar = bars + warp * R;
+    uint8_t* wst = base + (size_t)warp * R * Gm::STAGE;
+    if (lane == 0) {
+        for (int r = 0; r < R; ++r) mbar_init(&wbar[r], 1);
+        mbar_fence_init();
+    }
+    __syncwarp();
+
+    // flat position -> (sequence, KV head, logical block)
+    auto locate = [&](int64_t f, int& s_out, int& h_out, int& b_out) {
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)prefix[mid] * Hkv <= f) lo = mid;
+            else hi = mid - 1;
+        }
+        const int nb = prefix[lo + 1] - prefix[lo];
+        const int64_t rem = f - (int64_t)prefix[lo] * Hkv;
+        s_out = lo;
+        h_out = (int)(rem / nb);
+        b_out = (int)(rem - (int64_t)h_out * nb);
+    };
+    auto table_entry = [&](int64_t rel) -> int32_t {
+        if (rel >= n) return 0;
+        int s, h, b;
+        locate(f0 + rel, s, h, b);
+        return p.block_tables[(int64_t)s * p.max_blocks + b];
+    };
+
+    // ---- producer side: issue cursor, table window, TMA
+    const uint64_t pol = l2_policy_evict_first();
+    int32_t tbl_cur = table_entry(lane), tbl_next = table_entry(32 + lane);
+    int win = 0, ip = 0;
+    int is_, ih, ib;
+    locate(f0, is_, ih, ib);
+    auto issue_next = [&]() {
+        const int w = ip >> 5;
+        if (w != win) {
+            tbl_cur = tbl_next;
+            tbl_next = table_entry((int64_t)(w + 1) * 32 + lane);
+            win = w;
+        }
+        const int32_t phys = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
+        const int slot = ip % R;
+        if (lane == 0) {
+            uint8_t* dst = wst + (size_t)slot * Gm::STAGE;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE);
+            const int row = phys * BS;
+#pragma unroll
+            for (int c = 0; c < Gm::CH; ++c) {
+                tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+            }
+        }
+        ++ip;
+        if (++ib == prefix[is_ + 1] - prefix[is_]) {
+            ib = 0;
+            if (++ih == Hkv) {
+                ih = 0;
+                do {
+                    ++is_;
+                } while (is_ < S && prefix[is_ + 1] == prefix[is_]);
+            }
+        }
+    };
+    for (int r = 0; r < R && r < n; ++r) issue_next();
+
+    // ---- consumer side
+    const int g = lane >> 2, c4 = lane & 3;
+    // ldmatrix lane roles: matrix mi = lane / 8, row ri = lane % 8
+    const int mi = lane >> 3, ri = lane & 7;
+    // K (non-transposed A operand): token = (mi & 1) * 8 + ri, dims + (mi >> 1) * 8
+    const int k_tok = (mi & 1) * 8 + ri, k_dof = (mi >> 1) * 8;
+    // V^T (transposed A operand): token = (mi >> 1) * 8 + ri, dims + (mi & 1) * 8
+    const int v_tok = (mi >> 1) * 8 + ri, v_dof = (mi & 1) * 8;
+    auto swz = [](int tok, int dstart) -> uint32_t {
+        const int c = dstart >> 6, j = (dstart & 63) >> 3;
+        return (uint32_t)(c * BS * 128 + tok * 128 + ((j ^ (tok & 7)) << 4));
+    };
+
+    float acc[KS][NT][4];
+    float mrow[NT][2], lrow[NT][2];
+    uint32_t qb[KS][NT][2];
+
+    int cs, ch, cb;
+    locate(f0, cs, ch, cb);
+    int seg_b0 = cb, Lcur = p.context_lens[cs];
+    bool first_seg = true;
+    const T* qbase = static_cast<const T*>(p.q);
+
+    auto begin_unit = [&]() {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const int hh = nt * 8 + g;
+                if (hh < G) {
+                    const T* qp = qbase + (((int64_t)cs * p.num_heads + ch * G + hh) * HD + kk * 16 + 2 * c4);
+                    qb[kk][nt][0] = *reinterpret_cast<const uint32_t*>(qp);
+                    qb[kk][nt][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+                } else {
+                    qb[kk][nt][0] = qb[kk][nt][1] = 0u;
+                }
+            }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mrow[nt][0] = mrow[nt][1] = -INFINITY;
+            lrow[nt][0] = lrow[nt][1] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
+        }
+    };
+
+    auto finalize = [&](int bend, int nb) {
+        float lt[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float l = lrow[nt][e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                lt[nt][e] = l;
+            }
+        const bool complete = (seg_b0 == 0 && bend == nb);
+        if (complete) {
+            T* out = static_cast<T*>(p.out) + ((int64_t)cs * p.num_heads + (int64_t)ch * G) * HD;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int hh = nt * 8 + 2 * c4 + e;
+                    if (hh < G) {
+                        const float inv = 1.f / lt[nt][e];
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            out[hh * HD + mt * 16 + g] = Elt<T>::from_f(acc[mt][nt][e] * inv);
+                            out[hh * HD + mt * 16 + g + 8] = Elt<T>::from_f(acc[mt][nt][2 + e] * inv);
+                        }
+                    }
+                }
+        } else {
+            const int slot = first_seg ? 0 : 1;
+            float* rec = p.ws_part + ((gw * 2 + slot) * G) * (int64_t)(HD + 2);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int hh = nt * 8 + 2 * c4 + e;
+                    if (hh < G) {
+                        float* r = rec + hh * (HD + 2);
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            r[mt * 16 + g] = acc[mt][nt][e];
+                            r[mt * 16 + g + 8] = acc[mt][nt][2 + e];
+                        }
+                        if (g == 0) {
+                            r[HD] = mrow[nt][e];
+                            r[HD + 1] = lt[nt][e];
+                        }
+                    }
+                }
+        }
+    };
+
+    begin_unit();
+    const uint32_t st0 = smem_u32(wst);
+    for (int i = 0; i < n; ++i) {
+        const int slot = i % R;
+        if (!mbar_wait_bounded(&wbar[slot], (uint32_t)(i / R) & 1u, kMaxPolls)) {
+            if (lane == 0) atomicOr(&g_decode_status, kStatusTimeout);
+            for (int j = i + 1; j < ip; ++j) mbar_wait_bounded(&wbar[j % R], (uint32_t)(j / R) & 1u, kMaxPolls);
+            return;
+        }
+        const uint32_t kt = st0 + (uint32_t)slot * Gm::STAGE, vt = kt + Gm::TILE;
+        const int valid = min(BS, Lcur - cb * BS);
+
+        // S^T = K Q^T : 16 tokens x (8 NT) heads, fp32
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kt + swz(k_tok, kk * 16 + k_dof), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+        }
+
+        // online softmax over this block (exp2 domain)
+        const bool ok0 = g < valid, ok1 = g + 8 < valid;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float x0 = ok0 ? sc[nt][0] * p.scale_log2 : -INFINITY;
+            const float x1 = ok0 ? sc[nt][1] * p.scale_log2 : -INFINITY;
+            const float x2 = ok1 ? sc[nt][2] * p.scale_log2 : -INFINITY;
+            const float x3 = ok1 ? sc[nt][3] * p.scale_log2 : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(mrow[nt][0], mx0), mn1 = fmaxf(mrow[nt][1], mx1);
+            const float al0 = fast_exp2(mrow[nt][0] - mn0), al1 = fast_exp2(mrow[nt][1] - mn1);
+            mrow[nt][0] = mn0;
+            mrow[nt][1] = mn1;
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            lrow[nt][0] = fmaf(lrow[nt][0], al0, p0 + p2);
+            lrow[nt][1] = fmaf(lrow[nt][1], al1, p1 + p3);
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                acc[mt][nt][0] *= al0;
+                acc[mt][nt][1] *= al1;
+                acc[mt][nt][2] *= al0;
+                acc[mt][nt][3] *= al1;
+            }
+            pb[nt][0] = movm_t(pack2<T>(p0, p1));
+            pb[nt][1] = movm_t(pack2<T>(p2, p3));
+        }
+
+        // O^T += V^T P^T
+        uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+        if (valid < BS) {
+            m01 = (2 * c4 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 1 < valid ? 0xffff0000u : 0u);
+            m23 = (2 * c4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 9 < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vt + swz(v_tok, mt * 16 + v_dof), a0, a1, a2, a3);
+            a0 &= m01;
+            a1 &= m01;
+            a2 &= m23;
+            a3 &= m23;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+        __syncwarp();
+        if (ip < n) issue_next();
+
+        const int nb = prefix[cs + 1] - prefix[cs];
+        ++cb;
+        const bool unit_done = (cb == nb);
+        if (unit_done || i == n - 1) {
+            finalize(cb, nb);
+            first_seg = false;
+            if (unit_done && i < n - 1) {
+                cb = 0;
+                seg_b0 = 0;
+                if (++ch == Hkv) {
+                    ch = 0;
+                    do {
+                        ++cs;
+                    } while (cs < S && prefix[cs + 1] == prefix[cs]);
+                    Lcur = p.context_lens[cs];
+                }
+                begin_unit();
+            }
+        }
+    }
+}
+
+// Merge the partial states of every unit that was cut between warps.
+template <typename T, int HD>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const TcParams p, int64_t total_warps) {
+    pdl_wait_primary();
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+    const int P0 = p.ws_prefix[s], nb = p.ws_prefix[s + 1] - P0;
+    if (nb == 0) return;
+    const int64_t W = (int64_t)p.ws_prefix[S] * Hkv;
+    const int64_t U0 = (int64_t)P0 * Hkv + (int64_t)h * nb, U1 = U0 + nb;
+    auto start = [&](int64_t w) { return w * W / total_warps; };
+    auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / W; };
+    const int64_t w0 = warp_of(U0), w1 = warp_of(U1 - 1);
+    if (w0 == w1) return;  // the unit was finished by one warp
+    const int64_t st0 = start(w0);
+    T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + (int64_t)h * G) * HD;
+    for (int j = 0; j < G; ++j) {
+        float M = -INFINITY;
+        for (int64_t w = w0; w <= w1; ++w) {
+            if (start(w) == start(w + 1)) continue;
+            const int slot = (w == w0 && U0 > st0) ? 1 : 0;
+            const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
+            M = fmaxf(M, r[HD]);
+        }
+        float L = 0.f;
+        for (int64_t w = w0; w <= w1; ++w) {
+            if (start(w) == start(w + 1)) continue;
+            const int slot = (w == w0 && U0 > st0) ? 1 : 0;
+            const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
+            L += exp2f(r[HD] - M) * r[HD + 1];
+        }
+        const float inv = 1.f / L;
+        for (int d = threadIdx.x; d < HD; d += blockDim.x) {
+            float o = 0.f;
+            for (int64_t w = w0; w <= w1; ++w) {
+                if (start(w) == start(w + 1)) continue;
+                const int slot = (w == w0 && U0 > st0) ? 1 : 0;
+                const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
+                o += exp2f(r[HD] - M) * r[d];
+            }
+            out[j * HD + d] = Elt<T>::from_f(o * inv);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// The cache as a 3-D tensor: 64 elements (128 bytes) x (Hkv * CH) 128-byte
+// chunks of a token row x num_blocks * 16 token rows; one box = one chunk of
+// one KV head over the 16 rows of a block.
+bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, int num_blocks, int num_kv_heads, int head_dim,
+                 std::string* err) {
+    auto fn = encode_fn();
+    if (!fn) {
+        *err = "cuTensorMapEncodeTiled is not available from the driver";
+        return false;
+    }
+    const int ch = head_dim * 2 / 128;
+    cuuint64_t dims[3] = {64, (cuuint64_t)num_kv_heads * ch, (cuuint64_t)num_blocks * BS};
+    cuuint64_t strides[2] = {128, (cuuint64_t)num_kv_heads * head_dim * 2};
+    cuuint32_t box[3] = {64, 1, BS};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                    const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+        return false;
+    }
+    return true;
+}
+
+template <typename T, int HD, int NT>
+const void* kernel_ptr() {
+    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT>);
+}
+
+template <int HD>
+int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t max_context, int64_t override_ctas) {
+    if (override_ctas > 0) return (int)override_ctas;
+    int dev = 0, sms = 0, occ = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const size_t smem = smem_bytes<HD>(num_seqs);
+    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, Pipe<HD>::NW * 32, smem);
+    if (occ < 1) occ = 1;
+    int64_t grid = (int64_t)sms * occ;
+    // at least two blocks per warp on average when every context is max_context long
+    const int64_t wmax = (int64_t)num_seqs * num_kv_heads * ((max_context + BS - 1) / BS);
+    const int64_t cap = (wmax + 2 * Pipe<HD>::NW - 1) / (2 * Pipe<HD>::NW);
+    if (grid > cap) grid = cap;
+    return (int)(grid < 1 ? 1 : grid);
+}
+
+template <typename T, int HD, int NT>
+cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* workspace, std::string* err,
+                         cudaStream_t stream) {
+    CUtensorMap tmK, tmV;
+    if (!make_kv_map(&tmK, a.k_cache, a.dtype, num_blocks, a.num_kv_heads, HD, err) ||
+        !make_kv_map(&tmV, a.v_cache, a.dtype, num_blocks, a.num_kv_heads, HD, err))
+        return cudaErrorInvalidValue;
+    TcParams p;
+    p.out = a.out;
+    p.q = a.q;
+    p.block_tables = a.block_tables;
+    p.max_blocks = a.max_blocks;
+    p.context_lens = a.seq_lens;
+    p.num_seqs = a.num_seqs;
+    p.num_heads = a.num_heads;
+    p.num_kv_heads = a.num_kv_heads;
+    p.group = a.num_heads / a.num_kv_heads;
+    p.scale_log2 = a.scale * 1.4426950408889634f;
+    const size_t prefix_bytes = ((size_t)(a.num_seqs + 1) * 4 + 255) & ~(size_t)255;
+    p.ws_prefix = static_cast<int32_t*>(workspace);
+    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + prefix_bytes);
+
+    const void* kfn = kernel_ptr<T, HD, NT>();
+    const size_t smem = smem_bytes<HD>(a.num_seqs);
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    decode_tc_kernel<T, HD, NT><<<grid, Pipe<HD>::NW * 32, smem, stream>>>(tmK, tmV, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int64_t total_warps = (int64_t)grid * Pipe<HD>::NW;
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD>, p, total_warps);
+}
+
+template <typename T>
+cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* ws, std::string* err,
+                         cudaStream_t st) {
+    const int G = a.num_heads / a.num_kv_heads;
+    const bool two = G > 8;
+    switch (a.head_dim) {
+        case 64: return two ? launch_typed<T, 64, 2>(a, num_blocks, grid, ws, err, st)
+                            : launch_typed<T, 64, 1>(a, num_blocks, grid, ws, err, st);
+        case 128: return two ? launch_typed<T, 128, 2>(a, num_blocks, grid, ws, err, st)
+                             : launch_typed<T, 128, 1>(a, num_blocks, grid, ws, err, st);
+        default: return two ? launch_typed<T, 256, 2>(a, num_blocks, grid, ws, err, st)
+                            : launch_typed<T, 256, 1>(a, num_blocks, grid, ws, err, st);
+    }
+}
+
+}  // namespace
+
+bool decode_tc_supported(int dtype, int head_dim, int block_size, int group) {
+    return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
+           block_size == BS && group >= 1 && group <= 16;
+}
+
+int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override) {
+    (void)block_size;
+    const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
+    const bool two = group > 8;
+    const bool bf = dtype == 1;
+#define PA_KFN(HD)                                                                                      \
+    (bf ? (two ? kernel_ptr<__nv_bfloat16, HD, 2>() : kernel_ptr<__nv_bfloat16, HD, 1>())              \
+        : (two ? kernel_ptr<__half, HD, 2>() : kernel_ptr<__half, HD, 1>()))
+    switch (head_dim) {
+        case 64: return grid_for<64>(PA_KFN(64), s, num_kv_heads, max_context, ctas_override);
+        case 128: return grid_for<128>(PA_KFN(128), s, num_kv_heads, max_context, ctas_override);
+        default: return grid_for<256>(PA_KFN(256), s, num_kv_heads, max_context, ctas_override);
+    }
+#undef PA_KFN
+}
+
+size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas) {
+    (void)num_kv_heads;
+    const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
+    const int nw = head_dim == 256 ? Pipe<256>::NW : (head_dim == 128 ? Pipe<128>::NW : Pipe<64>::NW);
+    const size_t prefix_bytes = ((size_t)(s + 1) * 4 + 255) & ~(size_t)255;
+    return prefix_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 2) * sizeof(float);
+}
+
+cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
+                             std::string* err, cudaStream_t stream) {
+    if (a.num_seqs == 0) return cudaSuccess;
+    return a.dtype == 1 ? launch_dtype<__nv_bfloat16>(a, num_blocks, grid_ctas, workspace, err, stream)
+                        : launch_dtype<__half>(a, num_blocks, grid_ctas, workspace, err, stream);
+}
+
+uint32_t decode_tc_status(bool clear) {
+    unsigned int v = 0;
+    cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(v));
+    if (clear) {
+        const unsigned int z = 0;
+        cudaMemcpyToSymbol(g_decode_status, &z, sizeof(z));
+    }
+    return v;
+}
+
+}  // namespace pa

@@ -1,0 +1,72 @@
+// pa_internal.h -- host-side declarations shared by the library's translation
+// units (launchers called by the C ABI in pa_api.cu).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace pa {
+
+// Element size of a pa_dtype (PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2).
+inline int elt_size(int dtype) { return dtype == 0 ? 4 : 2; }
+
+// Upper limit of sequences one tensor-core decode launch handles (its
+// per-sequence block-count prefix lives in shared memory); the C ABI splits
+// larger batches into launches of at most this many sequences.
+constexpr int kDecodeMaxSeqsPerLaunch = 4096;
+
+// Most layers one pa_copy_blocks call takes (their pointers travel in the
+// kernel's parameter block).  Equal to PA_MAX_LAYERS of pa.h.
+#define PA_MAX_LAYERS_INTERNAL 128
+
+// Number of polls a bounded mbarrier wait makes before giving up.
+constexpr uint32_t kMaxPolls = 1u << 24;
+
+// ---- copy kernels (pa_copy.cu)
+cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_idx,
+                                const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
+                                cudaStream_t stream);
+cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_cache,
+                            void* v_cache, int64_t row_bytes, cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                               const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
+                               cudaStream_t stream);
+
+// ---- CUDA-core attention (pa_attn_simt.cu): any dtype, head_dim <= 256.
+// cu_seqlens_q == nullptr means one query per sequence (row i = sequence i).
+struct AttnArgs {
+    void* out;
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_tables;
+    int32_t max_blocks;
+    const int32_t* seq_lens;
+    const int32_t* cu_seqlens_q;
+    int32_t num_seqs;
+    int32_t total_q;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t block_size;
+    float scale;
+    int causal;
+    int dtype;
+};
+bool attn_simt_supported(int dtype, int head_dim);
+cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
+
+// ---- tensor-core decode (pa_decode_tc.cu)
+bool decode_tc_supported(int dtype, int head_dim, int block_size, int group);
+// Grid size (CTAs) the launch will use for this problem on the current device.
+int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override);
+size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas);
+cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
+                             std::string* err, cudaStream_t stream);
+uint32_t decode_tc_status(bool clear);
+
+}  // namespace pa

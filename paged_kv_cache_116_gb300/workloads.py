@@ -94,14 +94,16 @@ class Workload:
         return int(self.seq_lens.astype(np.int64).sum()) * self.num_kv_heads * self.head_dim * 2 * self.elt
 
 
-def _gen(seed: int) -> torch.Generator:
-    g = torch.Generator(device="cpu")
+def _gen(seed: int, device="cpu") -> torch.Generator:
+    g = torch.Generator(device=device)
     g.manual_seed(seed)
     return g
 
 
 def _normal(g, shape, std: float, dtype: str) -> torch.Tensor:
-    t = torch.randn(*shape, generator=g, dtype=torch.float32)
+    """N(0, std^2) values drawn in fp32 on the generator's device, then
+    rounded to the element type."""
+    t = torch.randn(*shape, generator=g, dtype=torch.float32, device=g.device)
     if std != 1.0:
         t.mul_(std)
     return t.to(TORCH_DTYPES[dtype])
@@ -139,8 +141,11 @@ def _rows_for(lens_before) -> tuple[np.ndarray, np.ndarray]:
 
 
 def decode_workload(name, dtype, block_size, num_heads, num_kv_heads, head_dim, lens, *, std=1.0,
-                    num_blocks=None, slack=0.10, seed=0, scale=None, tables=None, notes="") -> Workload:
-    """One new token per sequence at position L-1; positions 0..L-2 cached."""
+                    num_blocks=None, slack=0.10, seed=0, scale=None, tables=None, notes="",
+                    device="cpu") -> Workload:
+    """One new token per sequence at position L-1; positions 0..L-2 cached.
+    Values are drawn by torch's seeded generator on `device` (the CPU and
+    CUDA generators give different, each reproducible, streams)."""
     lens = np.asarray(lens, dtype=np.int32)
     S = lens.shape[0]
     need = sum(_blocks_for(int(L), block_size) for L in lens)
@@ -148,7 +153,7 @@ def decode_workload(name, dtype, block_size, num_heads, num_kv_heads, head_dim, 
         num_blocks = int(math.ceil(need * (1.0 + slack)))
     if tables is None:
         tables = _shuffled_tables(lens, block_size, num_blocks, seed)
-    g = _gen(seed + 1)
+    g = _gen(seed + 1, device)
     q = _normal(g, (S, num_heads, head_dim), std, dtype)
     pre_seq, pre_pos = _rows_for(lens - 1)
     pre_k = _normal(g, (pre_pos.shape[0], num_kv_heads, head_dim), std, dtype)
@@ -186,17 +191,18 @@ def gqa_batch_lengths(n: int = 64, seed: int = 0) -> np.ndarray:
     return np.array([p + o for p, o in pairs], dtype=np.int32)
 
 
-def gqa_decode_batch(seed: int = 0, num_seqs: int = 64) -> Workload:
+def gqa_decode_batch(seed: int = 0, num_seqs: int = 64, device="cpu") -> Workload:
     """bf16, block_size 16, Hq 32, Hkv 8, head_dim 128, 64 sequences, shuffled
     physical blocks, 10 % slack blocks."""
     return decode_workload("gqa_decode_bf16_64seq", "bf16", 16, 32, 8, 128, gqa_batch_lengths(num_seqs, seed),
-                           seed=seed, notes="L = randint(100,2000)+randint(20,1500), random.seed(0)")
+                           seed=seed, notes="L = randint(100,2000)+randint(20,1500), random.seed(0)",
+                           device=device)
 
 
-def long_context_decode(seed: int = 0, num_seqs: int = 8, context: int = 32768) -> Workload:
+def long_context_decode(seed: int = 0, num_seqs: int = 8, context: int = 32768, device="cpu") -> Workload:
     """bf16, block_size 16, Hq 32, Hkv 8, head_dim 128, 8 sequences of 32768."""
     return decode_workload("long_decode_bf16_8x32k", "bf16", 16, 32, 8, 128, [context] * num_seqs, seed=seed,
-                           notes="8 x 32768 tokens")
+                           notes="8 x 32768 tokens", device=device)
 
 
 def mha_lengths(n: int = 128, seed: int = 0, mean: float = 480.0, sigma: float = 1.0) -> np.ndarray:
@@ -207,11 +213,12 @@ def mha_lengths(n: int = 128, seed: int = 0, mean: float = 480.0, sigma: float =
     return np.clip(np.rint(rng.lognormal(mu, sigma, n)), 1, 2048).astype(np.int32)
 
 
-def mha_decode(seed: int = 0, num_seqs: int = 128) -> Workload:
+def mha_decode(seed: int = 0, num_seqs: int = 128, device="cpu") -> Workload:
     """fp16, block_size 16, Hq = Hkv = 40, head_dim 128, 128 sequences,
     values ~ N(0, 0.5^2)."""
     return decode_workload("mha_decode_fp16_128seq", "f16", 16, 40, 40, 128, mha_lengths(num_seqs, seed), std=0.5,
-                           seed=seed, notes="lognormal lengths sigma=1 mean 480 clip [1,2048]; std 0.5")
+                           seed=seed, notes="lognormal lengths sigma=1 mean 480 clip [1,2048]; std 0.5",
+                           device=device)
 
 
 class _FifoRefPool:
@@ -228,7 +235,7 @@ class _FifoRefPool:
 
 
 def mixed_varlen(seed: int = 0, num_chunks: int = 16, num_groups: int = 60, group_size: int = 4,
-                 prompt_len: int = 300, chunk_range=(64, 1024), cached_range=(0, 1024)) -> Workload:
+                 prompt_len: int = 300, chunk_range=(64, 1024), cached_range=(0, 1024), device="cpu") -> Workload:
     """bf16, block_size 16, Hq 12, Hkv 2, head_dim 128.
 
     Requests 0..num_chunks-1 are prefill chunks: n new tokens ~ U[64, 1024]
@@ -291,7 +298,7 @@ def mixed_varlen(seed: int = 0, num_chunks: int = 16, num_groups: int = 60, grou
     new_seq = np.repeat(np.arange(S, dtype=np.int32), query_lens.astype(np.int64))
     new_pos = np.concatenate([np.arange(int(seq_lens[i] - query_lens[i]), int(seq_lens[i]), dtype=np.int64)
                               for i in range(S)])
-    g = _gen(seed + 1)
+    g = _gen(seed + 1, device)
     N = int(query_lens.sum())
     q = _normal(g, (N, hq, hd), 1.0, dtype)
     pre_k = _normal(g, (pre_pos.shape[0], hkv, hd), 1.0, dtype)
@@ -330,7 +337,8 @@ def _round_robin(seq_lens, bs, num_blocks):
 
 
 def varlen_workload(name, dtype, block_size, num_heads, num_kv_heads, head_dim, seq_lens, query_lens, *,
-                    num_blocks=None, tables=None, std=1.0, seed=0, causal=True, slack=0.10) -> Workload:
+                    num_blocks=None, tables=None, std=1.0, seed=0, causal=True, slack=0.10,
+                    device="cpu") -> Workload:
     """Request i has seq_lens[i] tokens after the step, the last query_lens[i]
     of them new; the earlier ones are cached."""
     seq_lens = np.asarray(seq_lens, np.int32)
@@ -342,7 +350,7 @@ def varlen_workload(name, dtype, block_size, num_heads, num_kv_heads, head_dim, 
         num_blocks = max(1, int(math.ceil(need * (1.0 + slack))))
     if tables is None:
         tables = _shuffled_tables(seq_lens, block_size, num_blocks, seed)
-    g = _gen(seed + 1)
+    g = _gen(seed + 1, device)
     N = int(query_lens.sum())
     cached = seq_lens - query_lens
     pre_seq, pre_pos = _rows_for(cached)

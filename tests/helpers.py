@@ -59,3 +59,38 @@ def within_tol(got, exact, dtype):
     err = np.abs(got - exact)
     bound = ATOL[dtype] + RTOL[dtype] * np.abs(exact)
     return bool(np.all(err <= bound)), float(np.nanmax(err)) if err.size else 0.0
+
+
+def device_caches(w, dev, after_step=True):
+    """Device K/V caches of a workload built through the library itself:
+    NaN everywhere, cached rows via pa_slot_mapping + pa_write_kv on the
+    pre-step tables, then (after_step) pa_copy_blocks and the step's rows."""
+    import torch
+    import paged_kv_cache_116_gb300 as pa
+
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    kc = torch.full(shape, float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=dev)
+    vc = torch.full_like(kc, float("nan"))
+    if w.pre_pos.shape[0]:
+        slots = pa.pa_slot_mapping(torch.from_numpy(w.pre_block_tables).to(dev),
+                                   torch.from_numpy(w.pre_seq_idx).to(dev), torch.from_numpy(w.pre_pos).to(dev),
+                                   w.block_size)
+        pa.pa_write_kv(w.pre_k.to(dev), w.pre_v.to(dev), slots, kc, vc)
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    if after_step:
+        if w.cow_pairs.shape[0]:
+            pa.pa_copy_blocks(kc, vc, torch.from_numpy(w.cow_pairs).to(dev))
+        slots = pa.pa_slot_mapping(bt, torch.from_numpy(w.new_seq_idx).to(dev), torch.from_numpy(w.new_pos).to(dev),
+                                   w.block_size)
+        pa.pa_write_kv(w.new_k.to(dev), w.new_v.to(dev), slots, kc, vc)
+    return kc, vc, bt
+
+
+def raw_bits(t):
+    """Bit patterns of a cache (host numpy, uint32 for fp32 else uint16)."""
+    a = W.raw_numpy(t)
+    return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+def oracle_bits(a):
+    return a.view(np.uint32) if a.dtype == np.float32 else a

@@ -1,0 +1,170 @@
+"""GPU parity of pa_decode against the oracle.
+
+Tolerance: |gpu - exact| <= atol + rtol * |exact| with atol 1e-5 (fp32) /
+1e-2 (bf16, f16) and rtol the output type's unit roundoff (helpers.ATOL /
+RTOL).  Unused cache slots are NaN in every case, so a read outside a
+sequence's context fails the comparison.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_116_gb300 import workloads as W
+
+from helpers import device_caches, oracle_attention, oracle_caches, within_tol
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_116_gb300 as pa
+
+    return pa
+
+
+def run_decode(pa, w, kc, vc, bt, kernel=0, ctas=0, max_context=None):
+    pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, ctas)
+    try:
+        mc = int(w.seq_lens.max()) if max_context is None else max_context
+        lens = torch.from_numpy(w.seq_lens).to(DEV)
+        ws_bytes = pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                               mc, W.TORCH_DTYPES[w.dtype])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype],
+                         device=DEV)
+        pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, mc, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+        return out
+    finally:
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 0)
+        pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, 0)
+
+
+def compare(w, out, exact, rows=None):
+    got = out.double().cpu().numpy()
+    if rows is not None:
+        got, exact = got[rows], exact[rows]
+    ok, err = within_tol(got, exact, w.dtype)
+    assert ok, "max error %.3g beyond tolerance (%s)" % (err, w.name)
+    return err
+
+
+def test_tiny_decode_fp32(pa):
+    w = W.tiny_decode()
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    err = compare(w, run_decode(pa, w, kc, vc, bt), exact)
+    assert err < 1e-5
+
+
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_gqa_decode_batch_full(pa, kernel):
+    w = W.gqa_decode_batch(device=DEV)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel), exact)
+
+
+def test_long_context_decode_sampled(pa):
+    w = W.long_context_decode(device=DEV)
+    kc, vc, bt = device_caches(w, DEV)
+    sel = np.zeros(w.num_seqs, np.uint8)
+    sel[[0, 5]] = 1
+    okc, ovc = oracle_caches(w)
+    exact = oracle_attention(w, okc, ovc, seq_select=sel)
+    compare(w, run_decode(pa, w, kc, vc, bt), exact, rows=np.where(sel)[0])
+
+
+def test_mha_decode_fp16_full(pa):
+    w = W.mha_decode(device=DEV)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    compare(w, run_decode(pa, w, kc, vc, bt), exact)
+
+
+CASES = []
+_r = np.random.default_rng(123)
+for _i in range(14):
+    _hd = int(_r.choice([64, 128, 256]))
+    _g = int(_r.choice([1, 2, 4, 5, 8, 12, 16]))
+    _hkv = int(_r.choice([1, 2, 4]))
+    _dt = str(_r.choice(["bf16", "f16"]))
+    _S = int(_r.integers(1, 9))
+    _lens = _r.integers(1, 3 * 16 + 5, _S).tolist()
+    _lens[0] = int(_r.choice([1, 16, 32, 48]))  # exactly on a block boundary or a single token
+    CASES.append((_dt, _hd, _g, _hkv, _lens, _i))
+
+
+@pytest.mark.parametrize("dt,hd,g,hkv,lens,seed", CASES)
+def test_random_small_decode_both_kernels(pa, dt, hd, g, hkv, lens, seed):
+    w = W.decode_workload("rand", dt, 16, g * hkv, hkv, hd, lens, seed=seed)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    for kernel in (1, 2):
+        for ctas in (0, 1, 3):
+            compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel, ctas=ctas), exact)
+
+
+def test_zero_length_sequence_gives_zero_row(pa):
+    w = W.decode_workload("z", "bf16", 16, 8, 2, 128, [5, 1, 40], seed=9)
+    kc, vc, bt = device_caches(w, DEV)
+    w0 = W.decode_workload("z", "bf16", 16, 8, 2, 128, [5, 1, 40], seed=9)
+    w0.seq_lens = np.array([5, 0, 40], np.int32)
+    exact = oracle_attention(w)
+    for kernel in (1, 2):
+        out = run_decode(pa, w0, kc, vc, bt, kernel=kernel, max_context=40)
+        assert torch.count_nonzero(out[1]).item() == 0
+        compare(w, out[[0, 2]], exact[[0, 2]])
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_permuting_physical_blocks_is_bit_identical(pa, kernel):
+    w = W.decode_workload("perm", "bf16", 16, 32, 8, 128, [700, 33, 1, 250, 16], seed=5)
+    kc, vc, bt = device_caches(w, DEV)
+    base = run_decode(pa, w, kc, vc, bt, kernel=kernel)
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(w.num_blocks)).to(DEV)
+    kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_decode(pa, w, kc2, vc2, bt2, kernel=kernel)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
+def test_split_count_invariance_within_tolerance(pa):
+    w = W.decode_workload("split", "bf16", 16, 32, 8, 128, [2000, 1500, 37], seed=6)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    outs = [run_decode(pa, w, kc, vc, bt, kernel=2, ctas=c) for c in (1, 2, 7, 40, 300)]
+    for o in outs:
+        compare(w, o, exact)
+
+
+def test_check_mode_rejects_bad_tables(pa):
+    w = W.decode_workload("chk", "bf16", 16, 8, 2, 128, [20, 40], seed=1)
+    kc, vc, bt = device_caches(w, DEV)
+    bad = bt.clone()
+    bad[1, 1] = w.num_blocks + 3
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    out = torch.empty(2, 8, 128, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device=DEV)
+    pa.pa_set_check_mode(True)
+    try:
+        with pytest.raises(pa.PAError, match="PA_ERR_INDEX"):
+            pa.pa_decode(out, w.q.to(DEV), kc, vc, bad, lens, 40, w.scale, workspace=ws)
+        with pytest.raises(pa.PAError, match="PA_ERR_INDEX"):
+            pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, 30, w.scale, workspace=ws)  # L > max_context
+        pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, 40, w.scale, workspace=ws)
+    finally:
+        pa.pa_set_check_mode(False)
+    with pytest.raises(pa.PAError, match="PA_ERR_WORKSPACE"):
+        pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, 40, w.scale, workspace=ws[:16])
