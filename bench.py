@@ -38,8 +38,8 @@ METRIC = ("paged decode attention KV GB/s (fraction of HBM peak) and sequences/s
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-rotate", action="store_true", help="one pool copy (for profiling)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, clocks and cpu_baseline")
@@ -138,17 +138,20 @@ def _oracle_batch(num_seqs):
     return w, kc, vc, W.raw_numpy(w.q)
 
 
-def cpu_baseline(total_seqs, sample=8, repeats=3):
+def cpu_baseline(total_seqs, sample=8, budget_s=10.0):
     """The oracle (as it stands) on a bounded sample: the first `sample`
-    sequences of the batch, timed `repeats` times."""
+    sequences of the batch, repeated for about budget_s seconds."""
     import oracle
 
     w, kc, vc, q = _oracle_batch(sample)
     per_tok = w.num_kv_heads * w.head_dim * 2 * w.elt
-    t = time.perf_counter()
-    for _ in range(repeats):
+    repeats, t = 0, time.perf_counter()
+    while True:
         oracle.decode_attention(q, kc, vc, w.block_tables, w.seq_lens, w.scale, w.dtype)
-    el = time.perf_counter() - t
+        repeats += 1
+        el = time.perf_counter() - t
+        if el >= budget_s:
+            break
     return {"value": int(w.seq_lens.sum()) * per_tok * repeats / el / 1e9, "unit": "GB/s",
             "cores": oracle.max_threads(), "kind": "oracle",
             "sample": "first %d of %d sequences (%d tokens) x %d, fp64 C oracle with OpenMP, %.1f s" % (
@@ -237,42 +240,64 @@ def main():
     slot_buf = torch.empty(S, dtype=torch.int64, device=dev)
     ws_bytes = pa.pa_decode_workspace_size(S, hq, hkv, hd, bs, max_ctx, torch.bfloat16)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(i, ev=None):
+    def step(i):
+        """One generation step through the C ABI on the current stream."""
         kc, vc = pools[i % copies]
-        pa.pa_slot_mapping(bt, seq_idx, pos, bs, slot_out=slot_buf, stream=stream)
-        pa.pa_write_kv(new_k, new_v, slot_buf, kc, vc, stream=stream)
-        if ev is not None:
-            ev[0].record(stream)
-        pa.pa_decode(out, q, kc, vc, bt, lens, max_ctx, w.scale, workspace=ws, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
+        st = torch.cuda.current_stream()
+        pa.pa_slot_mapping(bt, seq_idx, pos, bs, slot_out=slot_buf, stream=st)
+        pa.pa_write_kv(new_k, new_v, slot_buf, kc, vc, stream=st)
+        pa.pa_decode(out, q, kc, vc, bt, lens, max_ctx, w.scale, workspace=ws, stream=st)
 
-    launches_per_step = 4  # slot mapping, write, decode, split merge
+    def decode_only(i):
+        kc, vc = pools[i % copies]
+        pa.pa_decode(out, q, kc, vc, bt, lens, max_ctx, w.scale, workspace=ws, stream=torch.cuda.current_stream())
+
+    launches_per_step = 3  # slot mapping, write, decode
 
     for i in range(max(args.warmup, 3)):
         step(i)
     torch.cuda.synchronize()
 
+    # The step is captured once per pool copy into CUDA graphs (what a serving
+    # loop replays); the same C-ABI calls run eagerly give `eager`.
+    def capture(fn):
+        gs = []
+        for c in range(copies):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, capture_error_mode="thread_local"):
+                fn(c)
+            gs.append(g)
+        return gs
+
+    step_graphs = capture(step)
+    dec_graphs = capture(decode_only)
+    for i in range(max(args.warmup, 3)):
+        step_graphs[i % copies].replay()
+        dec_graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    def timed(fn_i):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        a.record()
+        for i in range(args.steps):
+            fn_i(i)
+        b.record()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        return a.elapsed_time(b)
+
     clocks = Clocks()
     if rank == 0 and not args.no_extras:
         clocks.start()
-    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0.record(stream)
-    for i in range(args.steps):
-        step(i, dec_ev[i])
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    ms = t0.elapsed_time(t1)
-    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+        time.sleep(0.5)
+    ms = timed(lambda i: step_graphs[i % copies].replay())
     clk = clocks.stop() if rank == 0 and not args.no_extras else None
+    dec_ms = timed(lambda i: dec_graphs[i % copies].replay()) / args.steps
+    eager_ms = timed(step) / args.steps
 
     if world > 1:
         t = torch.tensor([ms], device=dev)
@@ -282,7 +307,9 @@ def main():
     value = kv_bytes * world * args.steps / (ms / 1e3) / 1e9
     seq_per_s = S * world * args.steps / (ms / 1e3)
 
-    # e2e: the same step through the public API from pinned host buffers
+    # e2e: each step's inputs from pinned host memory, the step, the output
+    # back to pinned host memory -- all inside the timed region (captured as
+    # one graph per pool copy, like the device-only step)
     e2e = None
     if not args.no_extras:
         h_q = q.cpu().pin_memory()
@@ -298,35 +325,36 @@ def main():
 
         def e2e_step(i):
             kc, vc = pools[i % copies]
+            st = torch.cuda.current_stream()
             for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_lens, h_lens), (d_seq, h_seq),
                          (d_pos, h_pos)):
                 d.copy_(h, non_blocking=True)
-            pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=stream)
-            pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=stream)
-            pa.pa_decode(out, d_q, kc, vc, d_bt, d_lens, max_ctx, w.scale, workspace=ws, stream=stream)
+            pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=st)
+            pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=st)
+            pa.pa_decode(out, d_q, kc, vc, d_bt, d_lens, max_ctx, w.scale, workspace=ws, stream=st)
             h_out.copy_(out, non_blocking=True)
 
         for i in range(3):
             e2e_step(i)
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for i in range(args.steps):
-            e2e_step(i)
-        b.record(stream)
+        e2e_graphs = capture(e2e_step)
+        for i in range(3):
+            e2e_graphs[i % copies].replay()
         torch.cuda.synchronize()
-        e_ms = a.elapsed_time(b)
+        e_ms = timed(lambda i: e2e_graphs[i % copies].replay())
         if world > 1:
             t = torch.tensor([e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
         e2e = {"value": kv_bytes * world * args.steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
+               "how": "pinned-host inputs -> H2D copies -> pa_slot_mapping/pa_write_kv/pa_decode -> D2H output, "
+                      "replayed as a CUDA graph per step"}
 
     peaks, kind = measured_peaks()
-    dec_avg = sum(dec_ms) / len(dec_ms)
+    dec_avg = dec_ms
     achieved = alg_bytes / (dec_avg / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": "decode_tc_kernel + decode_merge_kernel (one pa_decode call)",
+    roof = {"bound": "hbm", "kernel": "decode_tc_kernel (one pa_decode call, split merge included)",
             "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
             "peak_kind": kind, "traffic": traffic_record("pa_decode_tc.cu"), "algorithmic_bytes": alg_bytes,
             "decode_us": dec_avg * 1e3}
@@ -340,8 +368,10 @@ def main():
                        "block_size": bs, "num_blocks": w.num_blocks, "total_context": int(w.seq_lens.sum()),
                        "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2: %d pool copies of %.2f GB "
                        "alternate between steps" % (copies, 2 * pools[0][0].numel() * 2 / 1e9),
-                       "step": "pa_slot_mapping + pa_write_kv + pa_decode", "seed": 0},
+                       "step": "pa_slot_mapping + pa_write_kv + pa_decode, replayed as a CUDA graph",
+                       "seed": 0},
             "seq_per_s": seq_per_s,
+            "eager_ms_per_step": eager_ms,
             "roofline": roof,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,

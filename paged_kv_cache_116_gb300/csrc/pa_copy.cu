@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -45,6 +46,9 @@ constexpr int kWriteWarps = 8;
 __global__ void __launch_bounds__(kWriteWarps * 32)
     write_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
                     int64_t n, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t row_vecs) {
+    // a dependent kernel (the decode reading these rows) may be scheduled
+    // now; it waits for this grid to finish before it reads anything
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t item = blockIdx.x * (int64_t)(kWriteWarps / 2) + (warp >> 1);
     if (item >= n) return;

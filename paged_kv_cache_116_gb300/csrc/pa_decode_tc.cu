@@ -11,10 +11,12 @@
 //    Hkv * sum(ceil(L/16)) blocks, cut into equal contiguous ranges, one per
 //    warp of a persistent grid, so every warp streams the same number of
 //    bytes whatever the length mix.  A unit cut between warps leaves partial
-//    softmax states (m, l, unnormalised o) that a second, tiny kernel merges
-//    by their log-sum-exp ("aiqz.cc PagedAttention", §工程实现要点: blocks
-//    computed apart and merged by the online-softmax rule).  The cut depends
-//    only on the lengths, never on physical block ids.
+//    softmax states (m, l, unnormalised o) in the workspace; the last of the
+//    unit's warps to finish (an epoch-tagged atomic count per unit, so the
+//    workspace never needs clearing) merges them by their log-sum-exp, in
+//    a fixed order ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
+//    apart and merged by the online-softmax rule).  The cut depends only on
+//    the lengths, never on physical block ids.
 //  * Each warp runs its own R-deep ring of shared-memory stages.  One lane
 //    issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle) of the
 //    K and V tiles of a 16-token block -- rows of one KV head, gathered
@@ -33,6 +35,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -57,8 +60,9 @@ struct TcParams {
     int32_t num_kv_heads;
     int32_t group;
     float scale_log2;
-    int32_t* ws_prefix;  // [num_seqs + 1] block-count prefix, written by CTA 0
-    float* ws_part;      // [total_warps][2][group][HD + 2] partial states
+    unsigned long long* ws_cnt;  // [num_seqs * num_kv_heads] (epoch << 16) | partials done
+    float* ws_part;              // [total_warps][2] records of group * (HD + 4) floats
+    unsigned long long epoch;    // this launch's tag, < 2^48, never reused by the process
 };
 
 template <int HD>
@@ -95,7 +99,10 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
 
-    pdl_launch_dependents();
+    // With programmatic dependent launch this grid may start while the
+    // previous kernel on the stream (e.g. the K/V write) is still running;
+    // every input is read after this wait.
+    pdl_wait_primary();
     if (threadIdx.x == 0) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
@@ -128,8 +135,6 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
     __syncthreads();
 
     const int64_t W = (int64_t)prefix[S] * Hkv;
-    if (blockIdx.x == 0)
-        for (int s = threadIdx.x; s <= S; s += blockDim.x) p.ws_prefix[s] = prefix[s];
     // sequences with no context get a zero row
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
         if (prefix[s + 1] == prefix[s]) {
@@ -258,6 +263,42 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         }
     };
 
+    // Combine the partial records of unit (cs, ch) held by warps w0..w1, in
+    // warp order; lanes split the group's G * HD outputs into runs of 16.
+    auto merge_unit = [&](int64_t w0, int64_t w1, int64_t U0) {
+        const int64_t st0 = w0 * W / TW;
+        T* out = static_cast<T*>(p.out) + ((int64_t)cs * p.num_heads + (int64_t)ch * G) * HD;
+        for (int base_e = lane * 16; base_e < G * HD; base_e += 32 * 16) {
+            const int j = base_e / HD, d0 = base_e - j * HD;
+            float M = -INFINITY, L = 0.f, o[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) o[t] = 0.f;
+            for (int64_t w = w0; w <= w1; ++w) {
+                if (w * W / TW == (w + 1) * W / TW) continue;  // empty range
+                const int slot = (w == w0 && U0 > st0) ? 1 : 0;
+                const float* r = p.ws_part + (w * 2 + slot) * (int64_t)G * (HD + 4) + j * (HD + 4);
+                const float m = __ldcg(r + HD), l = __ldcg(r + HD + 1);
+                float4 a[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) a[t] = __ldcg(reinterpret_cast<const float4*>(r + d0) + t);
+                const float Mn = fmaxf(M, m);
+                const float c = exp2f(M - Mn), e = exp2f(m - Mn);
+                L = L * c + e * l;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    o[4 * t + 0] = o[4 * t + 0] * c + e * a[t].x;
+                    o[4 * t + 1] = o[4 * t + 1] * c + e * a[t].y;
+                    o[4 * t + 2] = o[4 * t + 2] * c + e * a[t].z;
+                    o[4 * t + 3] = o[4 * t + 3] * c + e * a[t].w;
+                }
+                M = Mn;
+            }
+            const float inv = 1.f / L;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) out[j * HD + d0 + t] = Elt<T>::from_f(o[t] * inv);
+        }
+    };
+
     auto finalize = [&](int bend, int nb) {
         float lt[NT][2];
 #pragma unroll
@@ -289,14 +330,14 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                 }
         } else {
             const int slot = first_seg ? 0 : 1;
-            float* rec = p.ws_part + ((gw * 2 + slot) * G) * (int64_t)(HD + 2);
+            float* rec = p.ws_part + (gw * 2 + slot) * (int64_t)G * (HD + 4);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                 for (int e = 0; e < 2; ++e) {
                     const int hh = nt * 8 + 2 * c4 + e;
                     if (hh < G) {
-                        float* r = rec + hh * (HD + 2);
+                        float* r = rec + hh * (HD + 4);
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
                             r[mt * 16 + g] = acc[mt][nt][e];
@@ -308,6 +349,30 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                         }
                     }
                 }
+            __threadfence();
+            __syncwarp();
+            // the warps that hold this unit: [w0, w1], empty ranges excluded
+            const int64_t U0 = (int64_t)prefix[cs] * Hkv + (int64_t)ch * nb, U1 = U0 + nb;
+            const int64_t w0 = ((U0 + 1) * TW - 1) / W, w1 = (U1 * TW - 1) / W;
+            int last = 0;
+            if (lane == 0) {
+                int expected = 0;
+                for (int64_t w = w0; w <= w1; ++w) expected += (w * W / TW < (w + 1) * W / TW) ? 1 : 0;
+                unsigned long long* cnt = p.ws_cnt + (int64_t)cs * Hkv + ch;
+                unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt), want;
+                while (true) {  // ends: each failed swap means another writer's succeeded
+                    want = ((cur >> 16) == p.epoch) ? cur + 1 : ((p.epoch << 16) | 1ull);
+                    const unsigned long long prev = atomicCAS(cnt, cur, want);
+                    if (prev == cur) break;
+                    cur = prev;
+                }
+                last = ((int)(want & 0xffffull) == expected) ? 1 : 0;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+                __threadfence();
+                merge_unit(w0, w1, U0);
+            }
         }
     };
 
@@ -411,52 +476,13 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
     }
 }
 
-// Merge the partial states of every unit that was cut between warps.
-template <typename T, int HD>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const TcParams p, int64_t total_warps) {
-    pdl_wait_primary();
-    const int h = blockIdx.x, s = blockIdx.y;
-    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
-    const int P0 = p.ws_prefix[s], nb = p.ws_prefix[s + 1] - P0;
-    if (nb == 0) return;
-    const int64_t W = (int64_t)p.ws_prefix[S] * Hkv;
-    const int64_t U0 = (int64_t)P0 * Hkv + (int64_t)h * nb, U1 = U0 + nb;
-    auto start = [&](int64_t w) { return w * W / total_warps; };
-    auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / W; };
-    const int64_t w0 = warp_of(U0), w1 = warp_of(U1 - 1);
-    if (w0 == w1) return;  // the unit was finished by one warp
-    const int64_t st0 = start(w0);
-    T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + (int64_t)h * G) * HD;
-    for (int j = 0; j < G; ++j) {
-        float M = -INFINITY;
-        for (int64_t w = w0; w <= w1; ++w) {
-            if (start(w) == start(w + 1)) continue;
-            const int slot = (w == w0 && U0 > st0) ? 1 : 0;
-            const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
-            M = fmaxf(M, r[HD]);
-        }
-        float L = 0.f;
-        for (int64_t w = w0; w <= w1; ++w) {
-            if (start(w) == start(w + 1)) continue;
-            const int slot = (w == w0 && U0 > st0) ? 1 : 0;
-            const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
-            L += exp2f(r[HD] - M) * r[HD + 1];
-        }
-        const float inv = 1.f / L;
-        for (int d = threadIdx.x; d < HD; d += blockDim.x) {
-            float o = 0.f;
-            for (int64_t w = w0; w <= w1; ++w) {
-                if (start(w) == start(w + 1)) continue;
-                const int slot = (w == w0 && U0 > st0) ? 1 : 0;
-                const float* r = p.ws_part + ((w * 2 + slot) * G + j) * (int64_t)(HD + 2);
-                o += exp2f(r[HD] - M) * r[d];
-            }
-            out[j * HD + d] = Elt<T>::from_f(o * inv);
-        }
-    }
-}
-
 // ---------------------------------------------------------------- host side
+
+// Tags of successive launches (48 bits, never 0, never reused in a process).
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{0};
+    return ((counter.fetch_add(1) + 1) & ((1ull << 48) - 1)) | (1ull << 47);
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -504,7 +530,8 @@ const void* kernel_ptr() {
 
 template <int HD>
 int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t max_context, int64_t override_ctas) {
-    if (override_ctas > 0) return (int)override_ctas;
+    // the per-unit count holds up to 65535 partials: keep the grid's warps below that
+    if (override_ctas > 0) return (int)(override_ctas < 16000 ? override_ctas : 16000);
     int dev = 0, sms = 0, occ = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -538,30 +565,28 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.num_kv_heads = a.num_kv_heads;
     p.group = a.num_heads / a.num_kv_heads;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const size_t prefix_bytes = ((size_t)(a.num_seqs + 1) * 4 + 255) & ~(size_t)255;
-    p.ws_prefix = static_cast<int32_t*>(workspace);
-    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + prefix_bytes);
+    const size_t cnt_bytes = ((size_t)a.num_seqs * a.num_kv_heads * 8 + 255) & ~(size_t)255;
+    p.ws_cnt = static_cast<unsigned long long*>(workspace);
+    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes);
+    p.epoch = next_epoch();
 
     const void* kfn = kernel_ptr<T, HD, NT>();
     const size_t smem = smem_bytes<HD>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    decode_tc_kernel<T, HD, NT><<<grid, Pipe<HD>::NW * 32, smem, stream>>>(tmK, tmV, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
+    // programmatic dependent launch: the grid may be scheduled while the
+    // previous kernel on the stream finishes; the kernel waits for it first
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
-    cfg.blockDim = dim3(128);
-    cfg.dynamicSmemBytes = 0;
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(Pipe<HD>::NW * 32);
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int64_t total_warps = (int64_t)grid * Pipe<HD>::NW;
-    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<T, HD>, p, total_warps);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT>, tmK, tmV, p);
 }
 
 template <typename T>
@@ -604,11 +629,10 @@ int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int
 }
 
 size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas) {
-    (void)num_kv_heads;
     const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
     const int nw = head_dim == 256 ? Pipe<256>::NW : (head_dim == 128 ? Pipe<128>::NW : Pipe<64>::NW);
-    const size_t prefix_bytes = ((size_t)(s + 1) * 4 + 255) & ~(size_t)255;
-    return prefix_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 2) * sizeof(float);
+    const size_t cnt_bytes = ((size_t)s * num_kv_heads * 8 + 255) & ~(size_t)255;
+    return cnt_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
