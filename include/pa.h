@@ -198,6 +198,31 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
                     int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
+ * memory when they run it: a runtime or plugin host that hands out all
+ * device memory from its own pool and forbids cudaMalloc in its callbacks, a
+ * latency-critical loop that cannot afford an allocation's possible device
+ * synchronisation, or code with no allocator at hand.  The pages have no
+ * counterpart; it exists for those callers only.
+ * Same arguments and result as pa_decode (tensor-core cases: bf16/f16,
+ * head_dim 64/128/256, block_size 16, at most 16 query heads per KV head;
+ * others return PA_ERR_UNSUPPORTED), but no workspace: the split-KV scratch
+ * is one library-owned device array of 8 MiB per device, held from load
+ * until process exit.  A problem whose scratch (pa_decode_workspace_size
+ * with default options) exceeds 8 MiB returns PA_ERR_WORKSPACE before
+ * anything is enqueued.  The call allocates nothing.  The first call with a
+ * device current looks up that device's array address; make it before any
+ * stream capture.  All calls on a device share the array: calls whose
+ * kernels overlap on the GPU race and must be ordered by the caller.
+ */
+PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                                   int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                                   int32_t block_size, int32_t max_context, float scale, int dtype,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -84,6 +84,12 @@ pa_status check_geometry(int32_t num_heads, int32_t num_kv_heads, int32_t head_d
 
 }  // namespace
 
+namespace pa {
+// Sets the reason pa_last_error() reports (used by entry points defined in
+// other translation units).
+void record_error(const std::string& msg) { g_last_error = msg; }
+}  // namespace pa
+
 extern "C" {
 
 const char* pa_status_string(int status) {

@@ -25,6 +25,9 @@ constexpr int kDecodeMaxSeqsPerLaunch = 4096;
 // Number of polls a bounded mbarrier wait makes before giving up.
 constexpr uint32_t kMaxPolls = 1u << 24;
 
+// Reason reported by pa_last_error() for the calling thread (pa_api.cu).
+void record_error(const std::string& msg);
+
 // ---- copy kernels (pa_copy.cu)
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_idx,
                                 const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
