@@ -124,7 +124,7 @@ pa_status pa_set_check_mode(int on) { return pa_set_option(PA_OPT_CHECK_MODE, on
 pa_status pa_device_status(int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pa_device_status");
-    const uint32_t bits = pa::decode_tc_status(clear != 0);
+    const uint32_t bits = pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0);
     if (bits & 1u) return fail(PA_ERR_TIMEOUT, "a kernel's bounded barrier wait ran out");
     return PA_OK;
 }
@@ -356,8 +356,12 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
-    if (g_options[PA_OPT_VARLEN_KERNEL] == 2)
-        return fail(PA_ERR_UNSUPPORTED, "no tensor-core varlen kernel in this build");
+    const bool tc_ok = pa::varlen_tc_supported(dtype, head_dim, block_size);
+    const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
+    if (want == 2 && !tc_ok)
+        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernel takes bf16/f16, head_dim 64/128 and "
+                                        "block_size 16");
+    const bool use_tc = tc_ok && want != 1;
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
         pa_status err = PA_OK;
@@ -394,6 +398,13 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.dtype = dtype;
+    if (use_tc) {
+        std::string err;
+        cudaError_t e = pa::launch_varlen_tc(a, num_blocks, &err, st);
+        if (e != cudaSuccess)
+            return err.empty() ? cuda_fail(e, "pa_varlen launch") : fail(PA_ERR_CUDA, "pa_varlen: " + err);
+        return PA_OK;
+    }
     cudaError_t e = pa::launch_attn_simt(a, st);
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_varlen launch");
 }

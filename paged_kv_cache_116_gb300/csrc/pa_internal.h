@@ -72,4 +72,9 @@ cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_cta
                              std::string* err, cudaStream_t stream);
 uint32_t decode_tc_status(bool clear);
 
+// ---- tensor-core varlen (pa_varlen_tc.cu)
+bool varlen_tc_supported(int dtype, int head_dim, int block_size);
+cudaError_t launch_varlen_tc(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream);
+uint32_t varlen_tc_status(bool clear);
+
 }  // namespace pa

@@ -98,3 +98,49 @@ def test_check_mode_rejects_bad_cu_seqlens(pa):
         pa.pa_varlen(out, w.q.to(DEV), kc, vc, bt, lens, cu, 8, 37, w.scale)
     finally:
         pa.pa_set_check_mode(False)
+
+
+TC_CASES = []
+_r2 = np.random.default_rng(2024)
+for _i in range(12):
+    _hd = int(_r2.choice([64, 128]))
+    _g = int(_r2.choice([1, 2, 3, 6, 8, 12]))
+    _hkv = int(_r2.choice([1, 2, 4]))
+    _dt = str(_r2.choice(["bf16", "f16"]))
+    _S = int(_r2.integers(1, 9))
+    _q = _r2.integers(1, 200, _S)
+    _q[_r2.random(_S) < 0.4] = 1  # decode rows mixed in
+    _cached = _r2.integers(0, 300, _S)
+    _cached[0] = 0 if _S > 1 else _cached[0]  # a full prefill with no cached context
+    TC_CASES.append((_dt, _hd, _g, _hkv, (_cached + _q).tolist(), _q.tolist(), _i))
+
+
+@pytest.mark.parametrize("dt,hd,g,hkv,lens,qlens,seed", TC_CASES)
+def test_random_varlen_tensor_core_kernel(pa, dt, hd, g, hkv, lens, qlens, seed):
+    w = W.varlen_workload("rand_tc", dt, 16, g * hkv, hkv, hd, lens, qlens, seed=100 + seed)
+    kc, vc, bt = device_caches(w, DEV)
+    for causal in (True, False):
+        exact = oracle_attention(w, causal=causal)
+        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2), exact)
+
+
+def test_varlen_kernels_agree_on_mixed_step(pa):
+    w = W.mixed_varlen(num_chunks=4, num_groups=6, device=DEV)
+    kc, vc, bt = device_caches(w, DEV)
+    a = run_varlen(pa, w, kc, vc, bt, kernel=1).double().cpu().numpy()
+    b = run_varlen(pa, w, kc, vc, bt, kernel=2).double().cpu().numpy()
+    exact = oracle_attention(w)
+    assert within_tol(a, exact, w.dtype)[0] and within_tol(b, exact, w.dtype)[0]
+
+
+def test_varlen_permutation_bit_identical(pa):
+    w = W.varlen_workload("perm_v", "bf16", 16, 12, 2, 128, [300, 81, 17, 1000], [1, 81, 5, 130], seed=3)
+    kc, vc, bt = device_caches(w, DEV)
+    base = run_varlen(pa, w, kc, vc, bt, kernel=2)
+    perm = torch.from_numpy(np.random.default_rng(4).permutation(w.num_blocks)).to(DEV)
+    kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=2)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
