@@ -1,19 +1,25 @@
-"""Benchmark of the paged-KV hot path on the 64-sequence GQA decode batch.
+"""Benchmark of the paged-KV hot path (default: the 64-sequence GQA decode batch).
 
-One step = the generation step of the batch through the C ABI:
-pa_slot_mapping (the new token of each sequence) -> pa_write_kv (its K/V
-row) -> pa_decode (tensor-core kernel + split merge).  Inputs are resident
-in HBM; two copies of the K/V pool (2 x 0.55 GB, each larger than the
-129 MB L2) alternate between steps so no step reads a pool the previous one
-left in L2.
+A step is one pass of the path over one batch, through the C ABI:
+  decode workloads: pa_slot_mapping (each sequence's new token) ->
+                    pa_write_kv (its K/V row) -> pa_decode
+  mixed_varlen:     pa_copy_blocks (copy-on-write of the shared tails) ->
+                    pa_slot_mapping -> pa_write_kv (every new token) ->
+                    pa_varlen (prefill chunks + decode rows)
+Inputs are resident in HBM.  Enough copies of the K/V pool to exceed twice
+the 129 MB L2 alternate between steps, so no step reads a pool the previous
+one left in L2.  The step is captured once per pool copy as a CUDA graph and
+replayed (what a serving loop does); `eager_ms_per_step` is the same calls
+issued one by one.
 
-Prints ONE JSON line (rank 0).  `value` is algorithmic K/V bytes read per
-step over the device time of the step (GB/s); `roofline` is the decode
-kernels' own time against the measured HBM copy bandwidth; `e2e` is the same
-metric with each step's inputs copied from pinned host memory and the output
-copied back inside the timed region; `cpu_baseline` is the CPU oracle on a
-bounded sample.  `--impl reference` times that oracle alone as the
-reference arm.
+Prints ONE JSON line (rank 0).  `value` is the algorithmic K/V bytes the
+step's attention reads over the step's device time (GB/s); `roofline` is the
+dominant kernel timed alone (its own graph, same rotation) against the
+measured HBM copy bandwidth (decode) or the measured bf16 tensor rate
+(varlen); `e2e` is the step with its inputs copied from pinned host memory
+and its output copied back inside the timed region; `cpu_baseline` is the
+CPU oracle on a bounded sample.  `--impl reference` times that oracle alone
+as the reference arm.
 
 Multi-GPU (torchrun): every rank runs its own replica of the batch (the
 sequences are independent, no data-path collective); `value` sums all ranks'
@@ -22,6 +28,7 @@ bytes over the slowest rank's time.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -32,7 +39,9 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = ("paged decode attention KV GB/s (fraction of HBM peak) and sequences/s, 1×GB300")
+METRIC = "paged decode attention KV GB/s (fraction of HBM peak) and sequences/s, 1×GB300"
+L2_BYTES = 129 * 10 ** 6
+WORKLOADS = ("gqa_decode_batch", "long_context_decode", "mha_decode", "tiny_decode", "mixed_varlen")
 
 
 def parse():
@@ -41,9 +50,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=WORKLOADS, default="gqa_decode_batch")
     ap.add_argument("--no-rotate", action="store_true", help="one pool copy (for profiling)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, clocks and cpu_baseline")
-    ap.add_argument("--num-seqs", type=int, default=64)
     return ap.parse_args()
 
 
@@ -52,17 +61,17 @@ def measured_peaks():
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             return json.load(f), "measured"
     except OSError:
-        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
-def traffic_record(kernel_file):
-    """DRAM bytes per launch of the decode kernel from a committed ncu
-    summary, if it was taken on the current kernel source."""
+def traffic_record(workload, kernel_file):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary of this workload, if it was taken on the current kernel source."""
     src = os.path.join(ROOT, "paged_kv_cache_116_gb300", "csrc", kernel_file)
-    path = os.path.join(ROOT, "profiles", "decode_tc_gqa64_traffic.json")
+    path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            rec = json.load(f)
+            rec = json.load(f).get(workload, {})
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
         if rec.get("source_sha256") == sha:
             return rec.get("dram_bytes_per_launch")
@@ -99,7 +108,7 @@ class Clocks:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
@@ -108,6 +117,7 @@ class Clocks:
             try:
                 sm.append(float(f[1]))
                 mx.append(float(f[2]))
+                power.append(float(f[3]))
             except ValueError:
                 continue
             for n, v in zip(names, f[5:9]):
@@ -116,75 +126,119 @@ class Clocks:
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(power),
+                "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def _oracle_batch(num_seqs):
-    """The first num_seqs sequences of the batch (the same length stream),
-    values drawn on the host, written into an oracle-side pool."""
+# ---------------------------------------------------------------- workloads
+
+
+def make_workload(name, device):
+    from paged_kv_cache_116_gb300 import workloads as W
+
+    return W.tiny_decode() if name == "tiny_decode" else getattr(W, name)(device=device)
+
+
+def varlen_flops(w):
+    """2 x the multiply-adds of Q K^T and P V over the causal (or full) key ranges."""
+    total = 0.0
+    for n, L in zip(w.query_lens.tolist(), w.seq_lens.tolist()):
+        total += n * (L - n) + n * (n + 1) / 2 if w.causal else n * L
+    return 4.0 * w.num_heads * w.head_dim * total
+
+
+def oracle_setup(w):
+    """Oracle-side pool of a (host) workload after the step's copies and writes."""
     import numpy as np
 
     import oracle
     from paged_kv_cache_116_gb300 import workloads as W
 
-    w = W.gqa_decode_batch(num_seqs=num_seqs)
-    kc = np.full((w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), 0x7FC0, dtype=np.uint16)
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    if w.dtype == "f32":
+        kc = np.full(shape, np.nan, np.float32)
+    else:
+        kc = np.full(shape, 0x7FC0 if w.dtype == "bf16" else 0x7E00, np.uint16)
     vc = kc.copy()
     s = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
     oracle.write_kv(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), s, kc, vc)
+    if w.cow_pairs.shape[0]:
+        oracle.copy_blocks([kc], [vc], w.cow_pairs)
     s = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
     oracle.write_kv(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), s, kc, vc)
-    return w, kc, vc, W.raw_numpy(w.q)
+    return kc, vc, W.raw_numpy(w.q)
 
 
-def cpu_baseline(total_seqs, sample=8, budget_s=10.0):
-    """The oracle (as it stands) on a bounded sample: the first `sample`
-    sequences of the batch, repeated for about budget_s seconds."""
+def oracle_step(w, kc, vc, q):
     import oracle
 
-    w, kc, vc, q = _oracle_batch(sample)
-    per_tok = w.num_kv_heads * w.head_dim * 2 * w.elt
-    repeats, t = 0, time.perf_counter()
+    return oracle.paged_attention(q, kc, vc, w.block_tables, w.seq_lens, w.query_start_loc, w.scale, w.dtype,
+                                  w.causal)
+
+
+def host_sample_workload(name):
+    """A bounded sample of a workload with the same generators, values drawn
+    on the host: its first requests (or, for the mixed step, fewer chunks and
+    sampling groups)."""
+    from paged_kv_cache_116_gb300 import workloads as W
+
+    return {"gqa_decode_batch": lambda: W.gqa_decode_batch(num_seqs=8),
+            "long_context_decode": lambda: W.long_context_decode(num_seqs=1),
+            "mha_decode": lambda: W.mha_decode(num_seqs=16),
+            "tiny_decode": W.tiny_decode,
+            "mixed_varlen": lambda: W.mixed_varlen(num_chunks=1, num_groups=4)}[name]()
+
+
+def cpu_sample(name, budget_s=10.0):
+    """The oracle (as it stands) on a bounded sample of the workload,
+    repeated for about budget_s seconds."""
+    import oracle
+
+    w = host_sample_workload(name)
+    kc, vc, q = oracle_setup(w)
+    per_step = w.kv_bytes_read()
+    reps, t = 0, time.perf_counter()
     while True:
-        oracle.decode_attention(q, kc, vc, w.block_tables, w.seq_lens, w.scale, w.dtype)
-        repeats += 1
+        oracle_step(w, kc, vc, q)
+        reps += 1
         el = time.perf_counter() - t
         if el >= budget_s:
             break
-    return {"value": int(w.seq_lens.sum()) * per_tok * repeats / el / 1e9, "unit": "GB/s",
-            "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": "first %d of %d sequences (%d tokens) x %d, fp64 C oracle with OpenMP, %.1f s" % (
-                sample, total_seqs, int(w.seq_lens.sum()), repeats, el),
-            "seq_per_s": sample * repeats / el}
+    return {"value": per_step * reps / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": "%d requests of the same generators (%d context tokens) x %d, fp64 C oracle with OpenMP, "
+                      "%.1f s" % (w.num_seqs, int(w.seq_lens.sum()), reps, el),
+            "seq_per_s": w.num_seqs * reps / el}
 
 
 def run_reference(args, rank):
-    """Reference arm: the CPU oracle on the first 8 sequences of the batch
-    per step (rank 0 only)."""
+    """Reference arm: the CPU oracle on a bounded sample of the workload per
+    step (rank 0 only)."""
     if rank != 0:
         return
     import oracle
 
-    sample = 8
-    w, kc, vc, q = _oracle_batch(sample)
-    step_bytes = int(w.seq_lens.sum()) * w.num_kv_heads * w.head_dim * 2 * w.elt
+    w = host_sample_workload(args.workload)
+    kc, vc, q = oracle_setup(w)
+    step_bytes = w.kv_bytes_read()
     for _ in range(args.warmup):
-        oracle.decode_attention(q, kc, vc, w.block_tables, w.seq_lens, w.scale, w.dtype)
+        oracle_step(w, kc, vc, q)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.decode_attention(q, kc, vc, w.block_tables, w.seq_lens, w.scale, w.dtype)
+        oracle_step(w, kc, vc, q)
     dt = time.perf_counter() - t
     value = step_bytes * args.steps / dt / 1e9
-    desc = "first %d of %d sequences per step, fp64 C oracle with OpenMP" % (sample, args.num_seqs)
+    desc = "%d requests of the %s generators per step, fp64 C oracle with OpenMP" % (w.num_seqs, args.workload)
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "gqa_decode_bf16_64seq", "num_seqs": args.num_seqs, "sample_seqs": sample},
+        "config": {"workload": w.name, "sample_requests": w.num_seqs},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ---------------------------------------------------------------- the GPU arm
 
 
 def main():
@@ -195,7 +249,6 @@ def main():
         run_reference(args, rank)
         return
 
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -207,59 +260,90 @@ def main():
 
     import __graft_entry__
 
-    __graft_entry__.build() if rank == 0 or world == 1 else None
+    if rank == 0 or world == 1:
+        __graft_entry__.build()
     if world > 1:
         dist.barrier()
     import paged_kv_cache_116_gb300 as pa
     from paged_kv_cache_116_gb300 import workloads as W
 
-    w = W.gqa_decode_batch(num_seqs=args.num_seqs, device=dev)
+    w = make_workload(args.workload, dev)
+    tdt = W.TORCH_DTYPES[w.dtype]
     S, hq, hkv, hd, bs = w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
-    max_ctx = int(w.seq_lens.max())
+    decode = w.is_decode and w.cow_pairs.shape[0] == 0
+    max_ctx, max_q = int(w.seq_lens.max()), int(w.query_lens.max())
     kv_bytes = w.kv_bytes_read()
-    # algorithmic bytes of the decode: K/V once per KV head + q + out + tables + lengths
-    alg_bytes = kv_bytes + 2 * S * hq * hd * w.elt + int(sum((L + bs - 1) // bs for L in w.seq_lens)) * 4 + S * 4
+    N = int(w.query_lens.sum())
 
-    # resident pools (two copies, alternated), filled through the library
-    copies = 1 if args.no_rotate else 2
+    # resident pools, filled through the library; enough copies to defeat L2
+    pool_bytes = 2 * w.num_blocks * bs * hkv * hd * w.elt
+    copies = 1 if args.no_rotate else min(16, max(2, math.ceil(2 * L2_BYTES / pool_bytes)))
+    l2_note = ("inputs larger than L2: %d pool copies of %.3f GB alternate between steps" % (copies, pool_bytes / 1e9)
+               if copies * pool_bytes > L2_BYTES else
+               "pool of %.6f GB x %d copies stays in L2 (launch-bound case)" % (pool_bytes / 1e9, copies))
     pools = []
+    pre_slots = None
+    if w.pre_pos.shape[0]:
+        pre_slots = pa.pa_slot_mapping(torch.from_numpy(w.pre_block_tables).to(dev),
+                                       torch.from_numpy(w.pre_seq_idx).to(dev), torch.from_numpy(w.pre_pos).to(dev),
+                                       bs)
+    pre_k = w.pre_k.to(dev) if pre_slots is not None else None
+    pre_v = w.pre_v.to(dev) if pre_slots is not None else None
     for c in range(copies):
-        kc = torch.full((w.num_blocks, bs, hkv, hd), float("nan"), dtype=torch.bfloat16, device=dev)
+        kc = torch.full((w.num_blocks, bs, hkv, hd), float("nan"), dtype=tdt, device=dev)
         vc = torch.full_like(kc, float("nan"))
-        slots = pa.pa_slot_mapping(torch.from_numpy(w.pre_block_tables).to(dev), torch.from_numpy(w.pre_seq_idx).to(dev),
-                                   torch.from_numpy(w.pre_pos).to(dev), bs)
-        pa.pa_write_kv(w.pre_k, w.pre_v, slots, kc, vc)
+        if pre_slots is not None:
+            pa.pa_write_kv(pre_k, pre_v, pre_slots, kc, vc)
         pools.append((kc, vc))
-    del w.pre_k, w.pre_v
+    w.pre_k = w.pre_v = pre_k = pre_v = None
     bt = torch.from_numpy(w.block_tables).to(dev)
     lens = torch.from_numpy(w.seq_lens).to(dev)
+    cu = torch.from_numpy(w.query_start_loc).to(dev)
     seq_idx = torch.from_numpy(w.new_seq_idx).to(dev)
     pos = torch.from_numpy(w.new_pos).to(dev)
-    q, new_k, new_v = w.q.contiguous(), w.new_k.contiguous(), w.new_v.contiguous()
+    pairs = torch.from_numpy(w.cow_pairs).to(dev)
+    q, new_k, new_v = w.q.to(dev).contiguous(), w.new_k.to(dev).contiguous(), w.new_v.to(dev).contiguous()
     out = torch.empty_like(q)
-    slot_buf = torch.empty(S, dtype=torch.int64, device=dev)
-    ws_bytes = pa.pa_decode_workspace_size(S, hq, hkv, hd, bs, max_ctx, torch.bfloat16)
+    slot_buf = torch.empty(N, dtype=torch.int64, device=dev)
+    if decode:
+        ws_bytes = pa.pa_decode_workspace_size(S, hq, hkv, hd, bs, max_ctx, tdt)
+    else:
+        ws_bytes = pa.pa_varlen_workspace_size(S, N, max_q, hq, hkv, hd, bs, max_ctx, tdt)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
-    def step(i):
-        """One generation step through the C ABI on the current stream."""
+
+    def attend(kc, vc, qq, tables, ll, cuq, st):
+        if decode:
+            pa.pa_decode(out, qq, kc, vc, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
+        else:
+            pa.pa_varlen(out, qq, kc, vc, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
+                         workspace=ws, stream=st)
+
+    def run_step(i, t_in):
+        """One pass of the path through the C ABI on the current stream."""
         kc, vc = pools[i % copies]
         st = torch.cuda.current_stream()
-        pa.pa_slot_mapping(bt, seq_idx, pos, bs, slot_out=slot_buf, stream=st)
-        pa.pa_write_kv(new_k, new_v, slot_buf, kc, vc, stream=st)
-        pa.pa_decode(out, q, kc, vc, bt, lens, max_ctx, w.scale, workspace=ws, stream=st)
+        d_q, d_k, d_v, d_bt, d_lens, d_cu, d_seq, d_pos, d_pairs = t_in
+        if d_pairs.shape[0]:
+            pa.pa_copy_blocks(kc, vc, d_pairs, stream=st)
+        pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=st)
+        pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=st)
+        attend(kc, vc, d_q, d_bt, d_lens, d_cu, st)
 
-    def decode_only(i):
+    dev_in = (q, new_k, new_v, bt, lens, cu, seq_idx, pos, pairs)
+
+    def step(i):
+        run_step(i, dev_in)
+
+    def kernel_only(i):
         kc, vc = pools[i % copies]
-        pa.pa_decode(out, q, kc, vc, bt, lens, max_ctx, w.scale, workspace=ws, stream=torch.cuda.current_stream())
+        attend(kc, vc, q, bt, lens, cu, torch.cuda.current_stream())
 
-    launches_per_step = 3  # slot mapping, write, decode
+    launches_per_step = 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
         step(i)
     torch.cuda.synchronize()
 
-    # The step is captured once per pool copy into CUDA graphs (what a serving
-    # loop replays); the same C-ABI calls run eagerly give `eager`.
     def capture(fn):
         gs = []
         for c in range(copies):
@@ -269,20 +353,19 @@ def main():
             gs.append(g)
         return gs
 
-    step_graphs = capture(step)
-    dec_graphs = capture(decode_only)
+    step_graphs, kern_graphs = capture(step), capture(kernel_only)
     for i in range(max(args.warmup, 3)):
         step_graphs[i % copies].replay()
-        dec_graphs[i % copies].replay()
+        kern_graphs[i % copies].replay()
     torch.cuda.synchronize()
 
-    def timed(fn_i):
+    def timed(fn_i, steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
         a.record()
-        for i in range(args.steps):
+        for i in range(steps):
             fn_i(i)
         b.record()
         torch.cuda.synchronize()
@@ -294,11 +377,11 @@ def main():
     if rank == 0 and not args.no_extras:
         clocks.start()
         time.sleep(0.5)
-    ms = timed(lambda i: step_graphs[i % copies].replay())
+    ms = timed(lambda i: step_graphs[i % copies].replay(), args.steps)
     clk = clocks.stop() if rank == 0 and not args.no_extras else None
-    dec_ms = timed(lambda i: dec_graphs[i % copies].replay()) / args.steps
-    eager_ms = timed(step) / args.steps
-
+    kern_ms = timed(lambda i: kern_graphs[i % copies].replay(), args.steps) / args.steps
+    eager_steps = min(args.steps, 2000)
+    eager_ms = timed(step, eager_steps) / eager_steps
     if world > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -307,31 +390,20 @@ def main():
     value = kv_bytes * world * args.steps / (ms / 1e3) / 1e9
     seq_per_s = S * world * args.steps / (ms / 1e3)
 
-    # e2e: each step's inputs from pinned host memory, the step, the output
-    # back to pinned host memory -- all inside the timed region (captured as
-    # one graph per pool copy, like the device-only step)
+    # e2e: each step's inputs from pinned host memory -> H2D, the step, the
+    # output D2H to pinned memory; captured and replayed like the step
     e2e = None
     if not args.no_extras:
-        h_q = q.cpu().pin_memory()
-        h_k, h_v = new_k.cpu().pin_memory(), new_v.cpu().pin_memory()
-        h_bt, h_lens = bt.cpu().pin_memory(), lens.cpu().pin_memory()
-        h_seq, h_pos = seq_idx.cpu().pin_memory(), pos.cpu().pin_memory()
+        host_in = [t.cpu().pin_memory() for t in dev_in]
+        dev_copy = [torch.empty_like(t) for t in dev_in]
         h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        d_q, d_k, d_v = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v)
-        d_bt, d_lens, d_seq, d_pos = torch.empty_like(bt), torch.empty_like(lens), torch.empty_like(seq_idx), \
-            torch.empty_like(pos)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v, h_bt, h_lens, h_seq, h_pos))
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = h_out.numel() * h_out.element_size()
 
         def e2e_step(i):
-            kc, vc = pools[i % copies]
-            st = torch.cuda.current_stream()
-            for d, h in ((d_q, h_q), (d_k, h_k), (d_v, h_v), (d_bt, h_bt), (d_lens, h_lens), (d_seq, h_seq),
-                         (d_pos, h_pos)):
+            for d, h in zip(dev_copy, host_in):
                 d.copy_(h, non_blocking=True)
-            pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=st)
-            pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=st)
-            pa.pa_decode(out, d_q, kc, vc, d_bt, d_lens, max_ctx, w.scale, workspace=ws, stream=st)
+            run_step(i, dev_copy)
             h_out.copy_(out, non_blocking=True)
 
         for i in range(3):
@@ -341,35 +413,50 @@ def main():
         for i in range(3):
             e2e_graphs[i % copies].replay()
         torch.cuda.synchronize()
-        e_ms = timed(lambda i: e2e_graphs[i % copies].replay())
+        e_steps = min(args.steps, 5000)
+        e_ms = timed(lambda i: e2e_graphs[i % copies].replay(), e_steps)
         if world > 1:
             t = torch.tensor([e_ms], device=dev)
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e_ms = float(t.item())
-        e2e = {"value": kv_bytes * world * args.steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / args.steps,
-               "how": "pinned-host inputs -> H2D copies -> pa_slot_mapping/pa_write_kv/pa_decode -> D2H output, "
+        e2e = {"value": kv_bytes * world * e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / e_steps,
+               "how": "pinned-host inputs -> H2D copies -> the step's C-ABI calls -> D2H output, "
                       "replayed as a CUDA graph per step"}
 
     peaks, kind = measured_peaks()
-    dec_avg = dec_ms
-    achieved = alg_bytes / (dec_avg / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": "decode_tc_kernel (one pa_decode call, split merge included)",
-            "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-            "peak_kind": kind, "traffic": traffic_record("pa_decode_tc.cu"), "algorithmic_bytes": alg_bytes,
-            "decode_us": dec_avg * 1e3}
+    if decode:
+        nblk = int(sum((L + bs - 1) // bs for L in w.seq_lens.tolist()))
+        alg = kv_bytes + 2 * S * hq * hd * w.elt + nblk * 4 + S * 4
+        achieved = alg / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "decode_tc_kernel (pa_decode, split merge included)",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
+                "traffic": traffic_record(args.workload, "pa_decode_tc.cu"), "kernel_us": kern_ms * 1e3}
+        if w.dtype == "f32":
+            roof["kernel"] = "attn_simt_kernel (pa_decode, fp32 CUDA-core path)"
+    else:
+        fl = varlen_flops(w)
+        achieved = fl / (kern_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "kernel": "varlen_tc_kernel (pa_varlen)", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": kind + " bf16_tflops (burst)",
+                "algorithmic_flops": fl, "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
+                "traffic": traffic_record(args.workload, "pa_varlen_tc.cu"), "kernel_us": kern_ms * 1e3}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": S, "num_heads": hq, "num_kv_heads": hkv, "head_dim": hd,
-                       "block_size": bs, "num_blocks": w.num_blocks, "total_context": int(w.seq_lens.sum()),
-                       "kv_bytes_per_step": kv_bytes, "l2": "inputs larger than L2: %d pool copies of %.2f GB "
-                       "alternate between steps" % (copies, 2 * pools[0][0].numel() * 2 / 1e9),
-                       "step": "pa_slot_mapping + pa_write_kv + pa_decode, replayed as a CUDA graph",
-                       "seed": 0},
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "num_seqs": S, "new_tokens": N, "num_heads": hq, "num_kv_heads": hkv,
+                       "head_dim": hd, "block_size": bs, "num_blocks": w.num_blocks,
+                       "total_context": int(w.seq_lens.sum()), "cow_pairs": int(w.cow_pairs.shape[0]),
+                       "kv_bytes_per_step": kv_bytes,
+                       "l2": l2_note,
+                       "step": ("pa_copy_blocks + " if pairs.shape[0] else "") +
+                               "pa_slot_mapping + pa_write_kv + " + ("pa_decode" if decode else "pa_varlen") +
+                               ", replayed as a CUDA graph", "seed": 0},
             "seq_per_s": seq_per_s,
             "eager_ms_per_step": eager_ms,
             "roofline": roof,
@@ -378,7 +465,7 @@ def main():
             "e2e": e2e,
         }
         if not args.no_extras:
-            line["cpu_baseline"] = cpu_baseline(S)
+            line["cpu_baseline"] = cpu_sample(args.workload)
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
