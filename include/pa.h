@@ -78,8 +78,9 @@ typedef enum {
     /* Number of CTAs of the tensor-core decode kernel's balanced split;
      * 0 (default) picks one per resident slot of the device. */
     PA_OPT_DECODE_CTAS = 2,
-    /* Varlen kernel: 0 automatic (default), 1 the CUDA-core kernel, 2 the
-     * tensor-core kernel. */
+    /* Varlen kernel: 0 automatic (default: the tcgen05 kernel where it
+     * applies, else the CUDA-core kernel), 1 the CUDA-core kernel, 2 the
+     * mma.sync tensor-core kernel, 3 the tcgen05 (tensor-memory) kernel. */
     PA_OPT_VARLEN_KERNEL = 3
 } pa_option;
 

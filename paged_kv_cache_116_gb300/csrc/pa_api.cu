@@ -109,6 +109,8 @@ const char* pa_last_error(void) { return g_last_error.c_str(); }
 
 pa_status pa_set_option(int option, int64_t value) {
     if (option < 0 || option > PA_OPT_VARLEN_KERNEL) return fail(PA_ERR_INVALID_ARG, "unknown option");
+    if ((option == PA_OPT_DECODE_KERNEL && value > 2) || (option == PA_OPT_VARLEN_KERNEL && value > 3))
+        return fail(PA_ERR_INVALID_ARG, "unknown kernel choice");
     if (value < 0) return fail(PA_ERR_INVALID_ARG, "option values are non-negative");
     g_options[option] = value;
     return PA_OK;
@@ -124,7 +126,8 @@ pa_status pa_set_check_mode(int on) { return pa_set_option(PA_OPT_CHECK_MODE, on
 pa_status pa_device_status(int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pa_device_status");
-    const uint32_t bits = pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0);
+    const uint32_t bits =
+        pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0) | pa::varlen_umma_status(clear != 0);
     if (bits & 1u) return fail(PA_ERR_TIMEOUT, "a kernel's bounded barrier wait ran out");
     return PA_OK;
 }
@@ -357,11 +360,13 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
     const bool tc_ok = pa::varlen_tc_supported(dtype, head_dim, block_size);
+    const bool um_ok = pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
     const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
-    if (want == 2 && !tc_ok)
-        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernel takes bf16/f16, head_dim 64/128 and "
+    if ((want == 2 && !tc_ok) || (want == 3 && !um_ok))
+        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernels take bf16/f16, head_dim 64/128 and "
                                         "block_size 16");
-    const bool use_tc = tc_ok && want != 1;
+    const bool use_um = um_ok && (want == 3 || want == 0);
+    const bool use_tc = !use_um && tc_ok && (want == 2 || want == 0);
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
         pa_status err = PA_OK;
@@ -398,9 +403,10 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.dtype = dtype;
-    if (use_tc) {
+    if (use_um || use_tc) {
         std::string err;
-        cudaError_t e = pa::launch_varlen_tc(a, num_blocks, &err, st);
+        cudaError_t e = use_um ? pa::launch_varlen_umma(a, num_blocks, &err, st)
+                               : pa::launch_varlen_tc(a, num_blocks, &err, st);
         if (e != cudaSuccess)
             return err.empty() ? cuda_fail(e, "pa_varlen launch") : fail(PA_ERR_CUDA, "pa_varlen: " + err);
         return PA_OK;

@@ -77,4 +77,9 @@ bool varlen_tc_supported(int dtype, int head_dim, int block_size);
 cudaError_t launch_varlen_tc(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream);
 uint32_t varlen_tc_status(bool clear);
 
+// ---- tcgen05 varlen (pa_varlen_umma.cu)
+bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group);
+cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream);
+uint32_t varlen_umma_status(bool clear);
+
 }  // namespace pa

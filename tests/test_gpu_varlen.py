@@ -116,31 +116,41 @@ for _i in range(12):
 
 
 @pytest.mark.parametrize("dt,hd,g,hkv,lens,qlens,seed", TC_CASES)
-def test_random_varlen_tensor_core_kernel(pa, dt, hd, g, hkv, lens, qlens, seed):
+def test_random_varlen_tensor_core_kernels(pa, dt, hd, g, hkv, lens, qlens, seed):
+    """Both tensor-core kernels: mma.sync (2) and tcgen05 with tensor memory (3)."""
     w = W.varlen_workload("rand_tc", dt, 16, g * hkv, hkv, hd, lens, qlens, seed=100 + seed)
     kc, vc, bt = device_caches(w, DEV)
     for causal in (True, False):
         exact = oracle_attention(w, causal=causal)
-        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2), exact)
+        for kernel in (2, 3):
+            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=kernel), exact)
 
 
 def test_varlen_kernels_agree_on_mixed_step(pa):
     w = W.mixed_varlen(num_chunks=4, num_groups=6, device=DEV)
     kc, vc, bt = device_caches(w, DEV)
-    a = run_varlen(pa, w, kc, vc, bt, kernel=1).double().cpu().numpy()
-    b = run_varlen(pa, w, kc, vc, bt, kernel=2).double().cpu().numpy()
     exact = oracle_attention(w)
-    assert within_tol(a, exact, w.dtype)[0] and within_tol(b, exact, w.dtype)[0]
+    for kernel in (1, 2, 3):
+        got = run_varlen(pa, w, kc, vc, bt, kernel=kernel).double().cpu().numpy()
+        assert within_tol(got, exact, w.dtype)[0], "kernel %d" % kernel
 
 
-def test_varlen_permutation_bit_identical(pa):
+def test_mixed_varlen_full_tcgen05(pa):
+    w = W.mixed_varlen(device=DEV)
+    kc, vc, bt = device_caches(w, DEV)
+    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=3), oracle_attention(w))
+    pa.pa_device_status(clear=True)
+
+
+@pytest.mark.parametrize("kernel", [2, 3])
+def test_varlen_permutation_bit_identical(pa, kernel):
     w = W.varlen_workload("perm_v", "bf16", 16, 12, 2, 128, [300, 81, 17, 1000], [1, 81, 5, 130], seed=3)
     kc, vc, bt = device_caches(w, DEV)
-    base = run_varlen(pa, w, kc, vc, bt, kernel=2)
+    base = run_varlen(pa, w, kc, vc, bt, kernel=kernel)
     perm = torch.from_numpy(np.random.default_rng(4).permutation(w.num_blocks)).to(DEV)
     kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
     kc2[perm] = kc
     vc2[perm] = vc
     bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
-    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=2)
+    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=kernel)
     assert torch.equal(base.view(torch.int16), again.view(torch.int16))
