@@ -12,16 +12,16 @@
 // share every K/V tile.  Roles:
 //   warp 4 (one lane)   TMA: the Q tile once, then 64-key K/V tiles (four
 //                       16-token blocks through the block table) into a
-//                       3-stage ring;
+//                       2-stage ring (two CTAs share an SM);
 //   warp 5 (one lane)   issues tcgen05.mma: S = Q K^T (M 128, N 64, K = hd)
 //                       into tensor memory, then O += P V (M 128, N hd, K 64)
 //                       with V read MN-major; completion via tcgen05.commit;
 //   warps 0-3           one query row per thread: read S from tensor memory,
-//                       causal mask, exp2-domain online softmax, P to shared
-//                       memory (128-byte swizzled, the MMA's A operand); O is
-//                       rescaled in tensor memory only when a row's running
-//                       maximum grows by more than 2^8, and normalised and
-//                       stored at the end.
+//                       causal mask, exp2-domain online softmax, P (bf16/f16)
+//                       written back to tensor memory as the A operand of
+//                       P V; O is rescaled in tensor memory only when a row's
+//                       running maximum grows by more than 2^8, and
+//                       normalised and stored at the end.
 // S(k+1) is issued as soon as the softmax warps have read S(k), so it runs
 // under their exponentials.  V rows past the context are zeroed in shared
 // memory before P V.  Every wait is bounded in time; on expiry the CTA sets a
@@ -48,10 +48,10 @@ constexpr int BS = 16;          // tokens per block
 constexpr int BK = 64;          // keys per tile
 constexpr int BPT = BK / BS;    // blocks per key tile
 constexpr int TM = 128;         // rows of the MMA tile
-constexpr int R = 3;            // K/V stages
+constexpr int R = 2;            // K/V stages
 constexpr int NTHREADS = 192;   // 4 softmax warps + producer + MMA warp
 constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t S_COL = 0, O_COL = 128;
+constexpr uint32_t S_COL = 0, P_COL = 64, O_COL = 128;  // S 64 fp32 cols, P 32 packed cols, O hd cols
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 constexpr int kMaxSeqsSmem = 8192;
 
@@ -77,8 +77,7 @@ struct UGeo {
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = CH * QCH;
     static constexpr int STAGE = 2 * CH * KCH;  // K chunks, then V chunks
-    static constexpr int P_OFF = KV_OFF + R * STAGE;
-    static constexpr int BAR_OFF = P_OFF + TM * 128;
+    static constexpr int BAR_OFF = KV_OFF + R * STAGE;
     static constexpr int NBAR = 1 + 2 * R + 4;  // q_full, kv_full[R], kv_empty[R], s_full, s_free, p_full, o_done
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int CU_OFF = TADDR_OFF + 16;
@@ -90,7 +89,7 @@ size_t um_smem_bytes(int num_seqs) {
 }
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(NTHREADS, 1)
+__global__ void __launch_bounds__(NTHREADS, 2)
     varlen_umma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const UmParams p) {
     using Gm = UGeo<HD>;
@@ -207,16 +206,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (lane == 0) {
             const uint32_t idS = umma_idesc_f16(TM, BK, kBF16, false);
             const uint32_t idO = umma_idesc_f16(TM, HD, kBF16, true);
-            const uint32_t q_s = s_base + Gm::Q_OFF, p_s = s_base + Gm::P_OFF;
+            const uint32_t q_s = s_base + Gm::Q_OFF;
             auto issue_pv = [&](int j) -> bool {
                 if (!mbar_wait_ns(p_full, (uint32_t)j & 1u, WAIT_NS)) return false;
                 tc_fence_after();
                 const uint32_t v_s = s_base + Gm::KV_OFF + (j % R) * Gm::STAGE + Gm::CH * Gm::KCH;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t a = umma_sdesc_sw128(p_s + kk * 32, 16, 1024);
                     const uint64_t b = umma_sdesc_sw128(v_s + kk * 16 * 128, Gm::KCH, 1024);
-                    umma_f16(tmem + O_COL, a, b, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_f16_ts(tmem + O_COL, tmem + P_COL + kk * 8, b, idO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(o_done);
                 umma_commit(&kv_empty[j % R]);
@@ -250,7 +248,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ti = valid ? m / G : 0, gh = valid ? m - (m / G) * G : 0;
         const int prow = p.causal ? first_pos + t0 + ti : L - 1;
         const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-        uint8_t* p_row = base + Gm::P_OFF + m * 128;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int kt = 0; kt < nkt; ++kt) {
@@ -332,13 +329,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     const int c = e / (rows * 8), rem = e - c * rows * 8, r = keep + rem / 8, q16 = rem & 7;
                     *reinterpret_cast<uint4*>(v_t + c * Gm::KCH + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();
             }
-            // P row: 64 keys = 128 bytes, 16-byte chunks swizzled by row
+            // P row: 64 keys packed two per column into tensor memory
+            {
+                float pf[32];
 #pragma unroll
-            for (int q16 = 0; q16 < 8; ++q16)
-                *reinterpret_cast<uint4*>(p_row + ((q16 ^ (m & 7)) << 4)) =
-                    make_uint4(pk[4 * q16], pk[4 * q16 + 1], pk[4 * q16 + 2], pk[4 * q16 + 3]);
-            fence_proxy_async_smem();
+                for (int j = 0; j < 32; ++j) pf[j] = __uint_as_float(pk[j]);
+                tmem_st32(t_lane + P_COL, pf);
+                tmem_wait_st();
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
