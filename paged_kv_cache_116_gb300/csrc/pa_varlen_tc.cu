@@ -46,6 +46,7 @@ constexpr int BPT = BK / BS;  // blocks per key tile
 constexpr int TM = 64;        // (row, head) pairs per CTA
 constexpr int NC = 4;         // consumer warps (16 pairs each)
 constexpr int kMaxSeqsSmem = 8192;
+constexpr int kTableWindow = 512;  // block-table entries the producer stages at a time
 
 struct VlParams {
     void* out;
@@ -74,7 +75,7 @@ struct VGeo {
 
 template <int HD>
 constexpr size_t vl_smem_bytes(int num_seqs) {
-    return 1024 + (size_t)VGeo<HD>::R * VGeo<HD>::STAGE + (size_t)VGeo<HD>::R * 16 +
+    return 1024 + (size_t)VGeo<HD>::R * VGeo<HD>::STAGE + (size_t)VGeo<HD>::R * 16 + kTableWindow * 4 +
            (size_t)((num_seqs < kMaxSeqsSmem ? num_seqs : kMaxSeqsSmem) + 1) * 4;
 }
 
@@ -95,7 +96,8 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(base + (size_t)R * Gm::STAGE);
     uint64_t* empty = full + R;
-    int32_t* cu_s = reinterpret_cast<int32_t*>(empty + R);
+    int32_t* tbl_s = reinterpret_cast<int32_t*>(empty + R);
+    int32_t* cu_s = tbl_s + kTableWindow;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, G = p.group;
@@ -143,39 +145,45 @@ __global__ void __launch_bounds__((NC + 1) * 32)
     __syncthreads();
 
     if (warp == NC) {
-        // ---------------- producer
+        // ---------------- producer: the whole warp stages block-table
+        // windows (one round trip per 128 tiles), lane 0 issues the TMA loads
         if (lane == 0) {
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const uint64_t pol = l2_policy_evict_last();
-            for (int kt = 0; kt < nkt; ++kt) {
-                const int slot = kt % R;
-                if (!mbar_wait_bounded(&empty[slot], ((uint32_t)(kt / R) & 1u) ^ 1u, kMaxPolls)) {
-                    atomicOr(&g_varlen_status, kStatusTimeout);
-                    break;
-                }
-                int32_t phys[BPT];
-                int nvalid = 0;
+        }
+        const uint64_t pol = l2_policy_evict_last();
+        const int nblk = min(nb_seq, nkt * BPT);
+        bool run = true;
+        for (int w0 = 0; w0 < nblk && run; w0 += kTableWindow) {
+            const int wn = min(kTableWindow, nblk - w0);
+            for (int i = lane; i < wn; i += 32) tbl_s[i] = table[w0 + i];
+            __syncwarp();
+            if (lane == 0) {
+                const int kt_end = min(nkt, (w0 + wn + BPT - 1) / BPT);
+                for (int kt = w0 / BPT; kt < kt_end; ++kt) {
+                    const int slot = kt % R;
+                    if (!mbar_wait_bounded(&empty[slot], ((uint32_t)(kt / R) & 1u) ^ 1u, kMaxPolls)) {
+                        atomicOr(&g_varlen_status, kStatusTimeout);
+                        run = false;
+                        break;
+                    }
+                    const int nvalid = min(BPT, nb_seq - kt * BPT);
+                    uint8_t* dst = base + (size_t)slot * Gm::STAGE;
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(nvalid * 2 * Gm::CH * Gm::BLK));
+                    for (int j = 0; j < nvalid; ++j) {  // blocks past the context are never read
+                        const int row = tbl_s[kt * BPT + j - w0] * BS;
 #pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    const int b = kt * BPT + j;
-                    phys[j] = b < nb_seq ? table[b] : -1;
-                    nvalid += b < nb_seq ? 1 : 0;
-                }
-                uint8_t* dst = base + (size_t)slot * Gm::STAGE;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&full[slot], (uint32_t)(nvalid * 2 * Gm::CH * Gm::BLK));
-#pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    if (kt * BPT + j >= nb_seq) continue;  // past the context: never read
-#pragma unroll
-                    for (int c = 0; c < Gm::CH; ++c) {
-                        const int off = (c * BPT + j) * Gm::BLK;
-                        tma_load_3d(dst + off, &tmK, &full[slot], 0, kvh * Gm::CH + c, phys[j] * BS, pol);
-                        tma_load_3d(dst + Gm::TILE + off, &tmV, &full[slot], 0, kvh * Gm::CH + c, phys[j] * BS, pol);
+                        for (int c = 0; c < Gm::CH; ++c) {
+                            const int off = (c * BPT + j) * Gm::BLK;
+                            tma_load_3d(dst + off, &tmK, &full[slot], 0, kvh * Gm::CH + c, row, pol);
+                            tma_load_3d(dst + Gm::TILE + off, &tmV, &full[slot], 0, kvh * Gm::CH + c, row, pol);
+                        }
                     }
                 }
             }
+            run = __shfl_sync(0xffffffffu, run ? 1 : 0, 0) != 0;
+            __syncwarp();
         }
         return;
     }

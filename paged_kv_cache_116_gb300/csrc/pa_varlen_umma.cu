@@ -10,9 +10,11 @@
 // A CTA takes one KV head and T = floor(128 / G) consecutive new tokens of one
 // request, i.e. a 128-row tile of (token, group head) pairs -- the G heads
 // share every K/V tile.  Roles:
-//   warp 4 (one lane)   TMA: the Q tile once, then 64-key K/V tiles (four
-//                       16-token blocks through the block table) into a
-//                       2-stage ring (two CTAs share an SM);
+//   warp 4              TMA: the Q tile once, then 64-key K and V tiles (four
+//                       16-token blocks through the block table, staged in
+//                       windows of 512 entries) into separate 2-slot K and V
+//                       rings, so the next K tile loads as soon as its S is
+//                       done, not after P V (two CTAs share an SM);
 //   warp 5 (one lane)   issues tcgen05.mma: S = Q K^T (M 128, N 64, K = hd)
 //                       into tensor memory, then O += P V (M 128, N hd, K 64)
 //                       with V read MN-major; completion via tcgen05.commit;
@@ -54,6 +56,7 @@ constexpr uint32_t TMEM_COLS = 256;
 constexpr uint32_t S_COL = 0, P_COL = 64, O_COL = 128;  // S 64 fp32 cols, P 32 packed cols, O hd cols
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 constexpr int kMaxSeqsSmem = 8192;
+constexpr int kTableWindow = 512;  // block-table entries the producer stages at a time
 
 struct UmParams {
     void* out;
@@ -76,11 +79,14 @@ struct UGeo {
     static constexpr int KCH = BK * 128;        // bytes of one chunk of a K (or V) tile
     static constexpr int Q_OFF = 0;
     static constexpr int KV_OFF = CH * QCH;
-    static constexpr int STAGE = 2 * CH * KCH;  // K chunks, then V chunks
-    static constexpr int BAR_OFF = KV_OFF + R * STAGE;
-    static constexpr int NBAR = 1 + 2 * R + 4;  // q_full, kv_full[R], kv_empty[R], s_full, s_free, p_full, o_done
+    static constexpr int TILE = CH * KCH;       // bytes of a K (or V) tile
+    static constexpr int V_OFF = KV_OFF + R * TILE;
+    static constexpr int BAR_OFF = V_OFF + R * TILE;
+    // q_full, k_full[R], k_empty[R], v_full[R], v_empty[R], s_full, s_free, p_full, o_done
+    static constexpr int NBAR = 1 + 4 * R + 4;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int CU_OFF = TADDR_OFF + 16;
+    static constexpr int TBL_OFF = TADDR_OFF + 16;          // window of block-table entries
+    static constexpr int CU_OFF = TBL_OFF + kTableWindow * 4;
 };
 
 template <int HD>
@@ -98,15 +104,18 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::BAR_OFF);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = bars + 1 + R;
-    uint64_t* s_full = bars + 1 + 2 * R;
+    uint64_t* k_full = bars + 1;
+    uint64_t* k_empty = bars + 1 + R;
+    uint64_t* v_full = bars + 1 + 2 * R;
+    uint64_t* v_empty = bars + 1 + 3 * R;
+    uint64_t* s_full = bars + 1 + 4 * R;
     uint64_t* s_free = s_full + 1;
     uint64_t* p_full = s_full + 2;
     uint64_t* o_done = s_full + 3;
     volatile uint32_t* taddr_slot = reinterpret_cast<volatile uint32_t*>(base + Gm::TADDR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Gm::TADDR_OFF + 4);
     int32_t* cu_s = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);
+    int32_t* tbl_s = reinterpret_cast<int32_t*>(base + Gm::TBL_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, G = p.group, TT = p.tokens_per_tile;
@@ -161,45 +170,60 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     };
 
     if (warp == 4) {
-        // ---------------- producer
+        // ---------------- producer: the whole warp stages block-table
+        // windows (one round trip per 128 tiles), lane 0 issues the TMA loads
+        const uint64_t pol = l2_policy_evict_last();
         if (lane == 0) {
             prefetch_tmap(&tmQ);
             prefetch_tmap(&tmK);
             prefetch_tmap(&tmV);
-            const uint64_t pol = l2_policy_evict_last();
             mbar_arrive_expect_tx(q_full, (uint32_t)(Gm::CH * 128 * G * TT));
 #pragma unroll
             for (int c = 0; c < Gm::CH; ++c)
                 tma_load_3d(base + Gm::Q_OFF + c * Gm::QCH, &tmQ, q_full, 64 * c, kvh * G, q0 + t0, pol);
-            for (int kt = 0; kt < nkt && !*abort_flag; ++kt) {
-                const int slot = kt % R;
-                if (!mbar_wait_ns(&kv_empty[slot], ((uint32_t)(kt / R) & 1u) ^ 1u, WAIT_NS)) {
-                    fail();
-                    break;
-                }
-                int32_t phys[BPT];
-                int nvalid = 0;
-#pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    const int b = kt * BPT + j;
-                    phys[j] = b < nb_seq ? p.block_tables[(int64_t)req * p.max_blocks + b] : 0;
-                    nvalid += b < nb_seq ? 1 : 0;
-                }
-                uint8_t* st = base + Gm::KV_OFF + slot * Gm::STAGE;
-                fence_proxy_async_smem();
-                mbar_arrive_expect_tx(&kv_full[slot], (uint32_t)(nvalid * 2 * Gm::CH * BS * 128));
-#pragma unroll
-                for (int j = 0; j < BPT; ++j) {
-                    if (kt * BPT + j >= nb_seq) continue;  // past the context: never read
-#pragma unroll
-                    for (int c = 0; c < Gm::CH; ++c) {
-                        const int off = c * Gm::KCH + j * BS * 128;
-                        tma_load_3d(st + off, &tmK, &kv_full[slot], 0, kvh * Gm::CH + c, phys[j] * BS, pol);
-                        tma_load_3d(st + Gm::CH * Gm::KCH + off, &tmV, &kv_full[slot], 0, kvh * Gm::CH + c,
-                                    phys[j] * BS, pol);
+        }
+        const int nblk = min(nb_seq, nkt * BPT);
+        const int32_t* table = p.block_tables + (int64_t)req * p.max_blocks;
+        bool run = true;
+        for (int w0 = 0; w0 < nblk && run; w0 += kTableWindow) {
+            const int wn = min(kTableWindow, nblk - w0);
+            for (int i = lane; i < wn; i += 32) tbl_s[i] = table[w0 + i];
+            __syncwarp();
+            if (lane == 0) {
+                const int kt_end = min(nkt, (w0 + wn + BPT - 1) / BPT);
+                for (int kt = w0 / BPT; kt < kt_end; ++kt) {
+                    if (*abort_flag) {
+                        run = false;
+                        break;
                     }
+                    const int slot = kt % R;
+                    const uint32_t par = ((uint32_t)(kt / R) & 1u) ^ 1u;
+                    const int nvalid = min(BPT, nb_seq - kt * BPT);
+                    const uint32_t bytes = (uint32_t)(nvalid * Gm::CH * BS * 128);
+                    for (int half = 0; half < 2 && run; ++half) {  // K tile, then V tile
+                        uint64_t* emp = half ? &v_empty[slot] : &k_empty[slot];
+                        uint64_t* ful = half ? &v_full[slot] : &k_full[slot];
+                        if (!mbar_wait_ns(emp, par, WAIT_NS)) {
+                            fail();
+                            run = false;
+                            break;
+                        }
+                        uint8_t* st = base + (half ? Gm::V_OFF : Gm::KV_OFF) + slot * Gm::TILE;
+                        fence_proxy_async_smem();
+                        mbar_arrive_expect_tx(ful, bytes);
+                        for (int j = 0; j < nvalid; ++j) {  // blocks past the context are never read
+                            const int row = tbl_s[kt * BPT + j - w0] * BS;
+#pragma unroll
+                            for (int c = 0; c < Gm::CH; ++c)
+                                tma_load_3d(st + c * Gm::KCH + j * BS * 128, half ? &tmV : &tmK, ful, 0,
+                                            kvh * Gm::CH + c, row, pol);
+                        }
+                    }
+                    if (!run) break;
                 }
             }
+            run = __shfl_sync(0xffffffffu, run ? 1 : 0, 0) != 0;
+            __syncwarp();
         }
     } else if (warp == 5) {
         // ---------------- MMA issuer
@@ -208,26 +232,28 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             const uint32_t idO = umma_idesc_f16(TM, HD, kBF16, true);
             const uint32_t q_s = s_base + Gm::Q_OFF;
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_ns(p_full, (uint32_t)j & 1u, WAIT_NS)) return false;
+                if (!mbar_wait_ns(&v_full[j % R], (uint32_t)(j / R) & 1u, WAIT_NS) ||
+                    !mbar_wait_ns(p_full, (uint32_t)j & 1u, WAIT_NS))
+                    return false;
                 tc_fence_after();
-                const uint32_t v_s = s_base + Gm::KV_OFF + (j % R) * Gm::STAGE + Gm::CH * Gm::KCH;
+                const uint32_t v_s = s_base + Gm::V_OFF + (j % R) * Gm::TILE;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk) {
                     const uint64_t b = umma_sdesc_sw128(v_s + kk * 16 * 128, Gm::KCH, 1024);
                     umma_f16_ts(tmem + O_COL, tmem + P_COL + kk * 8, b, idO, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 umma_commit(o_done);
-                umma_commit(&kv_empty[j % R]);
+                umma_commit(&v_empty[j % R]);
                 return true;
             };
             bool ok = mbar_wait_ns(q_full, 0, WAIT_NS);
             for (int kt = 0; ok && kt < nkt && !*abort_flag; ++kt) {
                 const int slot = kt % R;
-                ok = mbar_wait_ns(&kv_full[slot], (uint32_t)(kt / R) & 1u, WAIT_NS) &&
+                ok = mbar_wait_ns(&k_full[slot], (uint32_t)(kt / R) & 1u, WAIT_NS) &&
                      (kt == 0 || mbar_wait_ns(s_free, (uint32_t)(kt - 1) & 1u, WAIT_NS));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t k_s = s_base + Gm::KV_OFF + slot * Gm::STAGE;
+                const uint32_t k_s = s_base + Gm::KV_OFF + slot * Gm::TILE;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const int c = kk >> 2, koff = (kk & 3) * 32;
@@ -236,6 +262,7 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     umma_f16(tmem + S_COL, a, b, idS, kk > 0 ? 1u : 0u);
                 }
                 umma_commit(s_full);
+                umma_commit(&k_empty[slot]);
                 if (kt > 0) ok = issue_pv(kt - 1);
             }
             if (ok && !*abort_flag) ok = issue_pv(nkt - 1);
@@ -323,7 +350,12 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             // keys at or past L hold no context: zero their V rows of this stage
             const int keep = L - kbase;
             if (keep < BK) {
-                uint8_t* v_t = base + Gm::KV_OFF + (kt % R) * Gm::STAGE + Gm::CH * Gm::KCH;
+                // this tile's V must have landed before its tail rows are cleared
+                if (!mbar_wait_ns(&v_full[kt % R], (uint32_t)(kt / R) & 1u, WAIT_NS)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* v_t = base + Gm::V_OFF + (kt % R) * Gm::TILE;
                 const int rows = BK - keep;
                 for (int e = threadIdx.x; e < rows * Gm::CH * 8; e += 128) {
                     const int c = e / (rows * 8), rem = e - c * rows * 8, r = keep + rem / 8, q16 = rem & 7;
