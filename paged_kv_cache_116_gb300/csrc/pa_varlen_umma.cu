@@ -300,28 +300,53 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             if (lane == 0) mbar_arrive(s_free);
 
             const int kbase = kt * BK;
+            // Raw scores; the mask only applies on tiles that reach past the
+            // row's last visible key (the causal diagonal or the context end).
+            // Rows past the request's pairs hold no query: flat zero scores,
+            // so they never force a rescale of the warp.
             float mx = -INFINITY;
+            if (!valid) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                // rows past the request's pairs hold no query: give them flat
-                // finite scores so they never force a rescale of the warp
-                float x = valid ? sv[j] * p.scale_log2 : 0.f;
-                if (valid && kbase + j > prow) x = -INFINITY;
-                sv[j] = x;
-                mx = fmaxf(mx, x);
+                for (int j = 0; j < 64; ++j) sv[j] = 0.f;
+                mx = 0.f;
+            } else if (kbase + BK - 1 > prow) {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    const float x = kbase + j > prow ? -INFINITY : sv[j];
+                    sv[j] = x;
+                    mx = fmaxf(mx, x);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
             }
-            const float m_new = fmaxf(m_used, mx);
+            // exp2 domain: x = s * scale * log2(e); a positive scale keeps the
+            // order, so the maximum is taken on raw scores and the scaling is
+            // fused into the exponent's argument
+            const float sl = p.scale_log2;
+            float m_tile;
+            if (sl > 0.f) {
+                m_tile = mx * sl;
+            } else {
+                m_tile = -INFINITY;
+#pragma unroll
+                for (int j = 0; j < 64; ++j) m_tile = fmaxf(m_tile, sv[j] == -INFINITY ? -INFINITY : sv[j] * sl);
+            }
+            const float m_new = fmaxf(m_used, m_tile);
             const bool grow = (m_used == -INFINITY) || (m_new > m_used + 8.f);
             float alpha = 1.f;
             if (grow) {
                 alpha = fast_exp2(m_used - m_new);
                 m_used = m_new;
             }
+            const float neg_m = -m_used;
             float sum = 0.f;
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float e0 = fast_exp2(sv[2 * j] - m_used), e1 = fast_exp2(sv[2 * j + 1] - m_used);
+                const float a0 = sv[2 * j] == -INFINITY ? -INFINITY : fmaf(sv[2 * j], sl, neg_m);
+                const float a1 = sv[2 * j + 1] == -INFINITY ? -INFINITY : fmaf(sv[2 * j + 1], sl, neg_m);
+                const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
                 sum += e0 + e1;
                 pk[j] = pack2<T>(e0, e1);
             }
