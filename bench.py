@@ -1,8 +1,10 @@
 """Benchmark of the paged-KV hot path (default: the 64-sequence GQA decode batch).
 
 A step is one pass of the path over one batch, through the C ABI:
-  decode workloads: pa_slot_mapping (each sequence's new token) ->
-                    pa_write_kv (its K/V row) -> pa_decode
+  decode workloads: pa_decode_append -- each sequence's new token is written
+                    at its translated slot and the batch is decoded, in one
+                    launch (--unfused: pa_slot_mapping -> pa_write_kv ->
+                    pa_decode, three launches; both times are reported)
   mixed_varlen:     pa_copy_blocks (copy-on-write of the shared tails) ->
                     pa_slot_mapping -> pa_write_kv (every new token) ->
                     pa_varlen (prefill chunks + decode rows)
@@ -53,6 +55,8 @@ def parse():
     ap.add_argument("--workload", choices=WORKLOADS, default="gqa_decode_batch")
     ap.add_argument("--no-rotate", action="store_true", help="one pool copy (for profiling)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, clocks and cpu_baseline")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode step as pa_slot_mapping + pa_write_kv + pa_decode instead of pa_decode_append")
     return ap.parse_args()
 
 
@@ -318,8 +322,9 @@ def main():
             pa.pa_varlen(out, qq, kc, vc, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
                          workspace=ws, stream=st)
 
-    def run_step(i, t_in):
-        """One pass of the path through the C ABI on the current stream."""
+    fused = decode and not args.unfused
+
+    def run_step_unfused(i, t_in):
         kc, vc = pools[i % copies]
         st = torch.cuda.current_stream()
         d_q, d_k, d_v, d_bt, d_lens, d_cu, d_seq, d_pos, d_pairs = t_in
@@ -329,7 +334,18 @@ def main():
         pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=st)
         attend(kc, vc, d_q, d_bt, d_lens, d_cu, st)
 
+    def run_step(i, t_in):
+        """One pass of the path through the C ABI on the current stream."""
+        if not fused:
+            return run_step_unfused(i, t_in)
+        kc, vc = pools[i % copies]
+        d_q, d_k, d_v, d_bt, d_lens = t_in[:5]
+        pa.pa_decode_append(out, d_q, d_k, d_v, kc, vc, d_bt, d_lens, max_ctx, w.scale, workspace=ws,
+                            stream=torch.cuda.current_stream())
+
     dev_in = (q, new_k, new_v, bt, lens, cu, seq_idx, pos, pairs)
+    if fused:
+        dev_in = dev_in[:5]  # a fused step reads q, the new rows, the tables and the lengths
 
     def step(i):
         run_step(i, dev_in)
@@ -338,7 +354,8 @@ def main():
         kc, vc = pools[i % copies]
         attend(kc, vc, q, bt, lens, cu, torch.cuda.current_stream())
 
-    launches_per_step = 3 + (1 if pairs.shape[0] else 0)
+    tc_decode = decode and w.dtype != "f32"
+    launches_per_step = (1 if tc_decode else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -354,6 +371,8 @@ def main():
         return gs
 
     step_graphs, kern_graphs = capture(step), capture(kernel_only)
+    unfused_graphs = capture(lambda i: run_step_unfused(i, (q, new_k, new_v, bt, lens, cu, seq_idx, pos, pairs))) \
+        if fused else None
     for i in range(max(args.warmup, 3)):
         step_graphs[i % copies].replay()
         kern_graphs[i % copies].replay()
@@ -380,6 +399,8 @@ def main():
     ms = timed(lambda i: step_graphs[i % copies].replay(), args.steps)
     clk = clocks.stop() if rank == 0 and not args.no_extras else None
     kern_ms = timed(lambda i: kern_graphs[i % copies].replay(), args.steps) / args.steps
+    unfused_ms = (timed(lambda i: unfused_graphs[i % copies].replay(), args.steps) / args.steps
+                  if unfused_graphs else None)
     eager_steps = min(args.steps, 2000)
     eager_ms = timed(step, eager_steps) / eager_steps
     if world > 1:
@@ -454,11 +475,13 @@ def main():
                        "total_context": int(w.seq_lens.sum()), "cow_pairs": int(w.cow_pairs.shape[0]),
                        "kv_bytes_per_step": kv_bytes,
                        "l2": l2_note,
-                       "step": ("pa_copy_blocks + " if pairs.shape[0] else "") +
-                               "pa_slot_mapping + pa_write_kv + " + ("pa_decode" if decode else "pa_varlen") +
-                               ", replayed as a CUDA graph", "seed": 0},
+                       "step": ("pa_decode_append (slot translation + K/V write + decode, one call)" if fused else
+                                ("pa_copy_blocks + " if pairs.shape[0] else "") + "pa_slot_mapping + pa_write_kv + " +
+                                ("pa_decode" if decode else "pa_varlen")) + ", replayed as a CUDA graph",
+                       "seed": 0},
             "seq_per_s": seq_per_s,
             "eager_ms_per_step": eager_ms,
+            "unfused_ms_per_step": unfused_ms,
             "roofline": roof,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,

@@ -174,6 +174,28 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_append -- one generation step of a decode batch in one call:
+ * for each sequence s with L = context_lens[s] >= 1 (L counts the new
+ * token), the new token's rows k_new[s], v_new[s] are written to the slot of
+ * position L-1, block_tables[s][(L-1) / block_size] * block_size +
+ * (L-1) % block_size ("分页 KV Cache", §块表与 slot mapping and
+ * PagedKVCache.write), and out[s] is the decode attention over positions
+ * 0..L-1 exactly as pa_decode computes it after that write ("分页 KV Cache",
+ * §分页注意力: the step writes the new K/V, then attends).  Equivalent to
+ * pa_slot_mapping + pa_write_kv + pa_decode; on the tensor-core path it is
+ * one kernel launch.  Sequences with L = 0 get a zero row and no write.
+ *   k_new, v_new: device [num_seqs, num_kv_heads, head_dim] of dtype, 16-byte aligned
+ *   k_cache, v_cache: written at one slot per sequence (the other arguments
+ *   as for pa_decode, same workspace size).
+ */
+PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new,
+                                  void* k_cache, void* v_cache, const int32_t* block_tables,
+                                  int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs,
+                                  int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t num_blocks, int32_t block_size, int32_t max_context, float scale,
+                                  int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_varlen -- the handbook's paged_attention: a batch of requests, each
  * with seq_lens[i] tokens of context after this step of which the last
  * n_i = cu_seqlens_q[i+1] - cu_seqlens_q[i] are new; request i's queries

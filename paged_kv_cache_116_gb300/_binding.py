@@ -19,7 +19,7 @@ DTYPE_CODE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_
 
 EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
-           "pa_decode", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc")
+           "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc")
 
 
 class PAError(RuntimeError):
@@ -53,6 +53,8 @@ def lib():
         "pa_copy_blocks": ([vp, vp, i32, vp, i32, i32, i32, i32, i32, ci, vp], ci),
         "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
         "pa_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz, vp], ci),
+        "pa_decode_append": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz,
+                              vp], ci),
         "pa_varlen_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32, ci], sz),
         "pa_decode_noalloc": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp], ci),
         "pa_varlen": ([vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, cf, ci, ci, vp,
@@ -164,6 +166,22 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context,
                          block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb, bs, max_context,
                          float(scale), _dtype(q), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_append(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, max_context, scale,
+                     workspace=None, stream=None):
+    """Write each sequence's new token (position L-1) into the pool and
+    decode: out, q [S, Hq, hd]; k_new, v_new [S, Hkv, hd]."""
+    _dev(out, q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, workspace)
+    nb, bs, hkv, hd = k_cache.shape
+    S, hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_decode_append(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb,
+                                bs, max_context, float(scale), _dtype(q), _ptr(workspace), ws_bytes,
+                                _stream(stream))
+    _check(st, "pa_decode_append")
     return out
 
 

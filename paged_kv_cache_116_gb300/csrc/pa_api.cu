@@ -258,7 +258,10 @@ size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num
     return pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid);
 }
 
-pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+}  // extern "C"
+
+static pa_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
+                             const void* v_cache, const int32_t* block_tables,
                     int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
                     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                     int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
@@ -270,6 +273,12 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "null pointer");
+    const bool append = k_new != nullptr || v_new != nullptr;
+    if (append && (!k_new || !v_new)) return fail(PA_ERR_INVALID_ARG, "k_new and v_new go together");
+    if (append && (!aligned16(k_new) || !aligned16(v_new)))
+        return fail(PA_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+    if (append && ((int64_t)num_kv_heads * head_dim * pa::elt_size(dtype)) % 16 != 0)
+        return fail(PA_ERR_UNSUPPORTED, "num_kv_heads * head_dim * element size must be a multiple of 16 bytes");
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
@@ -301,10 +310,17 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
     a.dtype = dtype;
 
     const int G = num_heads / num_kv_heads;
+    const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * pa::elt_size(dtype);
     pa_status sel;
     const bool tc = use_decode_tc(dtype, head_dim, block_size, G, &sel);
     if (sel != PA_OK) return sel;
     if (!tc) {
+        if (append) {  // write the new rows first, then attend from the pool
+            cudaError_t e = pa::launch_append_kv(k_new, v_new, block_tables, max_blocks, context_lens, num_seqs,
+                                                 block_size, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                                                 row_bytes, st);
+            if (e != cudaSuccess) return cuda_fail(e, "pa_decode_append launch");
+        }
         cudaError_t e = pa::launch_attn_simt(a, st);
         return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_decode launch");
     }
@@ -325,12 +341,39 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
         c.q = static_cast<const uint8_t*>(q) + (int64_t)s0 * num_heads * head_dim * elt;
         c.block_tables = block_tables + (int64_t)s0 * max_blocks;
         c.seq_lens = context_lens + s0;
+        if (append) {
+            c.k_new = static_cast<const uint8_t*>(k_new) + (int64_t)s0 * row_bytes;
+            c.v_new = static_cast<const uint8_t*>(v_new) + (int64_t)s0 * row_bytes;
+        }
         std::string err;
         cudaError_t e = pa::launch_decode_tc(c, num_blocks, grid, workspace, &err, st);
         if (e != cudaSuccess)
             return err.empty() ? cuda_fail(e, "pa_decode launch") : fail(PA_ERR_CUDA, "pa_decode: " + err);
     }
     return PA_OK;
+}
+
+extern "C" {
+
+pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                    int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+    return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context, scale, dtype,
+                       workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                           void* v_cache, const int32_t* block_tables, int32_t max_blocks,
+                           const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t num_blocks, int32_t block_size, int32_t max_context,
+                           float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new)) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context, scale, dtype,
+                       workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ varlen

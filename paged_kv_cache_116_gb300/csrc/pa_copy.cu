@@ -61,6 +61,26 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     for (int64_t e = lane; e < row_vecs; e += 32) dst[e] = ld_nc_v4(src + e);
 }
 
+// One warp per (sequence, K|V): the new token's row goes to the slot of
+// position L-1, translated through the sequence's block table.
+__global__ void __launch_bounds__(kWriteWarps * 32)
+    append_kv_kernel(const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
+                     const int32_t* __restrict__ block_tables, int32_t max_blocks,
+                     const int32_t* __restrict__ context_lens, int32_t num_seqs, int32_t block_size,
+                     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t row_vecs) {
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t s = blockIdx.x * (int64_t)(kWriteWarps / 2) + (warp >> 1);
+    if (s >= num_seqs) return;
+    const int32_t L = context_lens[s];
+    if (L <= 0) return;
+    const int64_t pos = L - 1, logical = pos / block_size;
+    const int64_t slot = (int64_t)block_tables[s * max_blocks + logical] * block_size + (pos - logical * block_size);
+    const uint4* src = ((warp & 1) ? v_new : k_new) + s * row_vecs;
+    uint4* dst = ((warp & 1) ? v_cache : k_cache) + slot * row_vecs;
+    for (int64_t e = lane; e < row_vecs; e += 32) dst[e] = ld_nc_v4(src + e);
+}
+
 // One CTA per (pair, layer); its threads stride over the K and V blocks.
 struct CopyPtrs {
     uint4* k[PA_MAX_LAYERS_INTERNAL];
@@ -105,6 +125,17 @@ cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_ma
     write_kv_kernel<<<(unsigned)blocks, kWriteWarps * 32, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n, static_cast<uint4*>(k_cache),
         static_cast<uint4*>(v_cache), row_bytes / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t block_size, void* k_cache,
+                             void* v_cache, int64_t row_bytes, cudaStream_t stream) {
+    if (num_seqs == 0) return cudaSuccess;
+    const int64_t per_cta = kWriteWarps / 2;
+    append_kv_kernel<<<(unsigned)((num_seqs + per_cta - 1) / per_cta), kWriteWarps * 32, 0, stream>>>(
+        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, max_blocks, context_lens,
+        num_seqs, block_size, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), row_bytes / 16);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,11 @@
 //    movmatrix and O^T += V^T P^T accumulates in fp32 registers.
 //  * Tokens past L in a sequence's last block are masked (scores to -inf,
 //    V operand lanes to zero) so whatever the unused slots hold never leaks.
+//  * Append mode fuses the generation step: the warp that owns a unit's
+//    last block patches the new token's K/V row (prefetched from the inputs)
+//    into the staged tile before its MMAs and stores the same row to the pool
+//    at slot = table[(L-1) / 16] * 16 + (L-1) % 16 ("分页 KV Cache", §块表与
+//    slot mapping) -- slot translation, write and attention in one launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -63,6 +68,13 @@ struct TcParams {
     unsigned long long* ws_cnt;  // [num_seqs * num_kv_heads] (epoch << 16) | partials done
     float* ws_part;              // [total_warps][2] records of group * (HD + 4) floats
     unsigned long long epoch;    // this launch's tag, < 2^48, never reused by the process
+    // append mode (k_new != nullptr): each sequence's token at position L-1
+    // arrives in k_new / v_new [num_seqs, Hkv, HD]; it is written to the pool
+    // and attended from these rows, not from the pool
+    const void* k_new;
+    const void* v_new;
+    void* k_pool;
+    void* v_pool;
 };
 
 template <int HD>
@@ -233,6 +245,12 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
     float acc[KS][NT][4];
     float mrow[NT][2], lrow[NT][2];
     uint32_t qb[KS][NT][2];
+    // append mode: this lane's 16-byte pieces of the new K and V rows of the
+    // unit's head (HD / 8 pieces each), and the pool block holding position L-1
+    constexpr int PPT = HD / 8;
+    constexpr int NPC = (2 * PPT + 31) / 32;
+    uint4 newp[NPC];
+    int32_t last_phys = 0;
 
     int cs, ch, cb;
     locate(f0, cs, ch, cb);
@@ -260,6 +278,19 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
             lrow[nt][0] = lrow[nt][1] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
+        }
+        if (p.k_new != nullptr) {
+#pragma unroll
+            for (int k = 0; k < NPC; ++k) {
+                const int i = lane + 32 * k;
+                if (i < 2 * PPT) {
+                    const uint8_t* src = static_cast<const uint8_t*>(i < PPT ? p.k_new : p.v_new) +
+                                         ((int64_t)cs * Hkv + ch) * HD * 2 + (i % PPT) * 16;
+                    newp[k] = *reinterpret_cast<const uint4*>(src);
+                }
+            }
+            const int nbu = prefix[cs + 1] - prefix[cs];
+            last_phys = p.block_tables[(int64_t)cs * p.max_blocks + nbu - 1];
         }
     };
 
@@ -387,6 +418,25 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         }
         const uint32_t kt = st0 + (uint32_t)slot * Gm::STAGE, vt = kt + Gm::TILE;
         const int valid = min(BS, Lcur - cb * BS);
+        if (p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
+            // the new token: into the staged tiles (its attention input) and the pool
+            const int r = valid - 1;
+            const int64_t slot_row = (int64_t)last_phys * BS + r;
+#pragma unroll
+            for (int k = 0; k < NPC; ++k) {
+                const int i = lane + 32 * k;
+                if (i < 2 * PPT) {
+                    const int j = i % PPT, c = j >> 3, q16 = j & 7;
+                    const uint32_t dst = (i < PPT ? kt : vt) + c * BS * 128 + r * 128 + ((q16 ^ (r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(newp[k].x),
+                                 "r"(newp[k].y), "r"(newp[k].z), "r"(newp[k].w)
+                                 : "memory");
+                    uint8_t* pool = static_cast<uint8_t*>(i < PPT ? p.k_pool : p.v_pool);
+                    *reinterpret_cast<uint4*>(pool + (slot_row * Hkv + ch) * HD * 2 + j * 16) = newp[k];
+                }
+            }
+            __syncwarp();
+        }
 
         // S^T = K Q^T : 16 tokens x (8 NT) heads, fp32
         float sc[NT][4];
@@ -569,6 +619,10 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.ws_cnt = static_cast<unsigned long long*>(workspace);
     p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes);
     p.epoch = next_epoch();
+    p.k_new = a.k_new;
+    p.v_new = a.v_new;
+    p.k_pool = const_cast<void*>(a.k_cache);
+    p.v_pool = const_cast<void*>(a.v_cache);
 
     const void* kfn = kernel_ptr<T, HD, NT>();
     const size_t smem = smem_bytes<HD>(a.num_seqs);

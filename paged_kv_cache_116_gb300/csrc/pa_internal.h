@@ -34,6 +34,11 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks,
                                 cudaStream_t stream);
 cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_cache,
                             void* v_cache, int64_t row_bytes, cudaStream_t stream);
+// Writes k_new[s] / v_new[s] ([S, Hkv, hd]) to each sequence's slot of
+// position context_lens[s] - 1 (sequences with length 0 are skipped).
+cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t* block_tables, int32_t max_blocks,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t block_size, void* k_cache,
+                             void* v_cache, int64_t row_bytes, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                                const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
                                cudaStream_t stream);
@@ -58,6 +63,10 @@ struct AttnArgs {
     float scale;
     int causal;
     int dtype;
+    // decode only: the new token of each sequence (position L-1), written to
+    // the pool and attended from these rows (nullptr: plain decode)
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
 };
 bool attn_simt_supported(int dtype, int head_dim);
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);

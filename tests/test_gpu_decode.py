@@ -168,3 +168,44 @@ def test_check_mode_rejects_bad_tables(pa):
         pa.pa_set_check_mode(False)
     with pytest.raises(pa.PAError, match="PA_ERR_WORKSPACE"):
         pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, 40, w.scale, workspace=ws[:16])
+
+
+# ---------------------------------------------------------------- fused append + decode
+
+APPEND_CASES = [
+    ("tiny", lambda: W.tiny_decode()),
+    ("gqa24", lambda: W.decode_workload("ap_gqa", "bf16", 16, 32, 8, 128, W.gqa_batch_lengths(24), seed=21)),
+    ("mha", lambda: W.decode_workload("ap_mha", "f16", 16, 8, 8, 128, [1, 16, 17, 300, 33], std=0.5, seed=22)),
+    ("g12_hd64", lambda: W.decode_workload("ap_g12", "bf16", 16, 24, 2, 64, [1, 2, 15, 16, 47, 129], seed=23)),
+    ("hd256", lambda: W.decode_workload("ap_256", "bf16", 16, 8, 2, 256, [5, 64, 200], seed=24)),
+]
+
+
+@pytest.mark.parametrize("name,make", APPEND_CASES)
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_decode_append_equals_write_then_decode(pa, name, make, kernel):
+    """One call writes each sequence's new token at slot(L-1) and attends:
+    the pool must equal the oracle's after the write (bit for bit) and the
+    output must match the oracle's attention over the written pool."""
+    w = make()
+    kc, vc, bt = device_caches(w, DEV, after_step=False)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    try:
+        ws_bytes = pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size,
+                                               mc, W.TORCH_DTYPES[w.dtype])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype],
+                         device=DEV)
+        pa.pa_decode_append(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc, vc,
+                            bt, lens, mc, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 0)
+    okc, ovc = oracle_caches(w)
+    from helpers import oracle_bits, raw_bits
+
+    assert np.array_equal(raw_bits(kc), oracle_bits(okc)) and np.array_equal(raw_bits(vc), oracle_bits(ovc))
+    compare(w, out, oracle_attention(w, okc, ovc))
