@@ -229,8 +229,9 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
  * synchronisation, or code with no allocator at hand.  The pages have no
  * counterpart; it exists for those callers only.
  * Same arguments and result as pa_decode (tensor-core cases: bf16/f16,
- * head_dim 64/128/256, block_size 16, at most 16 query heads per KV head;
- * others return PA_ERR_UNSUPPORTED), but no workspace: the split-KV scratch
+ * head_dim 64/128/256, block_size 8 or a multiple of 16 up to 256, at most
+ * 16 query heads per KV head; others return PA_ERR_UNSUPPORTED), but no
+ * workspace: the split-KV scratch
  * is one library-owned device array of 8 MiB per device, held from load
  * until process exit.  A problem whose scratch (pa_decode_workspace_size
  * with default options) exceeds 8 MiB returns PA_ERR_WORKSPACE before

@@ -240,7 +240,8 @@ static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, pa
     if (want == 1) return false;
     if (want == 2 && !ok) {
         *st = fail(PA_ERR_UNSUPPORTED, "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256, "
-                                       "block_size 16 and at most 16 query heads per KV head");
+                                       "block_size 8 or a multiple of 16 up to 256, and at most 16 query "
+                                       "heads per KV head");
         return false;
     }
     return ok;
@@ -406,8 +407,8 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     const bool um_ok = pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
     const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
     if ((want == 2 && !tc_ok) || (want == 3 && !um_ok))
-        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernels take bf16/f16, head_dim 64/128 and "
-                                        "block_size 16");
+        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernels take bf16/f16 and head_dim 64/128; "
+                                        "mma.sync takes block_size 16, tcgen05 8 or a multiple of 16");
     const bool use_um = um_ok && (want == 3 || want == 0);
     const bool use_tc = !use_um && tc_ok && (want == 2 || want == 0);
     cudaStream_t st = as_stream(stream);

@@ -6,9 +6,10 @@
 // keys of the sequence, K and V read through its block table.
 //
 // How, on sm_103a:
-//  * Work unit = (sequence, KV head); its keys are the sequence's logical
-//    blocks.  All units' blocks form one flat list of
-//    Hkv * sum(ceil(L/16)) blocks, cut into equal contiguous ranges, one per
+//  * Work unit = (sequence, KV head); its keys are cut into 16-token tiles
+//    (one pool block when block_size is 16, part of one when it is a larger
+//    multiple of 16, two blocks when it is 8).  All units' tiles form one
+//    flat list of Hkv * sum(ceil(L/16)) tiles, cut into equal contiguous ranges, one per
 //    warp of a persistent grid, so every warp streams the same number of
 //    bytes whatever the length mix.  A unit cut between warps leaves partial
 //    softmax states (m, l, unnormalised o) in the workspace; the last of the
@@ -52,7 +53,7 @@ namespace {
 
 __device__ unsigned int g_decode_status;
 
-constexpr int BS = 16;  // tokens per block (one m-tile)
+constexpr int BS = 16;  // tokens per tile (one m-tile); a pool block holds 8 or 16k tokens
 
 struct TcParams {
     void* out;
@@ -75,6 +76,7 @@ struct TcParams {
     const void* v_new;
     void* k_pool;
     void* v_pool;
+    int32_t block_size;  // tokens per pool block: 8, or a multiple of 16 up to 256
 };
 
 template <int HD>
@@ -183,16 +185,29 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         h_out = (int)(rem / nb);
         b_out = (int)(rem - (int64_t)h_out * nb);
     };
-    auto table_entry = [&](int64_t rel) -> int32_t {
+    // pool row of the first token of a tile (and, with 8-token blocks, of its
+    // second half; that half is never read past the context)
+    const int bsz = p.block_size;
+    auto table_entry = [&](int64_t rel, int32_t& row2) -> int32_t {
+        row2 = 0;
         if (rel >= n) return 0;
-        int s, h, b;
-        locate(f0 + rel, s, h, b);
-        return p.block_tables[(int64_t)s * p.max_blocks + b];
+        int s, h, t;
+        locate(f0 + rel, s, h, t);
+        const int32_t* tb = p.block_tables + (int64_t)s * p.max_blocks;
+        if (bsz == 8) {
+            const int nb8 = (p.context_lens[s] + 7) >> 3;
+            const int32_t r1 = tb[2 * t] * 8;
+            row2 = 2 * t + 1 < nb8 ? tb[2 * t + 1] * 8 : r1;
+            return r1;
+        }
+        const int tok = t * BS;
+        return tb[tok / bsz] * bsz + tok % bsz;
     };
 
     // ---- producer side: issue cursor, table window, TMA
     const uint64_t pol = l2_policy_evict_first();
-    int32_t tbl_cur = table_entry(lane), tbl_next = table_entry(32 + lane);
+    int32_t tbl_cur2, tbl_next2;
+    int32_t tbl_cur = table_entry(lane, tbl_cur2), tbl_next = table_entry(32 + lane, tbl_next2);
     int win = 0, ip = 0;
     int is_, ih, ib;
     locate(f0, is_, ih, ib);
@@ -200,20 +215,29 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         const int w = ip >> 5;
         if (w != win) {
             tbl_cur = tbl_next;
-            tbl_next = table_entry((int64_t)(w + 1) * 32 + lane);
+            tbl_cur2 = tbl_next2;
+            tbl_next = table_entry((int64_t)(w + 1) * 32 + lane, tbl_next2);
             win = w;
         }
-        const int32_t phys = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
+        const int32_t row = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
+        const int32_t row2 = __shfl_sync(0xffffffffu, tbl_cur2, ip & 31);
         const int slot = ip % R;
         if (lane == 0) {
             uint8_t* dst = wst + (size_t)slot * Gm::STAGE;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE);
-            const int row = phys * BS;
 #pragma unroll
             for (int c = 0; c < Gm::CH; ++c) {
-                tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
-                tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                if (bsz == 8) {  // two 8-row boxes, each a 1024-byte swizzle atom
+                    tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                    tma_load_3d(dst + c * BS * 128 + 1024, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row2, pol);
+                    tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                    tma_load_3d(dst + Gm::TILE + c * BS * 128 + 1024, &tmV, &wbar[slot], 0, ih * Gm::CH + c,
+                                row2, pol);
+                } else {
+                    tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                    tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
+                }
             }
         }
         ++ip;
@@ -289,8 +313,7 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                     newp[k] = *reinterpret_cast<const uint4*>(src);
                 }
             }
-            const int nbu = prefix[cs + 1] - prefix[cs];
-            last_phys = p.block_tables[(int64_t)cs * p.max_blocks + nbu - 1];
+            last_phys = p.block_tables[(int64_t)cs * p.max_blocks + (p.context_lens[cs] - 1) / bsz];
         }
     };
 
@@ -421,7 +444,7 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         if (p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
             // the new token: into the staged tiles (its attention input) and the pool
             const int r = valid - 1;
-            const int64_t slot_row = (int64_t)last_phys * BS + r;
+            const int64_t slot_row = (int64_t)last_phys * bsz + (Lcur - 1) % bsz;
 #pragma unroll
             for (int k = 0; k < NPC; ++k) {
                 const int i = lane + 32 * k;
@@ -551,17 +574,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // The cache as a 3-D tensor: 64 elements (128 bytes) x (Hkv * CH) 128-byte
 // chunks of a token row x num_blocks * 16 token rows; one box = one chunk of
 // one KV head over the 16 rows of a block.
-bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, int num_blocks, int num_kv_heads, int head_dim,
-                 std::string* err) {
+bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, int num_blocks, int block_size, int num_kv_heads,
+                 int head_dim, std::string* err) {
     auto fn = encode_fn();
     if (!fn) {
         *err = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
     }
     const int ch = head_dim * 2 / 128;
-    cuuint64_t dims[3] = {64, (cuuint64_t)num_kv_heads * ch, (cuuint64_t)num_blocks * BS};
+    cuuint64_t dims[3] = {64, (cuuint64_t)num_kv_heads * ch, (cuuint64_t)num_blocks * block_size};
     cuuint64_t strides[2] = {128, (cuuint64_t)num_kv_heads * head_dim * 2};
-    cuuint32_t box[3] = {64, 1, BS};
+    cuuint32_t box[3] = {64, 1, (cuuint32_t)(block_size == 8 ? 8 : BS)};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = fn(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                     const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -601,8 +624,8 @@ template <typename T, int HD, int NT>
 cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* workspace, std::string* err,
                          cudaStream_t stream) {
     CUtensorMap tmK, tmV;
-    if (!make_kv_map(&tmK, a.k_cache, a.dtype, num_blocks, a.num_kv_heads, HD, err) ||
-        !make_kv_map(&tmV, a.v_cache, a.dtype, num_blocks, a.num_kv_heads, HD, err))
+    if (!make_kv_map(&tmK, a.k_cache, a.dtype, num_blocks, a.block_size, a.num_kv_heads, HD, err) ||
+        !make_kv_map(&tmV, a.v_cache, a.dtype, num_blocks, a.block_size, a.num_kv_heads, HD, err))
         return cudaErrorInvalidValue;
     TcParams p;
     p.out = a.out;
@@ -623,6 +646,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.v_new = a.v_new;
     p.k_pool = const_cast<void*>(a.k_cache);
     p.v_pool = const_cast<void*>(a.v_cache);
+    p.block_size = a.block_size;
 
     const void* kfn = kernel_ptr<T, HD, NT>();
     const size_t smem = smem_bytes<HD>(a.num_seqs);
@@ -662,7 +686,7 @@ cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* 
 
 bool decode_tc_supported(int dtype, int head_dim, int block_size, int group) {
     return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
-           block_size == BS && group >= 1 && group <= 16;
+           (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) && group >= 1 && group <= 16;
 }
 
 int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,

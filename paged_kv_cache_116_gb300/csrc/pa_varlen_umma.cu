@@ -46,9 +46,9 @@ namespace {
 
 __device__ unsigned int g_umma_status;
 
-constexpr int BS = 16;          // tokens per block
+constexpr int BS = 16;          // keys per group (one TMA box of 16 rows, or two of 8)
 constexpr int BK = 64;          // keys per tile
-constexpr int BPT = BK / BS;    // blocks per key tile
+constexpr int BPT = BK / BS;    // groups per key tile
 constexpr int TM = 128;         // rows of the MMA tile
 constexpr int R = 2;            // K/V stages
 constexpr int NTHREADS = 192;   // 4 softmax warps + producer + MMA warp
@@ -68,6 +68,7 @@ struct UmParams {
     int32_t num_heads;
     int32_t group;
     int32_t tokens_per_tile;  // T = floor(128 / group)
+    int32_t block_size;       // tokens per pool block: 8, or a multiple of 16 up to 256
     int32_t causal;
     float scale_log2;
 };
@@ -86,7 +87,7 @@ struct UGeo {
     static constexpr int NBAR = 1 + 4 * R + 4;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TBL_OFF = TADDR_OFF + 16;          // window of block-table entries
-    static constexpr int CU_OFF = TBL_OFF + kTableWindow * 4;
+    static constexpr int CU_OFF = TBL_OFF + 2 * kTableWindow * 4;  // rows of each group's first and second box
 };
 
 template <int HD>
@@ -182,12 +183,24 @@ __global__ void __launch_bounds__(NTHREADS, 2)
             for (int c = 0; c < Gm::CH; ++c)
                 tma_load_3d(base + Gm::Q_OFF + c * Gm::QCH, &tmQ, q_full, 64 * c, kvh * G, q0 + t0, pol);
         }
-        const int nblk = min(nb_seq, nkt * BPT);
+        // pool row of every 16-key group this CTA reads (and of its second
+        // 8-row box with 8-token blocks), staged a window at a time
+        const int ngrp = min(nb_seq, nkt * BPT);
         const int32_t* table = p.block_tables + (int64_t)req * p.max_blocks;
+        const int bsz = p.block_size;
         bool run = true;
-        for (int w0 = 0; w0 < nblk && run; w0 += kTableWindow) {
-            const int wn = min(kTableWindow, nblk - w0);
-            for (int i = lane; i < wn; i += 32) tbl_s[i] = table[w0 + i];
+        for (int w0 = 0; w0 < ngrp && run; w0 += kTableWindow) {
+            const int wn = min(kTableWindow, ngrp - w0);
+            for (int i = lane; i < wn; i += 32) {
+                const int tok = (w0 + i) * BS;
+                if (bsz == 8) {
+                    const int32_t r1 = table[tok >> 3] * 8;
+                    tbl_s[i] = r1;
+                    tbl_s[kTableWindow + i] = tok + 8 < L ? table[(tok >> 3) + 1] * 8 : r1;
+                } else {
+                    tbl_s[i] = table[tok / bsz] * bsz + tok % bsz;
+                }
+            }
             __syncwarp();
             if (lane == 0) {
                 const int kt_end = min(nkt, (w0 + wn + BPT - 1) / BPT);
@@ -211,12 +224,20 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                         uint8_t* st = base + (half ? Gm::V_OFF : Gm::KV_OFF) + slot * Gm::TILE;
                         fence_proxy_async_smem();
                         mbar_arrive_expect_tx(ful, bytes);
-                        for (int j = 0; j < nvalid; ++j) {  // blocks past the context are never read
-                            const int row = tbl_s[kt * BPT + j - w0] * BS;
+                        for (int j = 0; j < nvalid; ++j) {  // groups past the context are never read
+                            const int e = kt * BPT + j - w0;
+                            const int row = tbl_s[e];
 #pragma unroll
-                            for (int c = 0; c < Gm::CH; ++c)
-                                tma_load_3d(st + c * Gm::KCH + j * BS * 128, half ? &tmV : &tmK, ful, 0,
-                                            kvh * Gm::CH + c, row, pol);
+                            for (int c = 0; c < Gm::CH; ++c) {
+                                uint8_t* dst = st + c * Gm::KCH + j * BS * 128;
+                                if (bsz == 8) {  // two 8-row boxes, each a 1024-byte swizzle atom
+                                    tma_load_3d(dst, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c, row, pol);
+                                    tma_load_3d(dst + 1024, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c,
+                                                tbl_s[kTableWindow + e], pol);
+                                } else {
+                                    tma_load_3d(dst, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c, row, pol);
+                                }
+                            }
                         }
                     }
                     if (!run) break;
@@ -482,9 +503,9 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     }
     {
         const int ch = HD / 64;
-        cuuint64_t dims[3] = {64, (cuuint64_t)a.num_kv_heads * ch, (cuuint64_t)num_blocks * BS};
+        cuuint64_t dims[3] = {64, (cuuint64_t)a.num_kv_heads * ch, (cuuint64_t)num_blocks * a.block_size};
         cuuint64_t strides[2] = {128, (cuuint64_t)a.num_kv_heads * HD * 2};
-        cuuint32_t box[3] = {64, 1, BS};
+        cuuint32_t box[3] = {64, 1, (cuuint32_t)(a.block_size == 8 ? 8 : BS)};
         if (!um_encode(&tmK, a.k_cache, a.dtype, dims, strides, box, err) ||
             !um_encode(&tmV, a.v_cache, a.dtype, dims, strides, box, err))
             return cudaErrorInvalidValue;
@@ -499,6 +520,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     p.num_heads = a.num_heads;
     p.group = G;
     p.tokens_per_tile = TT;
+    p.block_size = a.block_size;
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
     const int64_t tiles = (int64_t)a.total_q / TT + a.num_seqs;
@@ -522,7 +544,8 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
 }  // namespace
 
 bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group) {
-    return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128) && block_size == BS && group >= 1 &&
+    return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128) &&
+           (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) && group >= 1 &&
            group <= TM;
 }
 

@@ -209,3 +209,44 @@ def test_decode_append_equals_write_then_decode(pa, name, make, kernel):
 
     assert np.array_equal(raw_bits(kc), oracle_bits(okc)) and np.array_equal(raw_bits(vc), oracle_bits(ovc))
     compare(w, out, oracle_attention(w, okc, ovc))
+
+
+# ---------------------------------------------------------------- other block sizes
+
+BS_CASES = []
+_r3 = np.random.default_rng(321)
+for _bs in (8, 32, 64, 128, 256):
+    for _i in range(2):
+        _hd = int(_r3.choice([64, 128]))
+        _g = int(_r3.choice([1, 4, 6]))
+        _lens = _r3.integers(1, 3 * _bs + 40, int(_r3.integers(1, 7))).tolist()
+        _lens[0] = int(_r3.choice([1, _bs, _bs + 1, 2 * _bs]))
+        BS_CASES.append((_bs, _hd, _g, _lens, 400 + 10 * _bs + _i))
+
+
+@pytest.mark.parametrize("bs,hd,g,lens,seed", BS_CASES)
+def test_decode_block_sizes_both_kernels(pa, bs, hd, g, lens, seed):
+    w = W.decode_workload("bs", "bf16", bs, 2 * g, 2, hd, lens, seed=seed)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    for kernel in (1, 2):
+        compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel), exact)
+
+
+@pytest.mark.parametrize("bs", [8, 32, 128])
+def test_decode_append_block_sizes(pa, bs):
+    w = W.decode_workload("ap_bs", "bf16", bs, 8, 2, 128, [1, bs - 1, bs, bs + 1, 3 * bs + 5], seed=bs)
+    kc, vc, bt = device_caches(w, DEV, after_step=False)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    ws = torch.empty(max(pa.pa_decode_workspace_size(w.num_seqs, 8, 2, 128, bs, mc, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.empty((w.num_seqs, 8, 128), dtype=torch.bfloat16, device=DEV)
+    pa.pa_decode_append(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc, vc, bt,
+                        lens, mc, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    okc, ovc = oracle_caches(w)
+    from helpers import oracle_bits, raw_bits
+
+    assert np.array_equal(raw_bits(kc), oracle_bits(okc)) and np.array_equal(raw_bits(vc), oracle_bits(ovc))
+    compare(w, out, oracle_attention(w, okc, ovc))

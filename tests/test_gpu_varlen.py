@@ -154,3 +154,16 @@ def test_varlen_permutation_bit_identical(pa, kernel):
     bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
     again = run_varlen(pa, w, kc2, vc2, bt2, kernel=kernel)
     assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("bs", [8, 32, 64, 128])
+def test_varlen_tcgen05_block_sizes(pa, bs):
+    rng = np.random.default_rng(bs)
+    S = 5
+    q = rng.integers(1, 150, S)
+    q[1] = 1
+    lens = q + rng.integers(0, 3 * bs, S)
+    w = W.varlen_workload("vl_bs", "bf16", bs, 12, 2, 128, lens.tolist(), q.tolist(), seed=bs)
+    kc, vc, bt = device_caches(w, DEV)
+    for causal in (True, False):
+        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3), oracle_attention(w, causal=causal))
