@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--workload", choices=WORKLOADS, default="gqa_decode_batch")
     ap.add_argument("--no-rotate", action="store_true", help="one pool copy (for profiling)")
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, clocks and cpu_baseline")
+    ap.add_argument("--block-size", type=int, default=16,
+                    help="block size of the GQA decode batch (the block-size sweep); other workloads keep theirs")
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as pa_slot_mapping + pa_write_kv + pa_decode instead of pa_decode_append")
     return ap.parse_args()
@@ -137,10 +139,14 @@ class Clocks:
 # ---------------------------------------------------------------- workloads
 
 
-def make_workload(name, device):
+def make_workload(name, device, block_size=16):
     from paged_kv_cache_116_gb300 import workloads as W
 
-    return W.tiny_decode() if name == "tiny_decode" else getattr(W, name)(device=device)
+    if name == "tiny_decode":
+        return W.tiny_decode()
+    if name == "gqa_decode_batch":
+        return W.gqa_decode_batch(device=device, block_size=block_size)
+    return getattr(W, name)(device=device)
 
 
 def varlen_flops(w):
@@ -271,7 +277,7 @@ def main():
     import paged_kv_cache_116_gb300 as pa
     from paged_kv_cache_116_gb300 import workloads as W
 
-    w = make_workload(args.workload, dev)
+    w = make_workload(args.workload, dev, args.block_size)
     tdt = W.TORCH_DTYPES[w.dtype]
     S, hq, hkv, hd, bs = w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     decode = w.is_decode and w.cow_pairs.shape[0] == 0
@@ -354,7 +360,8 @@ def main():
         kc, vc = pools[i % copies]
         attend(kc, vc, q, bt, lens, cu, torch.cuda.current_stream())
 
-    tc_decode = decode and w.dtype != "f32"
+    tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in (64, 128, 256) and hq // hkv <= 16 and
+                 (bs == 8 or (bs % 16 == 0 and bs <= 256)))
     launches_per_step = (1 if tc_decode else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
@@ -450,12 +457,13 @@ def main():
         nblk = int(sum((L + bs - 1) // bs for L in w.seq_lens.tolist()))
         alg = kv_bytes + 2 * S * hq * hd * w.elt + nblk * 4 + S * 4
         achieved = alg / (kern_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "kernel": "decode_tc_kernel (pa_decode, split merge included)",
+        tc_ok = (w.dtype in ("bf16", "f16") and hd in (64, 128, 256) and hq // hkv <= 16 and
+                 (bs == 8 or (bs % 16 == 0 and bs <= 256)))
+        roof = {"bound": "hbm", "kernel": ("decode_tc_kernel (pa_decode, split merge included)" if tc_ok else
+                                           "attn_simt_kernel (pa_decode, CUDA-core path)"),
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
                 "traffic": traffic_record(args.workload, "pa_decode_tc.cu"), "kernel_us": kern_ms * 1e3}
-        if w.dtype == "f32":
-            roof["kernel"] = "attn_simt_kernel (pa_decode, fp32 CUDA-core path)"
     else:
         fl = varlen_flops(w)
         achieved = fl / (kern_ms / 1e3) / 1e12

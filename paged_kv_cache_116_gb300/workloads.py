@@ -191,10 +191,11 @@ def gqa_batch_lengths(n: int = 64, seed: int = 0) -> np.ndarray:
     return np.array([p + o for p, o in pairs], dtype=np.int32)
 
 
-def gqa_decode_batch(seed: int = 0, num_seqs: int = 64, device="cpu") -> Workload:
-    """bf16, block_size 16, Hq 32, Hkv 8, head_dim 128, 64 sequences, shuffled
-    physical blocks, 10 % slack blocks."""
-    return decode_workload("gqa_decode_bf16_64seq", "bf16", 16, 32, 8, 128, gqa_batch_lengths(num_seqs, seed),
+def gqa_decode_batch(seed: int = 0, num_seqs: int = 64, device="cpu", block_size: int = 16) -> Workload:
+    """bf16, block_size 16 (or another size for the block-size sweep), Hq 32,
+    Hkv 8, head_dim 128, 64 sequences, shuffled physical blocks, 10 % slack."""
+    name = "gqa_decode_bf16_64seq" + ("" if block_size == 16 else "_bs%d" % block_size)
+    return decode_workload(name, "bf16", block_size, 32, 8, 128, gqa_batch_lengths(num_seqs, seed),
                            seed=seed, notes="L = randint(100,2000)+randint(20,1500), random.seed(0)",
                            device=device)
 
