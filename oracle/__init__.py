@@ -40,6 +40,8 @@ def lib():
         L.oracle_write_kv.restype = None
         L.oracle_copy_blocks.argtypes = [vp, vp, i32, vp, i32, i64]
         L.oracle_copy_blocks.restype = None
+        L.oracle_swap_blocks.argtypes = [vp, vp, vp, vp, i32, vp, i32, i64]
+        L.oracle_swap_blocks.restype = None
         L.oracle_gather.argtypes = [vp, vp, i32, i32, i32, i32, ctypes.c_int, vp]
         L.oracle_gather.restype = None
         L.oracle_paged_attention.argtypes = [vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32,
@@ -102,6 +104,18 @@ def copy_blocks(k_caches, v_caches, block_pairs) -> None:
     kp = (ctypes.c_void_p * n)(*[c.ctypes.data for c in k_caches])
     vp = (ctypes.c_void_p * n)(*[c.ctypes.data for c in v_caches])
     lib().oracle_copy_blocks(kp, vp, n, _ptr(pairs), pairs.shape[0], block_bytes)
+
+
+def swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs) -> None:
+    """In-place: dst pools' blocks receive the src pools' blocks, every layer."""
+    pairs = _c(block_pairs, np.int64).reshape(-1, 2)
+    n = len(src_k)
+    for c in list(src_k) + list(src_v) + list(dst_k) + list(dst_v):
+        assert c.flags.c_contiguous
+    block_bytes = src_k[0].nbytes // src_k[0].shape[0]
+    arr = lambda cs: (ctypes.c_void_p * n)(*[c.ctypes.data for c in cs])  # noqa: E731
+    lib().oracle_swap_blocks(arr(src_k), arr(src_v), arr(dst_k), arr(dst_v), n, _ptr(pairs), pairs.shape[0],
+                             block_bytes)
 
 
 def gather(cache, block_table, seq_len: int, dtype: str) -> np.ndarray:

@@ -15,6 +15,8 @@
  *     translation formula.
  *   - write: "分页 KV Cache", paged.py PagedKVCache.write (row scatter, in
  *     index order).
+ *   - swap: the xxqk.cn PagedAttention article, §显存不够时的调度 (evicted
+ *     blocks go to CPU memory and come back).
  *   - block copy: "分页 KV Cache", exercise 2 answer (copy-on-write copies
  *     the old block's content into the new block); "KV cache：容量推导、分页与
  *     回收", kv_cache.py Sequence.append (allocate(copy of data)).
@@ -137,6 +139,21 @@ void oracle_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t nu
                    (size_t)block_bytes);
             memcpy((char*)v_caches[l] + dst * block_bytes, (const char*)v_caches[l] + src * block_bytes,
                    (size_t)block_bytes);
+        }
+    }
+}
+
+/* Swap: for every layer and pair, block dst of the destination pool receives
+ * block src of the source pool (K and V), the pools being different arrays
+ * (device pool and host pool in either direction).  "xxqk.cn PagedAttention",
+ * §显存不够时的调度: evicted blocks move to CPU memory and back. */
+void oracle_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k, void* const* dst_v,
+                        int32_t num_layers, const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes) {
+    for (int32_t l = 0; l < num_layers; ++l) {
+        for (int32_t p = 0; p < num_pairs; ++p) {
+            int64_t src = block_pairs[2 * p], dst = block_pairs[2 * p + 1];
+            memcpy((char*)dst_k[l] + dst * block_bytes, (const char*)src_k[l] + src * block_bytes, (size_t)block_bytes);
+            memcpy((char*)dst_v[l] + dst * block_bytes, (const char*)src_v[l] + src * block_bytes, (size_t)block_bytes);
         }
     }
 }

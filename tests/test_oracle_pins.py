@@ -413,3 +413,27 @@ def test_pins_detect_swapped_k_and_v():
     swapped = oracle.paged_attention(W.raw_numpy(w.q), vc, kc, w.block_tables, w.seq_lens,
                                      w.query_start_loc, w.scale, "f32")
     assert np.abs(swapped - ref).max() > 1e-3
+
+
+def test_swap_out_and_back_is_identity_and_moves_whole_blocks():
+    rng = np.random.default_rng(9)
+    dev_k = [rng.integers(0, 65535, (12, 4, 2, 8), dtype=np.uint16) for _ in range(2)]
+    dev_v = [rng.integers(0, 65535, (12, 4, 2, 8), dtype=np.uint16) for _ in range(2)]
+    host_k = [np.zeros((6, 4, 2, 8), np.uint16) for _ in range(2)]
+    host_v = [np.zeros((6, 4, 2, 8), np.uint16) for _ in range(2)]
+    k0, v0 = [k.copy() for k in dev_k], [v.copy() for v in dev_v]
+    out_pairs = np.array([[3, 0], [11, 5], [7, 2]], np.int64)  # device block -> host slot
+    oracle.swap_blocks(dev_k, dev_v, host_k, host_v, out_pairs)
+    for l in range(2):
+        for d, h in out_pairs:
+            assert np.array_equal(host_k[l][h], k0[l][d]) and np.array_equal(host_v[l][h], v0[l][d])
+        assert np.all(host_k[l][[1, 3, 4]] == 0)
+    # the blocks are freed on the device and come back into other physical blocks
+    for l in range(2):
+        dev_k[l][[3, 11, 7]] = 0
+        dev_v[l][[3, 11, 7]] = 0
+    in_pairs = np.array([[0, 9], [5, 1], [2, 4]], np.int64)  # host slot -> new device block
+    oracle.swap_blocks(host_k, host_v, dev_k, dev_v, in_pairs)
+    for l in range(2):
+        for (d_old, h), (_, d_new) in zip(out_pairs, in_pairs):
+            assert np.array_equal(dev_k[l][d_new], k0[l][d_old]) and np.array_equal(dev_v[l][d_new], v0[l][d_old])
