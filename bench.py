@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--no-extras", action="store_true", help="skip e2e, clocks and cpu_baseline")
     ap.add_argument("--block-size", type=int, default=16,
                     help="block size of the GQA decode batch (the block-size sweep); other workloads keep theirs")
+    ap.add_argument("--swap", action="store_true",
+                    help="measure pa_swap_blocks (device pool <-> pinned host pool) instead of the attention step")
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as pa_slot_mapping + pa_write_kv + pa_decode instead of pa_decode_append")
     return ap.parse_args()
@@ -251,12 +253,121 @@ def run_reference(args, rank):
 # ---------------------------------------------------------------- the GPU arm
 
 
+def run_swap(args):
+    """Preemption traffic: blocks of the GQA batch's geometry (16 tokens x 8
+    KV heads x 128 x bf16 = 32 KiB per K or V block) across 8 layers move
+    from the device pool to a pinned host pool and back, one pa_swap_blocks
+    call per direction.  Beside it: the same blocks moved by one
+    cudaMemcpyAsync per block and layer (torch copies, graph-captured), and
+    one contiguous copy of the same byte count (the copy engines' rate, the
+    denominator of frac)."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_116_gb300 as pa
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    layers, nb_dev, nb_host, n, bs, hkv, hd = 8, 4096, 1024, 1024, 16, 8, 128
+    g = torch.Generator(device=dev).manual_seed(0)
+    mk = lambda nb: torch.randint(-32768, 32767, (nb, bs, hkv, hd), generator=g, dtype=torch.int16,  # noqa: E731
+                                  device=dev).view(torch.bfloat16)
+    dk = [mk(nb_dev) for _ in range(layers)]
+    dv = [mk(nb_dev) for _ in range(layers)]
+    hk = [torch.empty((nb_host, bs, hkv, hd), dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+    hv = [torch.empty((nb_host, bs, hkv, hd), dtype=torch.bfloat16).pin_memory() for _ in range(layers)]
+    rng = np.random.default_rng(0)
+    picked = rng.choice(nb_dev, 2 * n, replace=False)  # blocks that go out, blocks they come back to
+    src, back = picked[:n], picked[n:]
+    dst = rng.permutation(nb_host)[:n]
+    out_pairs = torch.from_numpy(np.stack([src, dst], 1).astype(np.int64)).to(dev)
+    in_pairs = torch.from_numpy(np.stack([dst, back], 1).astype(np.int64)).to(dev)
+    block_bytes = bs * hkv * hd * 2
+    moved = 2 * layers * n * block_bytes  # K and V, one direction
+
+    def graph(fn):
+        fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, capture_error_mode="thread_local"):
+            fn()
+        return gr
+
+    def per_block(a_k, a_v, b_k, b_v, pairs):
+        pl = pairs.cpu().tolist()
+
+        def fn():
+            for l in range(layers):
+                for s_, d_ in pl:
+                    b_k[l][d_].copy_(a_k[l][s_], non_blocking=True)
+                    b_v[l][d_].copy_(a_v[l][s_], non_blocking=True)
+        return fn
+
+    bulk_d = torch.empty(moved, dtype=torch.uint8, device=dev)
+    bulk_h = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    gs = {
+        "swap_out": graph(lambda: pa.pa_swap_blocks(dk, dv, hk, hv, out_pairs, stream=torch.cuda.current_stream())),
+        "swap_in": graph(lambda: pa.pa_swap_blocks(hk, hv, dk, dv, in_pairs, stream=torch.cuda.current_stream())),
+        "memcpy_out": graph(per_block(dk, dv, hk, hv, out_pairs)),
+        "memcpy_in": graph(per_block(hk, hv, dk, dv, in_pairs)),
+        "bulk_out": graph(lambda: bulk_h.copy_(bulk_d, non_blocking=True)),
+        "bulk_in": graph(lambda: bulk_d.copy_(bulk_h, non_blocking=True)),
+    }
+    reps = max(args.steps if args.steps < 20000 else 20, 3)
+    res = {}
+    for name, gr in gs.items():
+        for _ in range(max(args.warmup if args.warmup < 20 else 3, 3)):
+            gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        res[name] = a.elapsed_time(b) / reps
+    # parity of what was timed: the last swap-in brought the out-swapped blocks back
+    for l in (0, layers - 1):
+        assert torch.equal(dk[l][torch.from_numpy(back).to(dev)].view(torch.int16),
+                           dk[l][torch.from_numpy(src).to(dev)].view(torch.int16))
+    gbs = {k: moved / (v / 1e3) / 1e9 for k, v in res.items()}
+    line = {
+        "metric": "block swap GB/s, device pool <-> pinned host pool", "value": gbs["swap_out"], "unit": "GB/s",
+        "n_gpus": 1, "steps": reps, "warmup": 3, "ms_per_step": res["swap_out"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (moved as bytes)", "data": "synthetic",
+        "config": {"workload": "swap_blocks", "layers": layers, "blocks_per_direction": n, "block_size": bs,
+                   "num_kv_heads": hkv, "head_dim": hd, "bytes_per_direction": moved,
+                   "step": "one pa_swap_blocks call (all layers, K and V), replayed as a CUDA graph"},
+        "swap_in_gbs": gbs["swap_in"],
+        "per_block_memcpy_gbs": {"out": gbs["memcpy_out"], "in": gbs["memcpy_in"],
+                                 "copies_per_direction": 2 * layers * n},
+        "roofline": {"bound": "link", "kernel": "swap_blocks_kernel", "achieved": gbs["swap_out"],
+                     "peak": gbs["bulk_out"], "unit": "GB/s", "frac": gbs["swap_out"] / gbs["bulk_out"],
+                     "peak_kind": "measured here: one contiguous cudaMemcpyAsync of the same bytes, same direction",
+                     "in": {"achieved": gbs["swap_in"], "peak": gbs["bulk_in"],
+                            "frac": gbs["swap_in"] / gbs["bulk_in"]},
+                     "traffic": None},
+        "gpu_launches": reps,
+        "ms": res,
+    }
+    print(json.dumps(line))
+
+
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.swap:
+        if rank == 0:
+            run_swap(args)
         return
 
     import torch
@@ -468,10 +579,11 @@ def main():
         fl = varlen_flops(w)
         achieved = fl / (kern_ms / 1e3) / 1e12
         peak = peaks["bf16_tflops"]
-        roof = {"bound": "tensor", "kernel": "varlen_tc_kernel (pa_varlen)", "achieved": achieved, "peak": peak,
+        roof = {"bound": "tensor", "kernel": "varlen_umma_kernel (pa_varlen, tcgen05)", "achieved": achieved,
+                "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": kind + " bf16_tflops (burst)",
                 "algorithmic_flops": fl, "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
-                "traffic": traffic_record(args.workload, "pa_varlen_tc.cu"), "kernel_us": kern_ms * 1e3}
+                "traffic": traffic_record(args.workload, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3}
 
     if rank == 0:
         line = {

@@ -146,6 +146,29 @@ PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, in
                          void* stream);
 
 /*
+ * pa_swap_blocks -- move whole blocks between two pools, e.g. the device
+ * pool and a host pool when sequences are preempted and resumed (the xxqk.cn
+ * PagedAttention article, §显存不够时的调度: evicted blocks go to CPU memory
+ * and come back; small blocks make this many small transfers).  For each
+ * layer l and pair p: block block_pairs[2p+1] of dst_k[l] / dst_v[l]
+ * receives block block_pairs[2p] of src_k[l] / src_v[l] (all block_size
+ * slots).  src_* and dst_* are HOST arrays of num_layers pointers; each
+ * pointer is device memory or pinned/registered host memory (the GPU reads
+ * or writes host pools directly, over NVLink-C2C on GB300); block_pairs is
+ * device or pinned host memory, int64 [num_pairs, 2] (src, dst).  Any other
+ * memory is PA_ERR_INVALID_ARG.  Destinations must be distinct and the two
+ * pools distinct (or the pairs' source and destination sets disjoint);
+ * check mode rejects out-of-range ids and repeated destinations.  Enqueued
+ * on `stream`; host pools must stay allocated until it completes.
+ * Bit-exact.
+ */
+PA_API pa_status pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k,
+                                void* const* dst_v, int32_t num_layers, const int64_t* block_pairs,
+                                int32_t num_pairs, int32_t src_num_blocks, int32_t dst_num_blocks,
+                                int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                                void* stream);
+
+/*
  * pa_decode -- one query per sequence over its paged context.
  * For sequence s and query head h (KV head kv = h / (num_heads / num_kv_heads),
  * the repeat_interleave grouping of the handbook's paged_attention):

@@ -19,7 +19,8 @@ DTYPE_CODE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_
 
 EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
-           "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc")
+           "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
+           "pa_swap_blocks")
 
 
 class PAError(RuntimeError):
@@ -51,6 +52,7 @@ def lib():
         "pa_slot_mapping": ([vp, i32, i32, vp, vp, i64, i32, vp, vp], ci),
         "pa_write_kv": ([vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, ci, vp], ci),
         "pa_copy_blocks": ([vp, vp, i32, vp, i32, i32, i32, i32, i32, ci, vp], ci),
+        "pa_swap_blocks": ([vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, ci, vp], ci),
         "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
         "pa_decode": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz, vp], ci),
         "pa_decode_append": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz,
@@ -148,6 +150,23 @@ def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
     st = lib().pa_copy_blocks(kp, vp, n, _ptr(block_pairs), block_pairs.shape[0], nb, bs, hkv, hd,
                               _dtype(k_caches[0]), _stream(stream))
     _check(st, "pa_copy_blocks")
+
+
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
+    """Copy blocks between two pools (device or pinned host tensors), every layer:
+    dst[pairs[p, 1]] = src[pairs[p, 0]]."""
+    if isinstance(src_k, torch.Tensor):
+        src_k, src_v, dst_k, dst_v = [src_k], [src_v], [dst_k], [dst_v]
+    for t in list(src_k) + list(src_v) + list(dst_k) + list(dst_v) + [block_pairs]:
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("pools and pairs must be contiguous CUDA or pinned host tensors")
+    n = len(src_k)
+    arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])  # noqa: E731
+    nbs, bs, hkv, hd = src_k[0].shape
+    st = lib().pa_swap_blocks(arr(src_k), arr(src_v), arr(dst_k), arr(dst_v), n, _ptr(block_pairs),
+                              block_pairs.shape[0], nbs, dst_k[0].shape[0], bs, hkv, hd, _dtype(src_k[0]),
+                              _stream(stream))
+    _check(st, "pa_swap_blocks")
 
 
 def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, dtype):

@@ -231,6 +231,69 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t n
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_copy_blocks launch");
 }
 
+// Device address a kernel can use for p: device memory as is, pinned or
+// registered host memory through its device mapping; nullptr otherwise.
+static const void* device_view(const void* p) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return p;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer) {
+        const uint8_t* base = static_cast<const uint8_t*>(at.hostPointer);
+        return static_cast<const uint8_t*>(at.devicePointer) + (static_cast<const uint8_t*>(p) - base);
+    }
+    return nullptr;
+}
+
+pa_status pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k, void* const* dst_v,
+                         int32_t num_layers, const int64_t* block_pairs, int32_t num_pairs, int32_t src_num_blocks,
+                         int32_t dst_num_blocks, int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                         void* stream) {
+    if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "num_pairs must be non-negative and both pools non-empty");
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, src_num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (num_layers < 1 || num_layers > PA_MAX_LAYERS)
+        return fail(PA_ERR_INVALID_ARG, "num_layers must be in [1, PA_MAX_LAYERS]");
+    if (num_pairs == 0) return PA_OK;
+    if (!src_k || !src_v || !dst_k || !dst_v || !block_pairs) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    const int64_t block_bytes = (int64_t)block_size * num_kv_heads * head_dim * pa::elt_size(dtype);
+    if (block_bytes % 16 != 0) return fail(PA_ERR_UNSUPPORTED, "a block must be a multiple of 16 bytes");
+    std::vector<void*> sk(num_layers), sv(num_layers), dk(num_layers), dv(num_layers);
+    for (int l = 0; l < num_layers; ++l) {
+        const void* in[4] = {src_k[l], src_v[l], dst_k[l], dst_v[l]};
+        void** out[4] = {&sk[l], &sv[l], &dk[l], &dv[l]};
+        for (int i = 0; i < 4; ++i) {
+            if (!in[i] || !aligned16(in[i])) return fail(PA_ERR_INVALID_ARG, "pools must be non-null and 16-byte aligned");
+            const void* d = device_view(in[i]);
+            if (!d)
+                return fail(PA_ERR_INVALID_ARG, "a pool is neither device memory nor pinned/registered host memory");
+            *out[i] = const_cast<void*>(d);
+        }
+    }
+    const void* pairs_dev = device_view(block_pairs);
+    if (!pairs_dev) return fail(PA_ERR_INVALID_ARG, "block_pairs must be device or pinned host memory");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = PA_OK;
+        std::vector<int64_t> pr;
+        if (!to_host(pr, static_cast<const int64_t*>(pairs_dev), 2 * (int64_t)num_pairs, st, &err)) return err;
+        std::unordered_set<int64_t> dsts;
+        for (int32_t p = 0; p < num_pairs; ++p) {
+            const int64_t s = pr[2 * p], d = pr[2 * p + 1];
+            if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks)
+                return fail(PA_ERR_INDEX, "pair " + std::to_string(p) + ": block id outside its pool");
+            if (!dsts.insert(d).second)
+                return fail(PA_ERR_INDEX, "block " + std::to_string(d) + " is the destination of two pairs");
+        }
+    }
+    cudaError_t e = pa::launch_swap_blocks(sk.data(), sv.data(), dk.data(), dv.data(), num_layers,
+                                           static_cast<const int64_t*>(pairs_dev), num_pairs, block_bytes, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_swap_blocks launch");
+}
+
 // ------------------------------------------------------------------ decode
 
 static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, pa_status* st) {

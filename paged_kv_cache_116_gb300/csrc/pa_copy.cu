@@ -104,7 +104,66 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+// Swap: one CTA per (pair, layer) copies a block between two different
+// pools; either side may be pinned host memory reached over NVLink-C2C,
+// where a read takes microseconds, so each thread keeps kSwapUnroll K and
+// V vectors in flight before it stores them.
+struct SwapPtrs {
+    const uint4* src_k[PA_MAX_LAYERS_INTERNAL];
+    const uint4* src_v[PA_MAX_LAYERS_INTERNAL];
+    uint4* dst_k[PA_MAX_LAYERS_INTERNAL];
+    uint4* dst_v[PA_MAX_LAYERS_INTERNAL];
+};
+
+constexpr int kSwapUnroll = 4;
+
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(const SwapPtrs ptrs, const int64_t* __restrict__ pairs, int64_t block_vecs) {
+    const int64_t pair = blockIdx.x;
+    const int layer = blockIdx.y;
+    const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
+    const uint4* ks = ptrs.src_k[layer] + src * block_vecs;
+    const uint4* vs = ptrs.src_v[layer] + src * block_vecs;
+    uint4* kd = ptrs.dst_k[layer] + dst * block_vecs;
+    uint4* vd = ptrs.dst_v[layer] + dst * block_vecs;
+    for (int64_t base = threadIdx.x; base < block_vecs; base += kSwapUnroll * blockDim.x) {
+        uint4 a[kSwapUnroll], b[kSwapUnroll];
+#pragma unroll
+        for (int u = 0; u < kSwapUnroll; ++u) {
+            const int64_t e = base + (int64_t)u * blockDim.x;
+            if (e < block_vecs) {
+                a[u] = ks[e];
+                b[u] = vs[e];
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kSwapUnroll; ++u) {
+            const int64_t e = base + (int64_t)u * blockDim.x;
+            if (e < block_vecs) {
+                kd[e] = a[u];
+                vd[e] = b[u];
+            }
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k, void* const* dst_v,
+                               int32_t num_layers, const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
+                               cudaStream_t stream) {
+    if (num_pairs == 0) return cudaSuccess;
+    SwapPtrs ptrs;
+    for (int l = 0; l < num_layers; ++l) {
+        ptrs.src_k[l] = static_cast<const uint4*>(src_k[l]);
+        ptrs.src_v[l] = static_cast<const uint4*>(src_v[l]);
+        ptrs.dst_k[l] = static_cast<uint4*>(dst_k[l]);
+        ptrs.dst_v[l] = static_cast<uint4*>(dst_v[l]);
+    }
+    dim3 grid((unsigned)num_pairs, (unsigned)num_layers);
+    swap_blocks_kernel<<<grid, 256, 0, stream>>>(ptrs, block_pairs, block_bytes / 16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_idx,
                                 const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,

@@ -39,6 +39,9 @@ cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_ma
 cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t* block_tables, int32_t max_blocks,
                              const int32_t* context_lens, int32_t num_seqs, int32_t block_size, void* k_cache,
                              void* v_cache, int64_t row_bytes, cudaStream_t stream);
+cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k, void* const* dst_v,
+                               int32_t num_layers, const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
+                               cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                                const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
                                cudaStream_t stream);
