@@ -1,33 +1,40 @@
 // pa_varlen_umma.cu -- the varlen prefill/decode mix on the 5th-generation
 // tensor cores (tcgen05.mma, accumulators in tensor memory), bf16/f16,
-// head_dim 64 or 128, block_size 16.
+// head_dim 64 or 128, block_size 8 or a multiple of 16 up to 256.
 //
 // Same arithmetic as the handbook's paged_attention ("分页 KV Cache",
 // §分页注意力): request i owns query rows cu[i] .. cu[i+1]-1, its new token j
 // is at position L_i - n_i + j and (causal) sees keys 0..that position; query
 // head h reads KV head h / G.
 //
-// A CTA takes one KV head and T = floor(128 / G) consecutive new tokens of one
-// request, i.e. a 128-row tile of (token, group head) pairs -- the G heads
-// share every K/V tile.  Roles:
-//   warp 4              TMA: the Q tile once, then 64-key K and V tiles (four
-//                       16-token blocks through the block table, staged in
-//                       windows of 512 entries) into separate 2-slot K and V
-//                       rings, so the next K tile loads as soon as its S is
-//                       done, not after P V (two CTAs share an SM);
-//   warp 5 (one lane)   issues tcgen05.mma: S = Q K^T (M 128, N 64, K = hd)
-//                       into tensor memory, then O += P V (M 128, N hd, K 64)
-//                       with V read MN-major; completion via tcgen05.commit;
-//   warps 0-3           one query row per thread: read S from tensor memory,
-//                       causal mask, exp2-domain online softmax, P (bf16/f16)
-//                       written back to tensor memory as the A operand of
-//                       P V; O is rescaled in tensor memory only when a row's
-//                       running maximum grows by more than 2^8, and
-//                       normalised and stored at the end.
-// S(k+1) is issued as soon as the softmax warps have read S(k), so it runs
-// under their exponentials.  V rows past the context are zeroed in shared
-// memory before P V.  Every wait is bounded in time; on expiry the CTA sets a
-// status bit, abandons the tile and still frees its tensor memory.
+// A query tile is one KV head's G query heads over T = floor(128 / G)
+// consecutive new tokens of one request: 128 (token, head) rows that share
+// every K/V tile.  One CTA per SM takes two adjacent query tiles of one
+// request (A, the later tokens, and B), so each K/V tile that crosses the
+// L2 -> shared-memory path feeds two 128-row MMAs.  Roles (352 threads):
+//   warps 0-3 / 4-7     softmax of tile A / tile B: one query row per
+//                       thread; read S from tensor memory, causal mask,
+//                       exp2-domain online softmax, P (bf16/f16) written
+//                       back to tensor memory as the A operand of P V; O is
+//                       rescaled in tensor memory only when a row's running
+//                       maximum grows by more than 2^8, and normalised and
+//                       stored at the end;
+//   warp 8 / warp 9     TMA producers of the K / V tiles (128 keys = eight
+//                       16-token groups through the block table, staged in
+//                       windows of 512 entries), each into its own R-slot
+//                       ring; a tile's boxes are issued by one lane each;
+//   warp 10 (one lane)  issues tcgen05.mma as operands become ready:
+//                       S = Q K^T (M 128, N 128, K = hd) per tile, then
+//                       O += P V (M 128, N hd, K 128) with V read MN-major.
+// 128-key tiles: an M128 x N64 MMA instruction takes as long as M128 x N128,
+// so narrower S tiles would leave half the tensor pipe idle.
+// Tensor memory (512 columns): tile X in columns 256 X .. 256 X + 255:
+// S (128 fp32 columns), overwritten in place by P (bf16/f16, two per
+// column), then O (hd columns).  The MMAs of one thread execute in issue
+// order, so S_X(k+1), issued after P V_X(k), cannot overwrite P_X(k) before
+// P V_X(k) has read it.  V rows past the context are zeroed in shared memory
+// before P V.  Every wait is bounded in time; on expiry the CTA sets
+// a status bit, abandons the tile and still frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -47,16 +54,18 @@ namespace {
 __device__ unsigned int g_umma_status;
 
 constexpr int BS = 16;          // keys per group (one TMA box of 16 rows, or two of 8)
-constexpr int BK = 64;          // keys per tile
+constexpr int BK = 128;         // keys per tile
 constexpr int BPT = BK / BS;    // groups per key tile
 constexpr int TM = 128;         // rows of the MMA tile
-constexpr int R = 2;            // K/V stages
-constexpr int NTHREADS = 192;   // 4 softmax warps + producer + MMA warp
-constexpr uint32_t TMEM_COLS = 256;
-constexpr uint32_t S_COL = 0, P_COL = 64, O_COL = 128;  // S 64 fp32 cols, P 32 packed cols, O hd cols
+constexpr int R = 2;            // K and V stages
+constexpr int NWARPS = 11;      // 2 x 4 softmax warps, K producer, V producer, MMA issuer
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int W_KPROD = 8, W_VPROD = 9, W_MMA = 10;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t S_COL = 0, P_COL = 0, O_COL = 128;  // within a tile's 256 columns (P over S)
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
-constexpr int kMaxSeqsSmem = 8192;
-constexpr int kTableWindow = 512;  // block-table entries the producer stages at a time
+constexpr int kMaxSeqsSmem = 4096;
+constexpr int kTableWindow = 512;  // block-table entries a producer stages at a time
 
 struct UmParams {
     void* out;
@@ -76,18 +85,21 @@ struct UmParams {
 template <int HD>
 struct UGeo {
     static constexpr int CH = HD / 64;          // 128-byte chunks per head row
-    static constexpr int QCH = TM * 128;        // bytes of one chunk of the Q tile
+    static constexpr int QCH = TM * 128;        // bytes of one chunk of a Q tile
     static constexpr int KCH = BK * 128;        // bytes of one chunk of a K (or V) tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int KV_OFF = CH * QCH;
+    static constexpr int QT = CH * QCH;         // bytes of a Q tile
+    static constexpr int Q_OFF = 0;             // Q tiles A, B
     static constexpr int TILE = CH * KCH;       // bytes of a K (or V) tile
-    static constexpr int V_OFF = KV_OFF + R * TILE;
+    static constexpr int K_OFF = 2 * QT;
+    static constexpr int V_OFF = K_OFF + R * TILE;
     static constexpr int BAR_OFF = V_OFF + R * TILE;
-    // q_full, k_full[R], k_empty[R], v_full[R], v_empty[R], s_full, s_free, p_full, o_done
-    static constexpr int NBAR = 1 + 4 * R + 4;
+    // q_full, k_full[R], k_empty[R], v_full[R], v_empty[R],
+    // per tile: s_full, p_full, o_done; v_zeroed
+    static constexpr int NBAR = 1 + 4 * R + 6 + 1;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
-    static constexpr int TBL_OFF = TADDR_OFF + 16;          // window of block-table entries
-    static constexpr int CU_OFF = TBL_OFF + 2 * kTableWindow * 4;  // rows of each group's first and second box
+    static constexpr int TBL_OFF = TADDR_OFF + 16;                 // two producers' table windows
+    static constexpr int TBL_INTS = 2 * kTableWindow;              // rows of each group's first and second box
+    static constexpr int CU_OFF = TBL_OFF + 2 * TBL_INTS * 4;
 };
 
 template <int HD>
@@ -96,7 +108,7 @@ size_t um_smem_bytes(int num_seqs) {
 }
 
 template <typename T, int HD>
-__global__ void __launch_bounds__(NTHREADS, 2)
+__global__ void __launch_bounds__(NTHREADS, 1)
     varlen_umma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const UmParams p) {
     using Gm = UGeo<HD>;
@@ -109,55 +121,78 @@ __global__ void __launch_bounds__(NTHREADS, 2)
     uint64_t* k_empty = bars + 1 + R;
     uint64_t* v_full = bars + 1 + 2 * R;
     uint64_t* v_empty = bars + 1 + 3 * R;
-    uint64_t* s_full = bars + 1 + 4 * R;
-    uint64_t* s_free = s_full + 1;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* o_done = s_full + 3;
+    uint64_t* tb = bars + 1 + 4 * R;  // per tile X: tb[3X] s_full, +1 p_full, +2 o_done
+    uint64_t* v_zeroed = tb + 6;
     volatile uint32_t* taddr_slot = reinterpret_cast<volatile uint32_t*>(base + Gm::TADDR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Gm::TADDR_OFF + 4);
     int32_t* cu_s = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);
-    int32_t* tbl_s = reinterpret_cast<int32_t*>(base + Gm::TBL_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, G = p.group, TT = p.tokens_per_tile;
     const int kvh = blockIdx.y;
     pdl_wait_primary();
 
-    // ---- request and tile: request i owns tiles [floor(cu[i]/T) + i, floor(cu[i+1]/T) + i + 1)
+    // ---- request and tile pair: request i owns pairs
+    // [floor(cu[i] / 2T) + i, floor(cu[i+1] / 2T) + i + 1); a request's
+    // ceil(n / 2T) pairs fit, the rest are spare CTAs that return at once
     const bool cu_in_smem = S <= kMaxSeqsSmem;
     if (cu_in_smem)
         for (int i = threadIdx.x; i <= S; i += blockDim.x) cu_s[i] = p.cu[i];
     __syncthreads();
     auto cu_at = [&](int i) -> int { return cu_in_smem ? cu_s[i] : p.cu[i]; };
-    auto tile0 = [&](int i) -> int64_t { return (int64_t)cu_at(i) / TT + i; };
+    auto pair0 = [&](int i) -> int64_t { return (int64_t)cu_at(i) / (2 * TT) + i; };
     const int64_t bid = blockIdx.x;
     int lo = 0, hi = S - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (tile0(mid) <= bid) lo = mid;
+        if (pair0(mid) <= bid) lo = mid;
         else hi = mid - 1;
     }
     const int req = lo;
     const int q0 = cu_at(req), n_new = cu_at(req + 1) - q0;
     const int ntile = (n_new + TT - 1) / TT;
-    const int64_t t_rel = bid - tile0(req);
-    if (t_rel >= ntile) return;  // the spare tile of this request (uniform for the CTA)
-    const int t0 = (ntile - 1 - (int)t_rel) * TT;  // last tiles first
-    const int tn = min(TT, n_new - t0);
+    const int npair = (ntile + 1) / 2;
+    const int64_t p_rel = bid - pair0(req);
+    if (p_rel >= npair) return;  // spare CTA (uniform for the CTA)
     const int L = p.seq_lens[req];
     const int first_pos = L - n_new;
-    const int kv_end = p.causal ? first_pos + t0 + tn : L;
-    const int nkt = (kv_end + BK - 1) / BK;
     const int nb_seq = (L + BS - 1) / BS;
+    // tile A = the later tokens (last pairs first); tile B the tile before it, if any
+    const int tile_a = ntile - 1 - 2 * (int)p_rel;
+    const int ntiles = tile_a >= 1 ? 2 : 1;
+    int t0x[2], tnx[2], nktx[2];
+    for (int x = 0; x < 2; ++x) {
+        const int t = tile_a - x;
+        t0x[x] = t >= 0 ? t * TT : 0;
+        tnx[x] = t >= 0 ? min(TT, n_new - t0x[x]) : 0;
+        const int kv_end = p.causal ? first_pos + t0x[x] + tnx[x] : L;
+        nktx[x] = x < ntiles ? (kv_end + BK - 1) / BK : 0;
+    }
+    const int nkt = nktx[0];  // tile A reaches at least as far as tile B
+    const int klast = (L - 1) / BK;  // the key tile holding the context end
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < Gm::NBAR; ++i) mbar_init(&bars[i], (&bars[i] == s_free || &bars[i] == p_full) ? 4u : 1u);
+        for (int i = 0; i < Gm::NBAR; ++i) mbar_init(&bars[i], 1u);
+        for (int x = 0; x < 2; ++x) mbar_init(&tb[3 * x + 1], 4u);  // p_full: one arrival per softmax warp
+        mbar_init(v_zeroed, 4u);
         *abort_flag = 0;
         mbar_fence_init();
     }
-    if (warp == 5) {
+    if (warp == W_MMA) {
         tmem_alloc(const_cast<uint32_t*>(taddr_slot), TMEM_COLS);
         tmem_relinquish();
+    }
+    {
+        // Q rows past the G x T (token, head) pairs get no TMA data: zero
+        // them so their scores are finite and their (never stored) rows
+        // take the same unmasked path as the rest of their warp
+        const int pad = TM - G * TT, per_tile = Gm::CH * pad * 8;
+        for (int e = threadIdx.x; e < 2 * per_tile; e += NTHREADS) {
+            const int x = e / per_tile, r0 = e - x * per_tile, c = r0 / (pad * 8), r = r0 - c * pad * 8;
+            *reinterpret_cast<uint4*>(base + Gm::Q_OFF + x * Gm::QT + c * Gm::QCH + (G * TT + r / 8) * 128 +
+                                      (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
     }
     tc_fence_before();
     __syncthreads();
@@ -170,24 +205,34 @@ __global__ void __launch_bounds__(NTHREADS, 2)
         atomicOr(&g_umma_status, kStatusTimeout);
     };
 
-    if (warp == 4) {
-        // ---------------- producer: the whole warp stages block-table
-        // windows (one round trip per 128 tiles), lane 0 issues the TMA loads
+    if (warp == W_KPROD || warp == W_VPROD) {
+        // ---------------- producers: each stages its own block-table
+        // windows; lane 0 waits for the next free slot of its ring, then the
+        // tile's boxes are issued by one lane each in one instruction (a
+        // single thread's TMA issue rate, not bandwidth, would bound the
+        // load otherwise)
+        const int is_v = warp == W_VPROD;
         const uint64_t pol = l2_policy_evict_last();
+        const CUtensorMap* tm = is_v ? &tmV : &tmK;
+        uint64_t* fulls = is_v ? v_full : k_full;
+        uint64_t* emps = is_v ? v_empty : k_empty;
+        int32_t* tbl_s = reinterpret_cast<int32_t*>(base + Gm::TBL_OFF) + is_v * Gm::TBL_INTS;
         if (lane == 0) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmK);
-            prefetch_tmap(&tmV);
-            mbar_arrive_expect_tx(q_full, (uint32_t)(Gm::CH * 128 * G * TT));
+            prefetch_tmap(tm);
+            if (!is_v) {
+                prefetch_tmap(&tmQ);
+                mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * Gm::CH * 128 * G * TT));
+                for (int x = 0; x < ntiles; ++x)
 #pragma unroll
-            for (int c = 0; c < Gm::CH; ++c)
-                tma_load_3d(base + Gm::Q_OFF + c * Gm::QCH, &tmQ, q_full, 64 * c, kvh * G, q0 + t0, pol);
+                    for (int c = 0; c < Gm::CH; ++c)
+                        tma_load_3d(base + Gm::Q_OFF + x * Gm::QT + c * Gm::QCH, &tmQ, q_full, 64 * c, kvh * G,
+                                    q0 + t0x[x], pol);
+            }
         }
-        // pool row of every 16-key group this CTA reads (and of its second
-        // 8-row box with 8-token blocks), staged a window at a time
         const int ngrp = min(nb_seq, nkt * BPT);
         const int32_t* table = p.block_tables + (int64_t)req * p.max_blocks;
         const int bsz = p.block_size;
+        const int per_group = Gm::CH * (bsz == 8 ? 2 : 1);
         bool run = true;
         for (int w0 = 0; w0 < ngrp && run; w0 += kTableWindow) {
             const int wn = min(kTableWindow, ngrp - w0);
@@ -202,156 +247,169 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 }
             }
             __syncwarp();
-            if (lane == 0) {
-                const int kt_end = min(nkt, (w0 + wn + BPT - 1) / BPT);
-                for (int kt = w0 / BPT; kt < kt_end; ++kt) {
-                    if (*abort_flag) {
-                        run = false;
-                        break;
-                    }
-                    const int slot = kt % R;
-                    const uint32_t par = ((uint32_t)(kt / R) & 1u) ^ 1u;
-                    const int nvalid = min(BPT, nb_seq - kt * BPT);
-                    const uint32_t bytes = (uint32_t)(nvalid * Gm::CH * BS * 128);
-                    for (int half = 0; half < 2 && run; ++half) {  // K tile, then V tile
-                        uint64_t* emp = half ? &v_empty[slot] : &k_empty[slot];
-                        uint64_t* ful = half ? &v_full[slot] : &k_full[slot];
-                        if (!mbar_wait_ns(emp, par, WAIT_NS)) {
-                            fail();
-                            run = false;
-                            break;
-                        }
-                        uint8_t* st = base + (half ? Gm::V_OFF : Gm::KV_OFF) + slot * Gm::TILE;
-                        fence_proxy_async_smem();
-                        mbar_arrive_expect_tx(ful, bytes);
-                        for (int j = 0; j < nvalid; ++j) {  // groups past the context are never read
-                            const int e = kt * BPT + j - w0;
-                            const int row = tbl_s[e];
-#pragma unroll
-                            for (int c = 0; c < Gm::CH; ++c) {
-                                uint8_t* dst = st + c * Gm::KCH + j * BS * 128;
-                                if (bsz == 8) {  // two 8-row boxes, each a 1024-byte swizzle atom
-                                    tma_load_3d(dst, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c, row, pol);
-                                    tma_load_3d(dst + 1024, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c,
-                                                tbl_s[kTableWindow + e], pol);
-                                } else {
-                                    tma_load_3d(dst, half ? &tmV : &tmK, ful, 0, kvh * Gm::CH + c, row, pol);
-                                }
-                            }
-                        }
-                    }
-                    if (!run) break;
+            const int kt_end = min(nkt, (w0 + wn + BPT - 1) / BPT);
+            for (int kt = w0 / BPT; kt < kt_end && run; ++kt) {
+                const int slot = kt % R;
+                int ready = 0;
+                if (lane == 0) {
+                    ready = mbar_wait_ns(&emps[slot], ((uint32_t)(kt / R) & 1u) ^ 1u, WAIT_NS) && !*abort_flag;
+                    if (!ready) fail();
+                }
+                if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                    run = false;
+                    break;
+                }
+                const int nvalid = min(BPT, nb_seq - kt * BPT);
+                uint8_t* st = base + (is_v ? Gm::V_OFF : Gm::K_OFF) + slot * Gm::TILE;
+                if (lane == 0) {
+                    fence_proxy_async_smem();
+                    mbar_arrive_expect_tx(&fulls[slot], (uint32_t)(nvalid * Gm::CH * BS * 128));
+                }
+                __syncwarp();
+                // lane = (group j, chunk c[, 8-row half]); groups past the context are never read
+                if (lane < nvalid * per_group) {
+                    const int j = lane / per_group, r = lane - j * per_group;
+                    const int c = bsz == 8 ? (r >> 1) : r, h8 = bsz == 8 ? (r & 1) : 0;
+                    const int e = kt * BPT + j - w0;
+                    const int row = h8 ? tbl_s[kTableWindow + e] : tbl_s[e];
+                    tma_load_3d(st + c * Gm::KCH + j * BS * 128 + h8 * 1024, tm, &fulls[slot], 0,
+                                kvh * Gm::CH + c, row, pol);
                 }
             }
-            run = __shfl_sync(0xffffffffu, run ? 1 : 0, 0) != 0;
             __syncwarp();
         }
-    } else if (warp == 5) {
-        // ---------------- MMA issuer
+    } else if (warp == W_MMA) {
+        // ---------------- MMA issuer, in a fixed staggered order:
+        //   S_A(0) S_B(0) | P V_A(k) S_A(k+1) P V_B(k) S_B(k+1) | ...
+        // so tile A's softmax runs while tile B's MMAs execute and the
+        // other way round.  S_X(k+1) follows P V_X(k) in issue order, which
+        // is what lets S overwrite P in place.  A K (V) slot is released
+        // after the last S (P V) that reads it.
         if (lane == 0) {
             const uint32_t idS = umma_idesc_f16(TM, BK, kBF16, false);
             const uint32_t idO = umma_idesc_f16(TM, HD, kBF16, true);
-            const uint32_t q_s = s_base + Gm::Q_OFF;
-            auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_ns(&v_full[j % R], (uint32_t)(j / R) & 1u, WAIT_NS) ||
-                    !mbar_wait_ns(p_full, (uint32_t)j & 1u, WAIT_NS))
-                    return false;
-                tc_fence_after();
-                const uint32_t v_s = s_base + Gm::V_OFF + (j % R) * Gm::TILE;
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    const uint64_t b = umma_sdesc_sw128(v_s + kk * 16 * 128, Gm::KCH, 1024);
-                    umma_f16_ts(tmem + O_COL, tmem + P_COL + kk * 8, b, idO, (j > 0 || kk > 0) ? 1u : 0u);
-                }
-                umma_commit(o_done);
-                umma_commit(&v_empty[j % R]);
-                return true;
-            };
-            bool ok = mbar_wait_ns(q_full, 0, WAIT_NS);
-            for (int kt = 0; ok && kt < nkt && !*abort_flag; ++kt) {
-                const int slot = kt % R;
-                ok = mbar_wait_ns(&k_full[slot], (uint32_t)(kt / R) & 1u, WAIT_NS) &&
-                     (kt == 0 || mbar_wait_ns(s_free, (uint32_t)(kt - 1) & 1u, WAIT_NS));
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t k_s = s_base + Gm::KV_OFF + slot * Gm::TILE;
+            const int nka = nktx[0], nkb = nktx[1];
+            auto issue_s = [&](int x, int k) {
+                const uint32_t k_s = s_base + Gm::K_OFF + (k % R) * Gm::TILE;
+                const uint32_t q_s = s_base + Gm::Q_OFF + x * Gm::QT;
+                const uint32_t d = tmem + 256u * x + S_COL;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const int c = kk >> 2, koff = (kk & 3) * 32;
-                    const uint64_t a = umma_sdesc_sw128(q_s + c * Gm::QCH + koff, 16, 1024);
-                    const uint64_t b = umma_sdesc_sw128(k_s + c * Gm::KCH + koff, 16, 1024);
-                    umma_f16(tmem + S_COL, a, b, idS, kk > 0 ? 1u : 0u);
+                    const uint64_t qa = umma_sdesc_sw128(q_s + c * Gm::QCH + koff, 16, 1024);
+                    const uint64_t kb = umma_sdesc_sw128(k_s + c * Gm::KCH + koff, 16, 1024);
+                    umma_f16(d, qa, kb, idS, kk > 0 ? 1u : 0u);
                 }
-                umma_commit(s_full);
-                umma_commit(&k_empty[slot]);
-                if (kt > 0) ok = issue_pv(kt - 1);
+                umma_commit(&tb[3 * x]);
+                if (x == 1 || k >= nkb) umma_commit(&k_empty[k % R]);  // last reader of K(k)
+            };
+            auto issue_pv = [&](int x, int j) {
+                const uint32_t v_s = s_base + Gm::V_OFF + (j % R) * Gm::TILE;
+                const uint32_t a_t = tmem + 256u * x + P_COL;
+                const uint32_t d = tmem + 256u * x + O_COL;
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk) {
+                    const uint64_t vb = umma_sdesc_sw128(v_s + kk * 16 * 128, Gm::KCH, 1024);
+                    umma_f16_ts(d, a_t + kk * 8, vb, idO, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                if (j == nktx[x] - 1) umma_commit(&tb[3 * x + 2]);
+                if (x == 1 || j >= nkb) umma_commit(&v_empty[j % R]);  // last reader of V(j)
+            };
+            bool ok = mbar_wait_ns(q_full, 0, WAIT_NS) && mbar_wait_ns(&k_full[0], 0, WAIT_NS);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0, 0);
+                if (nkb > 0) issue_s(1, 0);
             }
-            if (ok && !*abort_flag) ok = issue_pv(nkt - 1);
+            for (int k = 0; ok && k < nka; ++k) {
+                ok = !*abort_flag && mbar_wait_ns(&tb[1], (uint32_t)k & 1u, WAIT_NS) &&
+                     mbar_wait_ns(&v_full[k % R], (uint32_t)(k / R) & 1u, WAIT_NS);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, k);
+                const bool more = k + 1 < nka;
+                if (more) {
+                    ok = mbar_wait_ns(&k_full[(k + 1) % R], (uint32_t)((k + 1) / R) & 1u, WAIT_NS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(0, k + 1);
+                }
+                if (k < nkb) {
+                    ok = mbar_wait_ns(&tb[4], (uint32_t)k & 1u, WAIT_NS);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(1, k);
+                    if (k + 1 < nkb) issue_s(1, k + 1);
+                }
+            }
             if (!ok) fail();
         }
     } else {
-        // ---------------- softmax + epilogue: one query row per thread
-        const int m = threadIdx.x;
-        const bool valid = m < tn * G;
+        // ---------------- softmax + epilogue of tile X: one query row per thread
+        const int x = warp >> 2;
+        const int wq = warp & 3;  // tensor-memory lane quarter of this warp
+        const int my_nkt = nktx[x];
+        uint64_t* s_full = &tb[3 * x];
+        uint64_t* p_full = &tb[3 * x + 1];
+        uint64_t* o_done = &tb[3 * x + 2];
+        const int m = threadIdx.x - 128 * x;
+        const bool valid = x < ntiles && m < tnx[x] * G;
         const int ti = valid ? m / G : 0, gh = valid ? m - (m / G) * G : 0;
-        const int prow = p.causal ? first_pos + t0 + ti : L - 1;
-        const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
+        const int prow = p.causal ? first_pos + t0x[x] + ti : L - 1;
+        const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16) + 256u * x;
+        const float sl = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int kt = 0; kt < nkt; ++kt) {
+        for (int kt = 0; kt < my_nkt; ++kt) {
+            // S_X(kt) complete; its commit also covers P V_X(kt-1), so O and
+            // the P columns are free once this wait returns
             if (*abort_flag || !mbar_wait_ns(s_full, (uint32_t)kt & 1u, WAIT_NS)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float sv[64];
-            {
-                float a[32], b[32];
-                tmem_ld32(t_lane + S_COL, a);
-                tmem_ld32(t_lane + S_COL + 32, b);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    sv[j] = a[j];
-                    sv[32 + j] = b[j];
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free);
-
             const int kbase = kt * BK;
-            // Raw scores; the mask only applies on tiles that reach past the
-            // row's last visible key (the causal diagonal or the context end).
-            // Rows past the request's pairs hold no query: flat zero scores,
-            // so they never force a rescale of the warp.
+            // Mask only on tiles that reach past the row's last visible key
+            // (the causal diagonal or the context end): `vis` = the last
+            // visible column of this tile.  Rows that hold no query of this
+            // request are never stored; they take the unmasked path with
+            // their warp instead of splitting it.
+            const int vis = valid ? min(prow - kbase, BK - 1) : BK - 1;
+            const bool full = vis == BK - 1;  // no masked column (most tiles)
+            // pass 1: the row maximum over the 128 raw scores
             float mx = -INFINITY;
-            if (!valid) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) sv[j] = 0.f;
-                mx = 0.f;
-            } else if (kbase + BK - 1 > prow) {
+            for (int q32 = 0; q32 < BK / 32; ++q32) {
+                float a[32];
+                tmem_ld32(t_lane + S_COL + 32 * q32, a);
+                tmem_wait_ld();
+                if (full) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float x = kbase + j > prow ? -INFINITY : sv[j];
-                    sv[j] = x;
-                    mx = fmaxf(mx, x);
+                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, a[j]);
+                } else {
+                    const int nv = vis - 32 * q32;  // columns j <= nv are visible
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, j <= nv ? a[j] : -INFINITY);
                 }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 64; ++j) mx = fmaxf(mx, sv[j]);
             }
             // exp2 domain: x = s * scale * log2(e); a positive scale keeps the
             // order, so the maximum is taken on raw scores and the scaling is
             // fused into the exponent's argument
-            const float sl = p.scale_log2;
             float m_tile;
             if (sl > 0.f) {
                 m_tile = mx * sl;
             } else {
                 m_tile = -INFINITY;
 #pragma unroll
-                for (int j = 0; j < 64; ++j) m_tile = fmaxf(m_tile, sv[j] == -INFINITY ? -INFINITY : sv[j] * sl);
+                for (int q32 = 0; q32 < BK / 32; ++q32) {
+                    float a[32];
+                    tmem_ld32(t_lane + S_COL + 32 * q32, a);
+                    tmem_wait_ld();
+                    const int nv = vis - 32 * q32;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (j <= nv) m_tile = fmaxf(m_tile, a[j] * sl);
+                }
             }
             const float m_new = fmaxf(m_used, m_tile);
             const bool grow = (m_used == -INFINITY) || (m_new > m_used + 8.f);
@@ -361,26 +419,38 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                 m_used = m_new;
             }
             const float neg_m = -m_used;
+            // pass 2: 32 keys at a time, exponentials packed two per column
+            // into the low half of the S columns (already read back); masked
+            // keys get exactly 0
             float sum = 0.f;
-            uint32_t pk[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float a0 = sv[2 * j] == -INFINITY ? -INFINITY : fmaf(sv[2 * j], sl, neg_m);
-                const float a1 = sv[2 * j + 1] == -INFINITY ? -INFINITY : fmaf(sv[2 * j + 1], sl, neg_m);
-                const float e0 = fast_exp2(a0), e1 = fast_exp2(a1);
-                sum += e0 + e1;
-                pk[j] = pack2<T>(e0, e1);
+            for (int q32 = 0; q32 < BK / 32; ++q32) {
+                float a[32];
+                tmem_ld32(t_lane + S_COL + 32 * q32, a);
+                tmem_wait_ld();
+                uint32_t pk[16];
+                if (full) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
+                        const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
+                        sum += e0 + e1;
+                        pk[j] = pack2<T>(e0, e1);
+                    }
+                } else {
+                    const int nv = vis - 32 * q32;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float e0 = 2 * j <= nv ? fast_exp2(fmaf(a[2 * j], sl, neg_m)) : 0.f;
+                        const float e1 = 2 * j + 1 <= nv ? fast_exp2(fmaf(a[2 * j + 1], sl, neg_m)) : 0.f;
+                        sum += e0 + e1;
+                        pk[j] = pack2<T>(e0, e1);
+                    }
+                }
+                tmem_st16(t_lane + P_COL + 16 * q32, pk);
             }
             l = l * alpha + sum;
             const bool rescale = __any_sync(0xffffffffu, grow && kt > 0);
-
-            if (kt > 0) {  // P V of the previous tile must be done: P buffer and O are shared
-                if (!mbar_wait_ns(o_done, (uint32_t)(kt - 1) & 1u, WAIT_NS)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
             if (rescale) {
 #pragma unroll
                 for (int c = 0; c < HD / 32; ++c) {
@@ -391,67 +461,69 @@ __global__ void __launch_bounds__(NTHREADS, 2)
                     for (int j = 0; j < 32; ++j) o[j] *= alpha;
                     tmem_st32(t_lane + O_COL + 32 * c, o);
                 }
-                tmem_wait_st();
             }
-            // keys at or past L hold no context: zero their V rows of this stage
-            const int keep = L - kbase;
-            if (keep < BK) {
-                // this tile's V must have landed before its tail rows are cleared
-                if (!mbar_wait_ns(&v_full[kt % R], (uint32_t)(kt / R) & 1u, WAIT_NS)) {
+            tmem_wait_st();
+            // Keys at or past L hold no context: their V rows of the tile that
+            // holds the context end are zeroed once, by tile A's warps (tile A
+            // reads every key tile tile B reads); tile B waits for that.
+            if (kt == klast && L - kbase < BK) {
+                if (x == 0) {
+                    if (!mbar_wait_ns(&v_full[kt % R], (uint32_t)(kt / R) & 1u, WAIT_NS)) {
+                        ok = false;
+                        break;
+                    }
+                    const int keep = L - kbase;
+                    uint8_t* v_t = base + Gm::V_OFF + (kt % R) * Gm::TILE;
+                    const int rows = BK - keep;
+                    for (int e = m; e < rows * Gm::CH * 8; e += 128) {
+                        const int c = e / (rows * 8), rem = e - c * rows * 8, r = keep + rem / 8, q16 = rem & 7;
+                        *reinterpret_cast<uint4*>(v_t + c * Gm::KCH + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(v_zeroed);
+                } else if (!mbar_wait_ns(v_zeroed, 0, WAIT_NS)) {
                     ok = false;
                     break;
                 }
-                uint8_t* v_t = base + Gm::V_OFF + (kt % R) * Gm::TILE;
-                const int rows = BK - keep;
-                for (int e = threadIdx.x; e < rows * Gm::CH * 8; e += 128) {
-                    const int c = e / (rows * 8), rem = e - c * rows * 8, r = keep + rem / 8, q16 = rem & 7;
-                    *reinterpret_cast<uint4*>(v_t + c * Gm::KCH + r * 128 + q16 * 16) = make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-            }
-            // P row: 64 keys packed two per column into tensor memory
-            {
-                float pf[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) pf[j] = __uint_as_float(pk[j]);
-                tmem_st32(t_lane + P_COL, pf);
-                tmem_wait_st();
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
-        if (ok && !*abort_flag && mbar_wait_ns(o_done, (uint32_t)(nkt - 1) & 1u, WAIT_NS)) {
-            tc_fence_after();
-            const float inv = 1.f / l;
-            T* orow = static_cast<T*>(p.out) +
-                      ((int64_t)(q0 + t0 + ti) * p.num_heads + (int64_t)kvh * G + gh) * HD;
+        if (my_nkt > 0) {
+            if (ok && !*abort_flag && mbar_wait_ns(o_done, 0, WAIT_NS)) {
+                tc_fence_after();
+                const float inv = 1.f / l;
+                T* orow = static_cast<T*>(p.out) +
+                          ((int64_t)(q0 + t0x[x] + ti) * p.num_heads + (int64_t)kvh * G + gh) * HD;
+#pragma unroll 1
+                for (int c = 0; c < HD / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(t_lane + O_COL + 32 * c, o);
+                    tmem_wait_ld();
+                    if (valid) {
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                float o[32];
-                tmem_ld32(t_lane + O_COL + 32 * c, o);
-                tmem_wait_ld();
-                if (valid) {
-#pragma unroll
-                    for (int q16 = 0; q16 < 4; ++q16) {
-                        uint4 v;
-                        v.x = pack2<T>(o[8 * q16 + 0] * inv, o[8 * q16 + 1] * inv);
-                        v.y = pack2<T>(o[8 * q16 + 2] * inv, o[8 * q16 + 3] * inv);
-                        v.z = pack2<T>(o[8 * q16 + 4] * inv, o[8 * q16 + 5] * inv);
-                        v.w = pack2<T>(o[8 * q16 + 6] * inv, o[8 * q16 + 7] * inv);
-                        *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q16) = v;
+                        for (int q16 = 0; q16 < 4; ++q16) {
+                            uint4 v;
+                            v.x = pack2<T>(o[8 * q16 + 0] * inv, o[8 * q16 + 1] * inv);
+                            v.y = pack2<T>(o[8 * q16 + 2] * inv, o[8 * q16 + 3] * inv);
+                            v.z = pack2<T>(o[8 * q16 + 4] * inv, o[8 * q16 + 5] * inv);
+                            v.w = pack2<T>(o[8 * q16 + 6] * inv, o[8 * q16 + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * q16) = v;
+                        }
                     }
                 }
+            } else {
+                fail();
             }
-        } else if (!ok || *abort_flag) {
-            fail();
         }
     }
 
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 5) tmem_dealloc(tmem, TMEM_COLS);
+    if (warp == W_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
 // ---------------------------------------------------------------- host side
@@ -523,13 +595,13 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     p.block_size = a.block_size;
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const int64_t tiles = (int64_t)a.total_q / TT + a.num_seqs;
+    const int64_t pairs = (int64_t)a.total_q / (2 * TT) + a.num_seqs;
     const size_t smem = um_smem_bytes<HD>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)tiles, (unsigned)a.num_kv_heads);
+    cfg.gridDim = dim3((unsigned)pairs, (unsigned)a.num_kv_heads);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;

@@ -23,13 +23,21 @@ def pa():
     return pa
 
 
-def run_varlen(pa, w, kc, vc, bt, causal=None, kernel=0):
+def run_varlen(pa, w, kc, vc, bt, causal=None, kernel=0, routed=False):
+    """routed: pass a workspace of pa_varlen_workspace_size bytes (the
+    library must accept both that and none)."""
     pa.pa_set_option(pa.PA_OPT_VARLEN_KERNEL, kernel)
     try:
         out = torch.full(tuple(w.q.shape), float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
+        mq, mc = int(w.query_lens.max()), int(w.seq_lens.max())
+        ws = None
+        if routed:
+            n = pa.pa_varlen_workspace_size(w.num_seqs, int(w.query_lens.sum()), mq, w.num_heads, w.num_kv_heads,
+                                            w.head_dim, w.block_size, mc, W.TORCH_DTYPES[w.dtype])
+            ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
         pa.pa_varlen(out, w.q.to(DEV), kc, vc, bt, torch.from_numpy(w.seq_lens).to(DEV),
-                     torch.from_numpy(w.query_start_loc).to(DEV), int(w.query_lens.max()), int(w.seq_lens.max()),
-                     w.scale, causal=w.causal if causal is None else causal)
+                     torch.from_numpy(w.query_start_loc).to(DEV), mq, mc,
+                     w.scale, causal=w.causal if causal is None else causal, workspace=ws)
         torch.cuda.synchronize()
         return out
     finally:
@@ -124,6 +132,7 @@ def test_random_varlen_tensor_core_kernels(pa, dt, hd, g, hkv, lens, qlens, seed
         exact = oracle_attention(w, causal=causal)
         for kernel in (2, 3):
             compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=kernel), exact)
+        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3, routed=True), exact)
 
 
 def test_varlen_kernels_agree_on_mixed_step(pa):
@@ -138,21 +147,21 @@ def test_varlen_kernels_agree_on_mixed_step(pa):
 def test_mixed_varlen_full_tcgen05(pa):
     w = W.mixed_varlen(device=DEV)
     kc, vc, bt = device_caches(w, DEV)
-    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=3), oracle_attention(w))
-    pa.pa_device_status(clear=True)
+    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=3, routed=True), oracle_attention(w))
+    pa.pa_device_status(clear=True)  # raises if a kernel recorded a timeout
 
 
-@pytest.mark.parametrize("kernel", [2, 3])
-def test_varlen_permutation_bit_identical(pa, kernel):
+@pytest.mark.parametrize("kernel,routed", [(2, False), (3, False), (3, True)])
+def test_varlen_permutation_bit_identical(pa, kernel, routed):
     w = W.varlen_workload("perm_v", "bf16", 16, 12, 2, 128, [300, 81, 17, 1000], [1, 81, 5, 130], seed=3)
     kc, vc, bt = device_caches(w, DEV)
-    base = run_varlen(pa, w, kc, vc, bt, kernel=kernel)
+    base = run_varlen(pa, w, kc, vc, bt, kernel=kernel, routed=routed)
     perm = torch.from_numpy(np.random.default_rng(4).permutation(w.num_blocks)).to(DEV)
     kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
     kc2[perm] = kc
     vc2[perm] = vc
     bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
-    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=kernel)
+    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=kernel, routed=routed)
     assert torch.equal(base.view(torch.int16), again.view(torch.int16))
 
 
@@ -166,4 +175,6 @@ def test_varlen_tcgen05_block_sizes(pa, bs):
     w = W.varlen_workload("vl_bs", "bf16", bs, 12, 2, 128, lens.tolist(), q.tolist(), seed=bs)
     kc, vc, bt = device_caches(w, DEV)
     for causal in (True, False):
-        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3), oracle_attention(w, causal=causal))
+        exact = oracle_attention(w, causal=causal)
+        for routed in (False, True):
+            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3, routed=routed), exact)
