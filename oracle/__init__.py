@@ -11,7 +11,8 @@ arrays (host memory) and return numpy arrays.  Element types: "f32",
 "bf16", "f16"; 16-bit buffers are passed as raw uint16 bit patterns.
 
 Pinned functions (see tests/test_oracle_pins.py): slot translation, write,
-block copy, gather, attention, and the block bookkeeping.  None is unpinned.
+block copy, block swap, gather, attention, and the block bookkeeping.  None is
+unpinned.
 """
 import ctypes
 import os
