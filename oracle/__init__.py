@@ -11,8 +11,9 @@ arrays (host memory) and return numpy arrays.  Element types: "f32",
 "bf16", "f16"; 16-bit buffers are passed as raw uint16 bit patterns.
 
 Pinned functions (see tests/test_oracle_pins.py): slot translation, write,
-block copy, block swap, gather, attention, and the block bookkeeping.  None is
-unpinned.
+block copy, block swap, gather, attention, the FP8 E4M3 codes, the quantizing
+write and attention over a quantized cache, and the block bookkeeping.  None
+is unpinned.
 """
 import ctypes
 import os
@@ -50,6 +51,17 @@ def lib():
         L.oracle_paged_attention.restype = None
         L.oracle_decode.argtypes = [vp, i64, ctypes.c_int, vp]
         L.oracle_decode.restype = None
+        L.oracle_e4m3_encode_array.argtypes = [vp, i64, vp]
+        L.oracle_e4m3_encode_array.restype = None
+        L.oracle_e4m3_decode_array.argtypes = [vp, i64, vp]
+        L.oracle_e4m3_decode_array.restype = None
+        L.oracle_quant_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp]
+        L.oracle_quant_rows.restype = None
+        L.oracle_write_kv_fp8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i32, i32, vp, vp, vp, vp]
+        L.oracle_write_kv_fp8.restype = None
+        L.oracle_paged_attention_fp8.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32,
+                                                 i32, i32, i32, ctypes.c_float, ctypes.c_int, ctypes.c_int]
+        L.oracle_paged_attention_fp8.restype = None
         L.oracle_max_threads.argtypes = []
         L.oracle_max_threads.restype = ctypes.c_int
         _lib = L
@@ -155,3 +167,62 @@ def decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale: flo
     qsl = np.arange(s + 1, dtype=np.int32)
     return paged_attention(q, k_cache, v_cache, block_tables, context_lens, qsl, scale, dtype, True,
                            seq_select, num_threads)
+
+
+# ---- quantized (FP8 E4M3) cache --------------------------------------------
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> E4M3 codes (nearest, ties to even, held at +-448)."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    lib().oracle_e4m3_encode_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    lib().oracle_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def quant_rows(x, dtype: str):
+    """Rows [..., row_len] (raw element buffer) -> (codes uint8 same shape, scales float32 [...])."""
+    x = _c(x)
+    row_len = x.shape[-1]
+    n = x.size // row_len
+    codes = np.empty(x.shape, dtype=np.uint8)
+    scales = np.empty(x.shape[:-1], dtype=np.float32)
+    lib().oracle_quant_rows(_ptr(x), DTYPES[dtype], n, row_len, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def write_kv_fp8(k, v, dtype: str, slot_mapping_, k_codes, v_codes, k_scales, v_scales) -> None:
+    """In place: k, v [n, Hkv, hd] (raw, `dtype`) quantized into codes [NB, bs, Hkv, hd] and
+    scales [NB, bs, Hkv] at the slots (negative slots skipped)."""
+    k, v = _c(k), _c(v)
+    sm = _c(slot_mapping_, np.int64)
+    for a in (k_codes, v_codes, k_scales, v_scales):
+        assert a.flags.c_contiguous
+    n, hkv, hd = k.shape
+    lib().oracle_write_kv_fp8(_ptr(k), _ptr(v), DTYPES[dtype], _ptr(sm), sm.shape[0], hkv, hd, _ptr(k_codes),
+                              _ptr(v_codes), _ptr(k_scales), _ptr(v_scales))
+
+
+def paged_attention_fp8(q, q_dtype: str, k_codes, v_codes, k_scales, v_scales, block_tables, seq_lens,
+                        query_start_loc, scale: float, causal: bool = True, num_threads: int = 0) -> np.ndarray:
+    """Varlen paged attention over a quantized cache, float64 [total_q, Hq, hd]."""
+    q = _c(q)
+    kc, vc = _c(k_codes, np.uint8), _c(v_codes, np.uint8)
+    ks, vs = _c(k_scales, np.float32), _c(v_scales, np.float32)
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    qsl = _c(query_start_loc, np.int32)
+    total_q, hq, hd = q.shape
+    nb, bs, hkv, hd2 = kc.shape
+    assert hd2 == hd and hq % hkv == 0 and ks.shape == (nb, bs, hkv)
+    out = np.full((total_q, hq, hd), np.nan, dtype=np.float64)
+    lib().oracle_paged_attention_fp8(_ptr(out), _ptr(q), DTYPES[q_dtype], _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                                     _ptr(bt), bt.shape[1], _ptr(sl), _ptr(qsl), sl.shape[0], hq, hkv, hd, bs,
+                                     ctypes.c_float(scale), 1 if causal else 0, num_threads)
+    return out

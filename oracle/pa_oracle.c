@@ -24,6 +24,16 @@
  *     first seq_len tokens through the block table, repeat KV heads with
  *     repeat_interleave, scores = q.k * scale, causal mask
  *     tril(diagonal = seq_len - num_new), softmax, P.V).
+ *   - quantized cache: "KV cache：容量推导、分页与回收" names a quantized
+ *     cache (量化缓存) as something that changes the per-token size, with no
+ *     method.  The reading taken here: FP8 E4M3 codes (the OCP 8-bit
+ *     floating-point format: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *     bits, no infinities, S.1111.111 = NaN, largest finite 448) with one
+ *     fp32 scale per written (token, KV head) row, scale = max|x| / 448
+ *     (1 for an all-zero row), code = x / scale rounded to the nearest code,
+ *     ties to the even code, values beyond 448 held at 448.  The division
+ *     and the maximum are taken in fp32, the precision the GPU takes the
+ *     same decisions in; the attention reads code value x scale exactly.
  *
  * Element types: 0 = fp32, 1 = bf16, 2 = fp16.  Inputs are decoded to double
  * exactly from their bit patterns; results are returned in double.  The
@@ -158,6 +168,85 @@ void oracle_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst
     }
 }
 
+/* ---- FP8 E4M3 codes ------------------------------------------------------- */
+
+/* Value of a code, from the format's definition: exponent field e, mantissa
+ * field m: normal (e > 0): (1 + m/8) 2^(e-7) = (8 + m) 2^(e-10); subnormal
+ * (e = 0): (m/8) 2^-6 = m 2^-9; e = 15 with m = 7 is NaN. */
+double oracle_e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+/* Nearest code to x (ties to the code with an even mantissa), |x| > 448
+ * held at +-448, NaN to 0x7F: a search over the 127 finite non-negative
+ * codes, whose values increase with the code. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7E;
+    uint8_t best = 0;
+    double best_d = a;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(oracle_e4m3_value((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = (uint8_t)c;
+            best_d = d;
+        }
+    }
+    return sign | best;
+}
+
+void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+
+void oracle_e4m3_decode_array(const uint8_t* c, int64_t n, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_value(c[i]);
+}
+
+/* One row of row_len elements (src in `dtype`) -> codes and its scale. */
+static void quant_row(const void* src, int64_t first, int32_t row_len, int dtype, uint8_t* codes, float* scale) {
+    float amax = 0.0f;
+    for (int32_t e = 0; e < row_len; ++e) {
+        const float x = (float)load_elt(src, first + e, dtype);
+        amax = fmaxf(amax, fabsf(x));
+    }
+    const float s = amax > 0.0f ? amax / 448.0f : 1.0f;
+    for (int32_t e = 0; e < row_len; ++e) {
+        const float x = (float)load_elt(src, first + e, dtype);
+        codes[e] = oracle_e4m3_encode(x / s);
+    }
+    *scale = s;
+}
+
+/* rows [n_rows, row_len] -> codes [n_rows, row_len], scales [n_rows] */
+void oracle_quant_rows(const void* src, int dtype, int64_t n_rows, int32_t row_len, uint8_t* codes, float* scales) {
+    for (int64_t r = 0; r < n_rows; ++r)
+        quant_row(src, r * row_len, row_len, dtype, codes + r * row_len, scales + r);
+}
+
+/* The quantizing write: token i's K and V rows ([n, num_kv_heads, head_dim]
+ * in `dtype`) go, one (token, KV head) row at a time, to codes at
+ * (slot * num_kv_heads + h) * head_dim and scales at slot * num_kv_heads + h;
+ * negative slots are skipped. */
+void oracle_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
+                         int32_t num_kv_heads, int32_t head_dim, uint8_t* k_codes, uint8_t* v_codes,
+                         float* k_scales, float* v_scales) {
+    for (int64_t i = 0; i < n; ++i) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0) continue;
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            const int64_t src = (i * num_kv_heads + h) * head_dim, dst = slot * num_kv_heads + h;
+            quant_row(k, src, head_dim, dtype, k_codes + dst * head_dim, k_scales + dst);
+            quant_row(v, src, head_dim, dtype, v_codes + dst * head_dim, v_scales + dst);
+        }
+    }
+}
+
 /* ---- gather --------------------------------------------------------------- */
 
 /* The first seq_len tokens of one sequence in logical order, as double
@@ -180,6 +269,48 @@ void oracle_gather(const void* cache, const int32_t* block_table, int32_t seq_le
 
 /* ---- attention ------------------------------------------------------------ */
 
+/* One request's rows, from its K and V gathered as double [seq_len, num_kv_heads, head_dim]. */
+static void attend_request(double* out, const void* q, int q_dtype, const double* k, const double* v,
+                           int32_t seq_len, int32_t start, int32_t num_new, int32_t num_heads, int32_t num_kv_heads,
+                           int32_t head_dim, double sc, int causal) {
+    const int32_t rep = num_heads / num_kv_heads;
+    const int64_t row = (int64_t)num_kv_heads * head_dim;
+    double* p = (double*)malloc(sizeof(double) * (size_t)seq_len);
+    double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
+    for (int32_t j = 0; j < num_new; ++j) {
+        const int64_t qrow = start + j;
+        const int64_t pos = (int64_t)seq_len - num_new + j;
+        const int32_t visible = causal ? (int32_t)(pos + 1) : seq_len;
+        for (int32_t h = 0; h < num_heads; ++h) {
+            const int32_t kvh = h / rep;
+            for (int32_t d = 0; d < head_dim; ++d) qv[d] = load_elt(q, (qrow * num_heads + h) * head_dim + d, q_dtype);
+            /* scores over the visible keys */
+            double m = -INFINITY;
+            for (int32_t s = 0; s < visible; ++s) {
+                double dot = 0.0;
+                for (int32_t d = 0; d < head_dim; ++d) dot += qv[d] * k[s * row + (int64_t)kvh * head_dim + d];
+                p[s] = dot * sc;
+                if (p[s] > m) m = p[s];
+            }
+            /* softmax */
+            double denom = 0.0;
+            for (int32_t s = 0; s < visible; ++s) {
+                p[s] = exp(p[s] - m);
+                denom += p[s];
+            }
+            /* P . V */
+            double* o = out + (qrow * num_heads + h) * head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                double acc = 0.0;
+                for (int32_t s = 0; s < visible; ++s) acc += p[s] * v[s * row + (int64_t)kvh * head_dim + d];
+                o[d] = acc / denom;
+            }
+        }
+    }
+    free(p);
+    free(qv);
+}
+
 /*
  * Varlen paged attention, request by request:
  *   q, out:           [total_q, num_heads, head_dim]  (q in `dtype`, out double)
@@ -199,8 +330,6 @@ void oracle_paged_attention(double* out, const void* q, const void* k_cache, con
                             int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                             int32_t head_dim, int32_t block_size, float scale, int causal,
                             int dtype, const uint8_t* seq_select, int num_threads) {
-    const int32_t rep = num_heads / num_kv_heads;
-    const double sc = (double)scale;
 #ifdef _OPENMP
     if (num_threads > 0) omp_set_num_threads(num_threads);
 #pragma omp parallel for schedule(dynamic, 1)
@@ -208,55 +337,60 @@ void oracle_paged_attention(double* out, const void* q, const void* k_cache, con
     for (int32_t i = 0; i < num_seqs; ++i) {
         if (seq_select && !seq_select[i]) continue;
         const int32_t seq_len = seq_lens[i];
-        const int32_t start = query_start_loc[i], end = query_start_loc[i + 1];
-        const int32_t num_new = end - start;
+        const int32_t start = query_start_loc[i], num_new = query_start_loc[i + 1] - start;
         if (seq_len <= 0 || num_new <= 0) continue;
         const int32_t* table = block_tables + (int64_t)i * max_blocks;
         const int64_t row = (int64_t)num_kv_heads * head_dim;
         double* k = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
         double* v = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
-        double* p = (double*)malloc(sizeof(double) * (size_t)seq_len);
-        double* qv = (double*)malloc(sizeof(double) * (size_t)head_dim);
         oracle_gather(k_cache, table, seq_len, block_size, num_kv_heads, head_dim, dtype, k);
         oracle_gather(v_cache, table, seq_len, block_size, num_kv_heads, head_dim, dtype, v);
-        for (int32_t j = 0; j < num_new; ++j) {
-            const int64_t qrow = start + j;
-            const int64_t pos = (int64_t)seq_len - num_new + j;
-            const int32_t visible = causal ? (int32_t)(pos + 1) : seq_len;
-            for (int32_t h = 0; h < num_heads; ++h) {
-                const int32_t kvh = h / rep;
-                for (int32_t d = 0; d < head_dim; ++d) qv[d] = load_elt(q, (qrow * num_heads + h) * head_dim + d, dtype);
-                /* scores over the visible keys */
-                double m = -INFINITY;
-                for (int32_t s = 0; s < visible; ++s) {
-                    double dot = 0.0;
-                    for (int32_t d = 0; d < head_dim; ++d) dot += qv[d] * k[s * row + (int64_t)kvh * head_dim + d];
-                    p[s] = dot * sc;
-                    if (p[s] > m) m = p[s];
-                }
-                /* softmax */
-                double denom = 0.0;
-                for (int32_t s = 0; s < visible; ++s) {
-                    p[s] = exp(p[s] - m);
-                    denom += p[s];
-                }
-                /* P . V */
-                double* o = out + (qrow * num_heads + h) * head_dim;
-                for (int32_t d = 0; d < head_dim; ++d) {
-                    double acc = 0.0;
-                    for (int32_t s = 0; s < visible; ++s) acc += p[s] * v[s * row + (int64_t)kvh * head_dim + d];
-                    o[d] = acc / denom;
-                }
-            }
-        }
+        attend_request(out, q, dtype, k, v, seq_len, start, num_new, num_heads, num_kv_heads, head_dim,
+                       (double)scale, causal);
         free(k);
         free(v);
-        free(p);
-        free(qv);
     }
 }
 
-/* Number of OpenMP threads a parallel region would use (1 without OpenMP). */
+/* The same over a quantized cache: K and V codes [num_blocks, block_size,
+ * num_kv_heads, head_dim] with scales [num_blocks, block_size, num_kv_heads];
+ * a key or value element reads code value x its row's scale (exact in
+ * double); q (and so the output's element type) is `q_dtype`. */
+void oracle_paged_attention_fp8(double* out, const void* q, int q_dtype, const uint8_t* k_codes,
+                                const uint8_t* v_codes, const float* k_scales, const float* v_scales,
+                                const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, int32_t num_seqs, int32_t num_heads,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, float scale,
+                                int causal, int num_threads) {
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int32_t i = 0; i < num_seqs; ++i) {
+        const int32_t seq_len = seq_lens[i];
+        const int32_t start = query_start_loc[i], num_new = query_start_loc[i + 1] - start;
+        if (seq_len <= 0 || num_new <= 0) continue;
+        const int32_t* table = block_tables + (int64_t)i * max_blocks;
+        const int64_t row = (int64_t)num_kv_heads * head_dim;
+        double* k = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
+        double* v = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
+        for (int32_t t = 0; t < seq_len; ++t) {
+            const int64_t slot = (int64_t)table[t / block_size] * block_size + t % block_size;
+            for (int32_t h = 0; h < num_kv_heads; ++h) {
+                const int64_t r = slot * num_kv_heads + h;
+                for (int32_t d = 0; d < head_dim; ++d) {
+                    k[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(k_codes[r * head_dim + d]) * (double)k_scales[r];
+                    v[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(v_codes[r * head_dim + d]) * (double)v_scales[r];
+                }
+            }
+        }
+        attend_request(out, q, q_dtype, k, v, seq_len, start, num_new, num_heads, num_kv_heads, head_dim,
+                       (double)scale, causal);
+        free(k);
+        free(v);
+    }
+}
+
 int oracle_max_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -437,3 +437,115 @@ def test_swap_out_and_back_is_identity_and_moves_whole_blocks():
     for l in range(2):
         for (d_old, h), (_, d_new) in zip(out_pairs, in_pairs):
             assert np.array_equal(dev_k[l][d_new], k0[l][d_old]) and np.array_equal(dev_v[l][d_new], v0[l][d_old])
+
+
+# ---- quantized cache (FP8 E4M3 codes, one scale per token and KV head) ----
+
+def _torch_fp8():
+    import torch
+
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("this torch has no float8_e4m3fn")
+    return torch
+
+
+def test_e4m3_values_of_all_256_codes_match_torch():
+    """The code table against torch's own float8_e4m3fn decoding (a library
+    routine): every finite value and the two NaN codes."""
+    torch = _torch_fp8()
+    codes = np.arange(256, dtype=np.uint8)
+    ours = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ours[fin], ref[fin])
+    assert np.isnan(ours).sum() == 2 and ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+def test_e4m3_encode_matches_torch_in_range_and_ties_go_to_even():
+    """Rounding against torch's conversion (round to nearest even) on random
+    values and on every midpoint between neighbouring codes; out of range
+    (where torch gives NaN) the format's largest finite value is kept."""
+    torch = _torch_fp8()
+    grid = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))  # 0 .. 448 increasing
+    mids = ((grid[1:] + grid[:-1]) / 2).astype(np.float32)
+    rng = np.random.default_rng(8)
+    rand = (rng.standard_normal(20000) * np.exp2(rng.integers(-12, 9, 20000))).astype(np.float32)
+    x = np.concatenate([mids, -mids, rand[np.abs(rand) <= 448], grid.astype(np.float32)])
+    ours = oracle.e4m3_encode(x)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+    # ties: the even mantissa wins (1.0625 -> 1.0, 1.1875 -> 1.25, 232 -> 224)
+    assert oracle.e4m3_decode(oracle.e4m3_encode(np.array([1.0625, 1.1875, 232.0], np.float32))).tolist() == \
+        [1.0, 1.25, 224.0]
+    big = oracle.e4m3_encode(np.array([449.0, 464.0, 1e6, -3e38, np.inf], np.float32))
+    assert big.tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0x7E]
+    assert oracle.e4m3_encode(np.array([np.nan], np.float32))[0] == 0x7F
+
+
+def test_quant_rows_scale_max_code_and_error_bound():
+    """scale = max|x| / 448 (fp32), the largest element encodes to +-448, and
+    every element comes back within half a code step: 2^-4 relative for
+    normal codes, 2^-10 x scale below them; an all-zero row keeps scale 1."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((64, 128)) * np.exp2(rng.integers(-8, 8, (64, 1)))).astype(np.float32)
+    x[5] = 0.0
+    codes, scales = oracle.quant_rows(x, "f32")
+    amax = np.abs(x).max(axis=1)
+    want = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    assert np.array_equal(scales, want)
+    dq = oracle.e4m3_decode(codes) * scales[:, None].astype(np.float64)
+    big = np.argmax(np.abs(x), axis=1)
+    for r in range(64):
+        if amax[r] > 0:
+            assert abs(oracle.e4m3_decode(codes[r, big[r]])) == 448.0
+    err = np.abs(dq - x.astype(np.float64))
+    bound = np.exp2(-4) * np.abs(x) + np.exp2(-10) * scales[:, None] + 1e-6 * np.abs(x)
+    assert np.all(err <= bound)
+    assert np.all(codes[5] == 0) and scales[5] == 1.0
+
+
+def _grid_pool(rng, nb, bs, hkv, hd):
+    """K/V values on the E4M3 grid times a power-of-two row scale, each row
+    holding +-448 x scale: quantizing them is lossless."""
+    codes = rng.integers(0, 0x7F, (nb, bs, hkv, hd)).astype(np.uint8)
+    codes |= (rng.integers(0, 2, codes.shape).astype(np.uint8) << 7)
+    codes[..., 0] = np.where(rng.integers(0, 2, codes.shape[:-1]) == 1, 0x7E, 0xFE)
+    scales = np.exp2(rng.integers(-9, -2, (nb, bs, hkv))).astype(np.float32)
+    vals = (oracle.e4m3_decode(codes) * scales[..., None]).astype(np.float32)
+    return codes, scales, vals
+
+
+def test_fp8_write_and_attention_are_lossless_on_grid_values():
+    """On values a quantized cache holds exactly, the quantizing write
+    reproduces the codes and scales, and attention over the codes equals the
+    pinned attention over the same values stored as fp32, bit for bit; a
+    swapped K/V scale changes the result."""
+    rng = np.random.default_rng(5)
+    nb, bs, hkv, hd, hq = 12, 4, 2, 16, 6
+    kcodes, kscales, kvals = _grid_pool(rng, nb, bs, hkv, hd)
+    vcodes, vscales, vvals = _grid_pool(rng, nb, bs, hkv, hd)
+    # the write: tokens in slot order
+    slots = np.arange(nb * bs, dtype=np.int64)
+    wk = np.zeros_like(kcodes)
+    wv = np.zeros_like(vcodes)
+    wks = np.zeros_like(kscales)
+    wvs = np.zeros_like(vscales)
+    oracle.write_kv_fp8(kvals.reshape(-1, hkv, hd), vvals.reshape(-1, hkv, hd), "f32", slots, wk, wv, wks, wvs)
+    assert np.array_equal(wk, kcodes) and np.array_equal(wv, vcodes)
+    assert np.array_equal(wks, kscales) and np.array_equal(wvs, vscales)
+    lens = np.array([7, 1, 20], np.int32)
+    qlens = np.array([3, 1, 20], np.int32)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = np.full((3, 6), -1, np.int32)
+    tables[0, :2], tables[1, :1], tables[2, :5] = perm[:2], perm[2:3], perm[3:8]
+    q = rng.standard_normal((int(qlens.sum()), hq, hd)).astype(np.float32)
+    for causal in (True, False):
+        got = oracle.paged_attention_fp8(q, "f32", kcodes, vcodes, kscales, vscales, tables, lens, qsl, 0.25,
+                                         causal=causal)
+        exact = oracle.paged_attention(q, kvals, vvals, tables, lens, qsl, 0.25, "f32", causal=causal)
+        assert np.array_equal(got, exact)
+        wrong = oracle.paged_attention_fp8(q, "f32", kcodes, vcodes, vscales, kscales, tables, lens, qsl, 0.25,
+                                           causal=causal)
+        assert not np.allclose(wrong, exact)
