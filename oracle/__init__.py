@@ -57,7 +57,7 @@ def lib():
         L.oracle_e4m3_decode_array.restype = None
         L.oracle_quant_rows.argtypes = [vp, ctypes.c_int, i64, i32, vp, vp]
         L.oracle_quant_rows.restype = None
-        L.oracle_write_kv_fp8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i32, i32, vp, vp, vp, vp]
+        L.oracle_write_kv_fp8.argtypes = [vp, vp, ctypes.c_int, vp, i64, i32, i32, i32, vp, vp, vp, vp]
         L.oracle_write_kv_fp8.restype = None
         L.oracle_paged_attention_fp8.argtypes = [vp, vp, ctypes.c_int, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32,
                                                  i32, i32, i32, ctypes.c_float, ctypes.c_int, ctypes.c_int]
@@ -199,13 +199,15 @@ def quant_rows(x, dtype: str):
 
 def write_kv_fp8(k, v, dtype: str, slot_mapping_, k_codes, v_codes, k_scales, v_scales) -> None:
     """In place: k, v [n, Hkv, hd] (raw, `dtype`) quantized into codes [NB, bs, Hkv, hd] and
-    scales [NB, bs, Hkv] at the slots (negative slots skipped)."""
+    scales [NB, Hkv, bs] at the slots (negative slots skipped)."""
     k, v = _c(k), _c(v)
     sm = _c(slot_mapping_, np.int64)
     for a in (k_codes, v_codes, k_scales, v_scales):
         assert a.flags.c_contiguous
     n, hkv, hd = k.shape
-    lib().oracle_write_kv_fp8(_ptr(k), _ptr(v), DTYPES[dtype], _ptr(sm), sm.shape[0], hkv, hd, _ptr(k_codes),
+    nb, bs = k_codes.shape[:2]
+    assert k_codes.shape == (nb, bs, hkv, hd) and k_scales.shape == (nb, hkv, bs)
+    lib().oracle_write_kv_fp8(_ptr(k), _ptr(v), DTYPES[dtype], _ptr(sm), sm.shape[0], hkv, hd, bs, _ptr(k_codes),
                               _ptr(v_codes), _ptr(k_scales), _ptr(v_scales))
 
 
@@ -220,7 +222,7 @@ def paged_attention_fp8(q, q_dtype: str, k_codes, v_codes, k_scales, v_scales, b
     qsl = _c(query_start_loc, np.int32)
     total_q, hq, hd = q.shape
     nb, bs, hkv, hd2 = kc.shape
-    assert hd2 == hd and hq % hkv == 0 and ks.shape == (nb, bs, hkv)
+    assert hd2 == hd and hq % hkv == 0 and ks.shape == (nb, hkv, bs) and vs.shape == ks.shape
     out = np.full((total_q, hq, hd), np.nan, dtype=np.float64)
     lib().oracle_paged_attention_fp8(_ptr(out), _ptr(q), DTYPES[q_dtype], _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
                                      _ptr(bt), bt.shape[1], _ptr(sl), _ptr(qsl), sl.shape[0], hq, hkv, hd, bs,

@@ -231,18 +231,23 @@ void oracle_quant_rows(const void* src, int dtype, int64_t n_rows, int32_t row_l
 
 /* The quantizing write: token i's K and V rows ([n, num_kv_heads, head_dim]
  * in `dtype`) go, one (token, KV head) row at a time, to codes at
- * (slot * num_kv_heads + h) * head_dim and scales at slot * num_kv_heads + h;
- * negative slots are skipped. */
+ * (slot * num_kv_heads + h) * head_dim -- the cache layout -- and to the
+ * scale at ((slot / block_size) * num_kv_heads + h) * block_size +
+ * slot % block_size: scales are laid out [num_blocks, num_kv_heads,
+ * block_size], so the scales of one KV head within one block are
+ * contiguous.  Negative slots are skipped. */
 void oracle_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
-                         int32_t num_kv_heads, int32_t head_dim, uint8_t* k_codes, uint8_t* v_codes,
-                         float* k_scales, float* v_scales) {
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
+                         uint8_t* v_codes, float* k_scales, float* v_scales) {
     for (int64_t i = 0; i < n; ++i) {
         const int64_t slot = slot_mapping[i];
         if (slot < 0) continue;
+        const int64_t blk = slot / block_size, off = slot % block_size;
         for (int32_t h = 0; h < num_kv_heads; ++h) {
             const int64_t src = (i * num_kv_heads + h) * head_dim, dst = slot * num_kv_heads + h;
-            quant_row(k, src, head_dim, dtype, k_codes + dst * head_dim, k_scales + dst);
-            quant_row(v, src, head_dim, dtype, v_codes + dst * head_dim, v_scales + dst);
+            const int64_t sc = (blk * num_kv_heads + h) * block_size + off;
+            quant_row(k, src, head_dim, dtype, k_codes + dst * head_dim, k_scales + sc);
+            quant_row(v, src, head_dim, dtype, v_codes + dst * head_dim, v_scales + sc);
         }
     }
 }
@@ -353,7 +358,7 @@ void oracle_paged_attention(double* out, const void* q, const void* k_cache, con
 }
 
 /* The same over a quantized cache: K and V codes [num_blocks, block_size,
- * num_kv_heads, head_dim] with scales [num_blocks, block_size, num_kv_heads];
+ * num_kv_heads, head_dim] with scales [num_blocks, num_kv_heads, block_size];
  * a key or value element reads code value x its row's scale (exact in
  * double); q (and so the output's element type) is `q_dtype`. */
 void oracle_paged_attention_fp8(double* out, const void* q, int q_dtype, const uint8_t* k_codes,
@@ -375,12 +380,14 @@ void oracle_paged_attention_fp8(double* out, const void* q, int q_dtype, const u
         double* k = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
         double* v = (double*)malloc(sizeof(double) * (size_t)(seq_len * row));
         for (int32_t t = 0; t < seq_len; ++t) {
-            const int64_t slot = (int64_t)table[t / block_size] * block_size + t % block_size;
+            const int64_t blk = table[t / block_size], off = t % block_size;
+            const int64_t slot = blk * block_size + off;
             for (int32_t h = 0; h < num_kv_heads; ++h) {
                 const int64_t r = slot * num_kv_heads + h;
+                const int64_t sc = (blk * num_kv_heads + h) * block_size + off;
                 for (int32_t d = 0; d < head_dim; ++d) {
-                    k[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(k_codes[r * head_dim + d]) * (double)k_scales[r];
-                    v[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(v_codes[r * head_dim + d]) * (double)v_scales[r];
+                    k[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(k_codes[r * head_dim + d]) * (double)k_scales[sc];
+                    v[t * row + (int64_t)h * head_dim + d] = oracle_e4m3_value(v_codes[r * head_dim + d]) * (double)v_scales[sc];
                 }
             }
         }

@@ -439,7 +439,8 @@ def test_swap_out_and_back_is_identity_and_moves_whole_blocks():
             assert np.array_equal(dev_k[l][d_new], k0[l][d_old]) and np.array_equal(dev_v[l][d_new], v0[l][d_old])
 
 
-# ---- quantized cache (FP8 E4M3 codes, one scale per token and KV head) ----
+# ---- quantized cache (FP8 E4M3 codes, one scale per token and KV head,
+#      scales laid out [num_blocks, num_kv_heads, block_size]) ----
 
 def _torch_fp8():
     import torch
@@ -511,8 +512,8 @@ def _grid_pool(rng, nb, bs, hkv, hd):
     codes = rng.integers(0, 0x7F, (nb, bs, hkv, hd)).astype(np.uint8)
     codes |= (rng.integers(0, 2, codes.shape).astype(np.uint8) << 7)
     codes[..., 0] = np.where(rng.integers(0, 2, codes.shape[:-1]) == 1, 0x7E, 0xFE)
-    scales = np.exp2(rng.integers(-9, -2, (nb, bs, hkv))).astype(np.float32)
-    vals = (oracle.e4m3_decode(codes) * scales[..., None]).astype(np.float32)
+    scales = np.exp2(rng.integers(-9, -2, (nb, hkv, bs))).astype(np.float32)  # [NB, Hkv, bs]
+    vals = (oracle.e4m3_decode(codes) * scales.transpose(0, 2, 1)[..., None]).astype(np.float32)
     return codes, scales, vals
 
 
