@@ -180,23 +180,34 @@ double oracle_e4m3_value(uint8_t c) {
     return s ? -v : v;
 }
 
-/* Nearest code to x (ties to the code with an even mantissa), |x| > 448
- * held at +-448, NaN to 0x7F: a search over the 127 finite non-negative
- * codes, whose values increase with the code. */
+/* Nearest code to x (ties to the code with an even mantissa), |x| >= 448
+ * held at +-448, NaN to 0x7F.  The 127 finite non-negative codes have
+ * values that increase with the code, so the nearest one is found by
+ * bisection for the last code whose value is <= |x|, then comparing it with
+ * the next code. */
+static double g_e4m3_table[127];
+static int g_e4m3_ready = 0;
+
 uint8_t oracle_e4m3_encode(float x) {
+    if (!g_e4m3_ready) {
+        for (int c = 0; c < 127; ++c) g_e4m3_table[c] = oracle_e4m3_value((uint8_t)c);
+        g_e4m3_ready = 1;
+    }
     if (isnan(x)) return 0x7F;
     const uint8_t sign = signbit(x) ? 0x80 : 0x00;
     const double a = fabs((double)x);
     if (a >= 448.0) return sign | 0x7E;
-    uint8_t best = 0;
-    double best_d = a;
-    for (int c = 1; c <= 0x7E; ++c) {
-        const double d = fabs(oracle_e4m3_value((uint8_t)c) - a);
-        if (d < best_d || (d == best_d && (c & 1) == 0)) {
-            best = (uint8_t)c;
-            best_d = d;
-        }
+    int lo = 0, hi = 0x7E; /* table[lo] <= a < table[hi] */
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (g_e4m3_table[mid] <= a) lo = mid;
+        else hi = mid;
     }
+    const double dl = a - g_e4m3_table[lo], dh = g_e4m3_table[hi] - a;
+    uint8_t best;
+    if (dl < dh) best = (uint8_t)lo;
+    else if (dh < dl) best = (uint8_t)hi;
+    else best = (uint8_t)((lo & 1) == 0 ? lo : hi);
     return sign | best;
 }
 
