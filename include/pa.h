@@ -64,7 +64,12 @@ typedef enum {
     PA_ERR_TIMEOUT = 6
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2 } pa_dtype;
+/* PA_FP8_E4M3: a quantized cache of 1-byte E4M3 codes (the OCP 8-bit
+ * floating-point format: 1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits, largest finite value 448, S.1111.111 = NaN).  Accepted as the pool
+ * type of pa_copy_blocks and pa_swap_blocks (which move bytes); the FP8
+ * entry points below take it implicitly. */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2, PA_FP8_E4M3 = 3 } pa_dtype;
 
 /* Library options (pa_set_option).  Global to the process, not thread-safe
  * against concurrent calls. */
@@ -130,6 +135,33 @@ PA_API pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_m
                       int32_t num_kv_heads, int32_t head_dim, int dtype, void* stream);
 
 /*
+ * pa_write_kv_fp8 -- the quantizing form of pa_write_kv, for a quantized
+ * cache.  The pages name a quantized cache (量化缓存) as one that changes the
+ * per-token KV size ("KV cache：容量推导、分页与回收", §输入放得下，输出还要留空间) and give
+ * no method; the reading implemented here: each (token, KV head) row x of
+ * k[i] (and of v[i]) is stored as E4M3 codes with one fp32 scale,
+ *   scale = max|x| / 448   (1 for an all-zero row),
+ *   code  = E4M3(x / scale), nearest with ties to even, held at +-448,
+ * the maximum and the division taken in fp32 (IEEE).  Codes go to row
+ * slot_mapping[i] of the code pools exactly where pa_write_kv puts a row; the
+ * scale of KV head h goes to
+ *   scales[(slot / block_size) * num_kv_heads + h) * block_size + slot % block_size],
+ * i.e. scales are laid out [num_blocks, num_kv_heads, block_size] so the 16
+ * scales a decode tile needs are contiguous.  A negative slot skips token i;
+ * slots must be distinct (check mode rejects duplicates and out-of-pool
+ * slots).  Bit-exact against that definition.
+ *   k, v:              device [n, num_kv_heads, head_dim] of dtype (PA_F32/BF16/F16)
+ *   slot_mapping:      device int64 [n]
+ *   k_codes, v_codes:  device uint8 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scales, v_scales: device fp32 [num_blocks, num_kv_heads, block_size]
+ * head_dim <= 256.
+ */
+PA_API pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t n,
+                                 void* k_codes, void* v_codes, float* k_scales, float* v_scales, int32_t num_blocks,
+                                 int32_t block_size, int32_t num_kv_heads, int32_t head_dim, int dtype,
+                                 void* stream);
+
+/*
  * pa_copy_blocks -- copy-on-write block copies.
  * For each layer l and pair p: block block_pairs[2p+1] of k_caches[l] and of
  * v_caches[l] receives a copy of block block_pairs[2p] (all block_size
@@ -138,6 +170,9 @@ PA_API pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_m
  * the source or destination of another pair of the same call (check mode
  * rejects that); otherwise the pairs run in any order.
  *   block_pairs: device int64 [num_pairs, 2] (src, dst)
+ * dtype may be PA_FP8_E4M3 (a quantized cache's code pools); its scale
+ * pools [num_blocks, num_kv_heads, block_size] are copied by a second call
+ * with dtype PA_F32 and head_dim 1.
  */
 #define PA_MAX_LAYERS 128
 PA_API pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
@@ -195,6 +230,32 @@ PA_API pa_status pa_decode(void* out, const void* q, const void* k_cache, const 
                     int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t num_blocks, int32_t block_size, int32_t max_context, float scale,
                     int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_fp8 -- pa_decode over a quantized cache (see pa_write_kv_fp8):
+ * a key or value element is its code's value times its (token, KV head)
+ * row's scale, and out is the decode attention of pa_decode over those
+ * values.  The cache moves half the bytes of a 16-bit cache.  On the
+ * tensor-core path (bf16/f16 q, head_dim 128 or 256, block_size 8 or a
+ * multiple of 16 up to 256, at most 16 query heads per KV head) codes are
+ * converted exactly to f16, q enters the mma as f16(q * scale * log2 e) and
+ * each softmax weight times its value scale as f16; other shapes and fp32 q
+ * run on the CUDA-core kernel in fp32.  Requires |q * scale| < 45000 on the
+ * tensor-core path (the f16 range).
+ *   out, q:            device [num_seqs, num_heads, head_dim] of dtype (PA_F32/BF16/F16)
+ *   k_codes, v_codes:  device uint8 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scales, v_scales: device fp32 [num_blocks, num_kv_heads, block_size], 16-byte aligned
+ *   workspace:         pa_decode_fp8_workspace_size(...) bytes
+ * The other arguments, the error behaviour and the split are pa_decode's.
+ */
+PA_API size_t pa_decode_fp8_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t block_size, int32_t max_context, int dtype);
+PA_API pa_status pa_decode_fp8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                               const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                               int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                               void* stream);
 
 /*
  * pa_decode_append -- one generation step of a decode batch in one call:

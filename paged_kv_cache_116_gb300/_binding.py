@@ -13,14 +13,16 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpa.so")
 
-PA_F32, PA_BF16, PA_F16 = 0, 1, 2
+PA_F32, PA_BF16, PA_F16, PA_FP8_E4M3 = 0, 1, 2, 3
 PA_OPT_CHECK_MODE, PA_OPT_DECODE_KERNEL, PA_OPT_DECODE_CTAS, PA_OPT_VARLEN_KERNEL = 0, 1, 2, 3
 DTYPE_CODE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
+# pools that only move bytes (copy, swap) may also hold E4M3 codes
+POOL_DTYPE_CODE = {**DTYPE_CODE, torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: PA_FP8_E4M3}
 
 EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
-           "pa_swap_blocks")
+           "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8")
 
 
 class PAError(RuntimeError):
@@ -51,6 +53,10 @@ def lib():
         "pa_device_status": ([ci], ci),
         "pa_slot_mapping": ([vp, i32, i32, vp, vp, i64, i32, vp, vp], ci),
         "pa_write_kv": ([vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, ci, vp], ci),
+        "pa_write_kv_fp8": ([vp, vp, vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, ci, vp], ci),
+        "pa_decode_fp8_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
+        "pa_decode_fp8": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz,
+                           vp], ci),
         "pa_copy_blocks": ([vp, vp, i32, vp, i32, i32, i32, i32, i32, ci, vp], ci),
         "pa_swap_blocks": ([vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, ci, vp], ci),
         "pa_decode_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
@@ -96,6 +102,13 @@ def _dtype(t):
         raise TypeError("unsupported dtype %s" % t.dtype)
 
 
+def _pool_dtype(t):
+    try:
+        return POOL_DTYPE_CODE[t.dtype]
+    except KeyError:
+        raise TypeError("unsupported pool dtype %s" % t.dtype)
+
+
 def _dev(*ts):
     for t in ts:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
@@ -138,17 +151,37 @@ def pa_write_kv(k, v, slot_mapping, k_cache, v_cache, stream=None):
     _check(st, "pa_write_kv")
 
 
+def pa_write_kv_fp8(k, v, slot_mapping, k_codes, v_codes, k_scales, v_scales, stream=None):
+    """Quantizing write: rows of k, v [N, Hkv, hd] -> E4M3 codes [NB, bs, Hkv, hd] (uint8) at
+    slot_mapping [N] and one fp32 scale per row in scales [NB, Hkv, bs]."""
+    _dev(k, v, slot_mapping, k_codes, v_codes, k_scales, v_scales)
+    nb, bs, hkv, hd = k_codes.shape
+    if tuple(k_scales.shape) != (nb, hkv, bs) or tuple(v_scales.shape) != (nb, hkv, bs):
+        raise ValueError("scales must be [num_blocks, num_kv_heads, block_size]")
+    if k_scales.dtype != torch.float32 or v_scales.dtype != torch.float32:
+        raise TypeError("scales must be float32")
+    st = lib().pa_write_kv_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), slot_mapping.shape[0], _ptr(k_codes),
+                               _ptr(v_codes), _ptr(k_scales), _ptr(v_scales), nb, bs, hkv, hd, _dtype(k),
+                               _stream(stream))
+    _check(st, "pa_write_kv_fp8")
+
+
 def pa_copy_blocks(k_caches, v_caches, block_pairs, stream=None):
-    """Copy block pairs [P, 2] (src, dst) in every layer's K and V cache."""
+    """Copy block pairs [P, 2] (src, dst) in every layer's K and V cache.  Pools are
+    [NB, bs, Hkv, hd] (uint8: E4M3 codes) or a quantized cache's scales [NB, Hkv, bs]."""
     if isinstance(k_caches, torch.Tensor):
         k_caches, v_caches = [k_caches], [v_caches]
     _dev(block_pairs, *k_caches, *v_caches)
     n = len(k_caches)
     kp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in k_caches])
     vp = (ctypes.c_void_p * n)(*[c.data_ptr() for c in v_caches])
-    nb, bs, hkv, hd = k_caches[0].shape
+    if k_caches[0].dim() == 3:  # scale pools of a quantized cache: [NB, Hkv, bs]
+        nb, hkv, bs = k_caches[0].shape
+        hd = 1
+    else:
+        nb, bs, hkv, hd = k_caches[0].shape
     st = lib().pa_copy_blocks(kp, vp, n, _ptr(block_pairs), block_pairs.shape[0], nb, bs, hkv, hd,
-                              _dtype(k_caches[0]), _stream(stream))
+                              _pool_dtype(k_caches[0]), _stream(stream))
     _check(st, "pa_copy_blocks")
 
 
@@ -164,7 +197,7 @@ def pa_swap_blocks(src_k, src_v, dst_k, dst_v, block_pairs, stream=None):
     arr = lambda ts: (ctypes.c_void_p * n)(*[t.data_ptr() for t in ts])  # noqa: E731
     nbs, bs, hkv, hd = src_k[0].shape
     st = lib().pa_swap_blocks(arr(src_k), arr(src_v), arr(dst_k), arr(dst_v), n, _ptr(block_pairs),
-                              block_pairs.shape[0], nbs, dst_k[0].shape[0], bs, hkv, hd, _dtype(src_k[0]),
+                              block_pairs.shape[0], nbs, dst_k[0].shape[0], bs, hkv, hd, _pool_dtype(src_k[0]),
                               _stream(stream))
     _check(st, "pa_swap_blocks")
 
@@ -185,6 +218,27 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, max_context,
                          block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb, bs, max_context,
                          float(scale), _dtype(q), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_fp8_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, dtype):
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else dtype
+    return lib().pa_decode_fp8_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context,
+                                              code)
+
+
+def pa_decode_fp8(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, max_context, scale,
+                  workspace=None, stream=None):
+    """Decode over a quantized cache: codes [NB, bs, Hkv, hd] uint8, scales [NB, Hkv, bs] fp32;
+    out, q [S, Hq, hd] of the query type."""
+    _dev(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, workspace)
+    nb, bs, hkv, hd = k_codes.shape
+    S, hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_decode_fp8(_ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+                             _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb, bs,
+                             max_context, float(scale), _dtype(q), _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pa_decode_fp8")
     return out
 
 

@@ -70,15 +70,38 @@ pa_status check_tables(const int32_t* block_tables, int32_t num_seqs, int32_t ma
     return PA_OK;
 }
 
+// bytes_only: the call moves bytes (copy, swap), so PA_FP8_E4M3 pools are
+// accepted as well.
 pa_status check_geometry(int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
-                         int32_t block_size, int dtype) {
-    if (!valid_dtype(dtype)) return fail(PA_ERR_INVALID_ARG, "dtype must be PA_F32, PA_BF16 or PA_F16");
+                         int32_t block_size, int dtype, bool bytes_only = false) {
+    if (!valid_dtype(dtype) && !(bytes_only && dtype == PA_FP8_E4M3))
+        return fail(PA_ERR_INVALID_ARG, bytes_only ? "dtype must be PA_F32, PA_BF16, PA_F16 or PA_FP8_E4M3"
+                                                   : "dtype must be PA_F32, PA_BF16 or PA_F16");
     if (num_kv_heads <= 0 || num_heads <= 0 || head_dim <= 0 || num_blocks <= 0 || block_size <= 0)
         return fail(PA_ERR_INVALID_ARG, "head counts, head_dim, num_blocks and block_size must be positive");
     if (num_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARG, "num_heads must be a multiple of num_kv_heads");
     if ((int64_t)num_blocks * block_size > INT32_MAX)
         return fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size must fit in int32");
+    return PA_OK;
+}
+
+// Check-mode validation of a slot mapping: in the pool, or negative (skip); distinct.
+pa_status check_slots(const int64_t* slot_mapping, int64_t n, int32_t num_blocks, int32_t block_size,
+                      cudaStream_t st) {
+    pa_status err = PA_OK;
+    std::vector<int64_t> sm;
+    if (!to_host(sm, slot_mapping, n, st, &err)) return err;
+    const int64_t slots = (int64_t)num_blocks * block_size;
+    std::unordered_set<int64_t> seen;
+    for (int64_t i = 0; i < n; ++i) {
+        if (sm[i] < 0) continue;
+        if (sm[i] >= slots)
+            return fail(PA_ERR_INDEX, "token " + std::to_string(i) + ": slot " + std::to_string(sm[i]) +
+                                          " outside the pool");
+        if (!seen.insert(sm[i]).second)
+            return fail(PA_ERR_INDEX, "slot " + std::to_string(sm[i]) + " written twice in one call");
+    }
     return PA_OK;
 }
 
@@ -172,28 +195,38 @@ pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_mapping,
         return fail(PA_ERR_INVALID_ARG, "k, v and the caches must be 16-byte aligned");
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
-        pa_status err = PA_OK;
-        std::vector<int64_t> sm;
-        if (!to_host(sm, slot_mapping, n, st, &err)) return err;
-        const int64_t slots = (int64_t)num_blocks * block_size;
-        std::unordered_set<int64_t> seen;
-        for (int64_t i = 0; i < n; ++i) {
-            if (sm[i] < 0) continue;
-            if (sm[i] >= slots)
-                return fail(PA_ERR_INDEX, "token " + std::to_string(i) + ": slot " + std::to_string(sm[i]) +
-                                              " outside the pool");
-            if (!seen.insert(sm[i]).second)
-                return fail(PA_ERR_INDEX, "slot " + std::to_string(sm[i]) + " written twice in one call");
-        }
+        pa_status err = check_slots(slot_mapping, n, num_blocks, block_size, st);
+        if (err != PA_OK) return err;
     }
     cudaError_t e = pa::launch_write_kv(k, v, slot_mapping, n, k_cache, v_cache, row_bytes, st);
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_write_kv launch");
 }
 
+pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_codes,
+                          void* v_codes, float* k_scales, float* v_scales, int32_t num_blocks, int32_t block_size,
+                          int32_t num_kv_heads, int32_t head_dim, int dtype, void* stream) {
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    if (g != PA_OK) return g;
+    if (head_dim > 256) return fail(PA_ERR_UNSUPPORTED, "head_dim must be at most 256");
+    if (n < 0) return fail(PA_ERR_INVALID_ARG, "n must be non-negative");
+    if (n == 0) return PA_OK;
+    if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
+        return fail(PA_ERR_INVALID_ARG, "null pointer");
+    cudaStream_t st = as_stream(stream);
+    if (check_mode()) {
+        pa_status err = check_slots(slot_mapping, n, num_blocks, block_size, st);
+        if (err != PA_OK) return err;
+    }
+    cudaError_t e = pa::launch_write_kv_fp8(k, v, dtype, slot_mapping, n, num_kv_heads, head_dim, block_size,
+                                            static_cast<uint8_t*>(k_codes), static_cast<uint8_t*>(v_codes), k_scales,
+                                            v_scales, st);
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_write_kv_fp8 launch");
+}
+
 pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers, const int64_t* block_pairs,
                          int32_t num_pairs, int32_t num_blocks, int32_t block_size, int32_t num_kv_heads,
                          int32_t head_dim, int dtype, void* stream) {
-    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype, true);
     if (g != PA_OK) return g;
     if (num_pairs < 0) return fail(PA_ERR_INVALID_ARG, "num_pairs must be non-negative");
     if (num_layers < 1 || num_layers > PA_MAX_LAYERS)
@@ -253,7 +286,7 @@ pa_status pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* ds
                          void* stream) {
     if (num_pairs < 0 || src_num_blocks <= 0 || dst_num_blocks <= 0)
         return fail(PA_ERR_INVALID_ARG, "num_pairs must be non-negative and both pools non-empty");
-    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, src_num_blocks, block_size, dtype);
+    pa_status g = check_geometry(num_kv_heads, num_kv_heads, head_dim, src_num_blocks, block_size, dtype, true);
     if (g != PA_OK) return g;
     if (num_layers < 1 || num_layers > PA_MAX_LAYERS)
         return fail(PA_ERR_INVALID_ARG, "num_layers must be in [1, PA_MAX_LAYERS]");
@@ -296,40 +329,55 @@ pa_status pa_swap_blocks(void* const* src_k, void* const* src_v, void* const* ds
 
 // ------------------------------------------------------------------ decode
 
-static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, pa_status* st) {
+static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, bool kv_fp8, pa_status* st) {
     const int64_t want = g_options[PA_OPT_DECODE_KERNEL];
-    const bool ok = pa::decode_tc_supported(dtype, head_dim, block_size, group);
+    const bool ok = pa::decode_tc_supported(dtype, head_dim, block_size, group, kv_fp8);
     *st = PA_OK;
     if (want == 1) return false;
     if (want == 2 && !ok) {
-        *st = fail(PA_ERR_UNSUPPORTED, "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256, "
-                                       "block_size 8 or a multiple of 16 up to 256, and at most 16 query "
-                                       "heads per KV head");
+        *st = fail(PA_ERR_UNSUPPORTED, kv_fp8 ? "the tensor-core decode kernel over an FP8 cache takes bf16/f16 "
+                                                "queries, head_dim 128/256, block_size 8 or a multiple of 16 up "
+                                                "to 256, and at most 16 query heads per KV head"
+                                              : "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256, "
+                                                "block_size 8 or a multiple of 16 up to 256, and at most 16 query "
+                                                "heads per KV head");
         return false;
     }
     return ok;
 }
 
-size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t block_size, int32_t max_context, int dtype) {
+static size_t decode_workspace(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t max_context, int dtype, bool kv_fp8) {
     if (num_seqs <= 0 || num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads || max_context < 0)
         return 0;
     pa_status st;
     const int G = num_heads / num_kv_heads;
-    if (!use_decode_tc(dtype, head_dim, block_size, G, &st)) return 0;
+    if (!use_decode_tc(dtype, head_dim, block_size, G, kv_fp8, &st)) return 0;
     const int grid = pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context, dtype, G,
-                                        g_options[PA_OPT_DECODE_CTAS]);
-    return pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid);
+                                        g_options[PA_OPT_DECODE_CTAS], kv_fp8);
+    return pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid, kv_fp8);
+}
+
+size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_context, int dtype) {
+    return decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, dtype, false);
+}
+
+size_t pa_decode_fp8_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                    int32_t block_size, int32_t max_context, int dtype) {
+    return decode_workspace(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_context, dtype, true);
 }
 
 }  // extern "C"
 
+// k_scales != nullptr: the caches hold E4M3 codes with these scales.
 static pa_status decode_impl(void* out, const void* q, const void* k_new, const void* v_new, const void* k_cache,
-                             const void* v_cache, const int32_t* block_tables,
-                    int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
-                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
-                    int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
-                    void* stream) {
+                             const void* v_cache, const float* k_scales, const float* v_scales,
+                             const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                             int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                             int32_t num_blocks, int32_t block_size, int32_t max_context, float scale, int dtype,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+    const bool fp8 = k_scales != nullptr;
     pa_status g = check_geometry(num_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
     if (g != PA_OK) return g;
     if (num_seqs < 0 || max_blocks < 0 || max_context < 0)
@@ -346,6 +394,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
+    if (fp8 && (!v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+        return fail(PA_ERR_INVALID_ARG, "k_scales and v_scales must be non-null and 16-byte aligned");
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
         pa_status err = PA_OK;
@@ -372,11 +422,14 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
     a.scale = scale;
     a.causal = 1;
     a.dtype = dtype;
+    a.kv_fp8 = fp8 ? 1 : 0;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
 
     const int G = num_heads / num_kv_heads;
     const int64_t row_bytes = (int64_t)num_kv_heads * head_dim * pa::elt_size(dtype);
     pa_status sel;
-    const bool tc = use_decode_tc(dtype, head_dim, block_size, G, &sel);
+    const bool tc = use_decode_tc(dtype, head_dim, block_size, G, fp8, &sel);
     if (sel != PA_OK) return sel;
     if (!tc) {
         if (append) {  // write the new rows first, then attend from the pool
@@ -389,8 +442,8 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
         return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_decode launch");
     }
     const int grid = pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context, dtype, G,
-                                        g_options[PA_OPT_DECODE_CTAS]);
-    const size_t need = pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid);
+                                        g_options[PA_OPT_DECODE_CTAS], fp8);
+    const size_t need = pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid, fp8);
     if (workspace_bytes < need || (need && !workspace))
         return fail(PA_ERR_WORKSPACE, "workspace holds " + std::to_string(workspace_bytes) + " bytes, " +
                                           std::to_string(need) + " needed");
@@ -424,9 +477,20 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache, const void* v
                     int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
                     int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
                     void* stream) {
-    return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, block_tables, max_blocks, context_lens, num_seqs,
-                       num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context, scale, dtype,
-                       workspace, workspace_bytes, stream);
+    return decode_impl(out, q, nullptr, nullptr, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context,
+                       scale, dtype, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_fp8(void* out, const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                        const float* v_scales, const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t num_blocks, int32_t block_size, int32_t max_context, float scale,
+                        int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && (!k_scales || !v_scales)) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    return decode_impl(out, q, nullptr, nullptr, k_codes, v_codes, k_scales, v_scales, block_tables, max_blocks,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context,
+                       scale, dtype, workspace, workspace_bytes, stream);
 }
 
 pa_status pa_decode_append(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -435,9 +499,9 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                            int32_t head_dim, int32_t num_blocks, int32_t block_size, int32_t max_context,
                            float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs > 0 && (!k_new || !v_new)) return fail(PA_ERR_INVALID_ARG, "null pointer");
-    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, block_tables, max_blocks, context_lens, num_seqs,
-                       num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context, scale, dtype,
-                       workspace, workspace_bytes, stream);
+    return decode_impl(out, q, k_new, v_new, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context,
+                       scale, dtype, workspace, workspace_bytes, stream);
 }
 
 // ------------------------------------------------------------------ varlen

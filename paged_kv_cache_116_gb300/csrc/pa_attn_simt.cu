@@ -10,6 +10,12 @@
 // (lanes split head_dim), and the warps' states are merged by their
 // log-sum-exp at the end ("aiqz.cc PagedAttention", §工程实现要点: per-block
 // softmax merged online).
+//
+// With a quantized cache (FP8 E4M3 codes, one fp32 scale per token and KV
+// head, scales [num_blocks, num_kv_heads, block_size]) a key or value element
+// is its code's value times its row's scale; the row scale multiplies the
+// dot product of the codes (keys) and the softmax weight (values).
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -23,8 +29,21 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kMaxDimsPerLane = 8;  // head_dim <= 256
 
-template <typename T>
+// Cached element -> float: T itself, or (FP8) the value of an E4M3 code.
+template <typename T, bool FP8> struct CacheElt {
+    using S = T;
+    static __device__ __forceinline__ float to_f(S x) { return Elt<T>::to_f(x); }
+};
+template <typename T> struct CacheElt<T, true> {
+    using S = uint8_t;
+    static __device__ __forceinline__ float to_f(S x) {
+        return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)x, __NV_E4M3)));
+    }
+};
+
+template <typename T, bool FP8>
 __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
+    using C = CacheElt<T, FP8>;
     const int row = blockIdx.x;   // query row
     const int head = blockIdx.y;  // query head
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -53,8 +72,8 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
     const int hd = a.head_dim;
     const int64_t row_elts = (int64_t)a.num_kv_heads * hd;
     const T* q = static_cast<const T*>(a.q) + ((int64_t)row * a.num_heads + head) * hd;
-    const T* kc = static_cast<const T*>(a.k_cache) + (int64_t)kvh * hd;
-    const T* vc = static_cast<const T*>(a.v_cache) + (int64_t)kvh * hd;
+    const typename C::S* kc = static_cast<const typename C::S*>(a.k_cache) + (int64_t)kvh * hd;
+    const typename C::S* vc = static_cast<const typename C::S*>(a.v_cache) + (int64_t)kvh * hd;
     const int32_t* table = a.block_tables + (int64_t)req * a.max_blocks;
     const float scale_log2 = a.scale * 1.4426950408889634f;
 
@@ -67,26 +86,34 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
     }
     float m = -INFINITY, l = 0.f;
     for (int t = warp; t < visible; t += kWarps) {
-        const int64_t slot = (int64_t)table[t / a.block_size] * a.block_size + t % a.block_size;
-        const T* kr = kc + slot * row_elts;
+        const int64_t blk = table[t / a.block_size], off_in = t % a.block_size;
+        const int64_t slot = blk * a.block_size + off_in;
+        float ks = 1.f, vs = 1.f;
+        if constexpr (FP8) {
+            const int64_t si = (blk * a.num_kv_heads + kvh) * a.block_size + off_in;
+            ks = a.k_scales[si];
+            vs = a.v_scales[si];
+        }
+        const typename C::S* kr = kc + slot * row_elts;
         float dot = 0.f;
 #pragma unroll
         for (int k = 0; k < kMaxDimsPerLane; ++k) {
             const int d = lane + 32 * k;
-            if (d < hd) dot = fmaf(qv[k], Elt<T>::to_f(kr[d]), dot);
+            if (d < hd) dot = fmaf(qv[k], C::to_f(kr[d]), dot);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        const float x = dot * scale_log2;
+        const float x = dot * ks * scale_log2;
         const float m_new = fmaxf(m, x);
         const float corr = exp2f(m - m_new);
         const float p = exp2f(x - m_new);
         l = l * corr + p;
-        const T* vr = vc + slot * row_elts;
+        const float pv = p * vs;
+        const typename C::S* vr = vc + slot * row_elts;
 #pragma unroll
         for (int k = 0; k < kMaxDimsPerLane; ++k) {
             const int d = lane + 32 * k;
-            if (d < hd) acc[k] = fmaf(p, Elt<T>::to_f(vr[d]), acc[k] * corr);
+            if (d < hd) acc[k] = fmaf(pv, C::to_f(vr[d]), acc[k] * corr);
         }
         m = m_new;
     }
@@ -128,10 +155,18 @@ bool attn_simt_supported(int dtype, int head_dim) {
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream) {
     if (a.total_q == 0) return cudaSuccess;
     dim3 grid((unsigned)a.total_q, (unsigned)a.num_heads);
+    if (a.kv_fp8) {
+        switch (a.dtype) {
+            case 0: attn_simt_kernel<float, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
+            case 1: attn_simt_kernel<__nv_bfloat16, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
+            default: attn_simt_kernel<__half, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
+        }
+        return cudaGetLastError();
+    }
     switch (a.dtype) {
-        case 0: attn_simt_kernel<float><<<grid, kWarps * 32, 0, stream>>>(a); break;
-        case 1: attn_simt_kernel<__nv_bfloat16><<<grid, kWarps * 32, 0, stream>>>(a); break;
-        default: attn_simt_kernel<__half><<<grid, kWarps * 32, 0, stream>>>(a); break;
+        case 0: attn_simt_kernel<float, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
+        case 1: attn_simt_kernel<__nv_bfloat16, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
+        default: attn_simt_kernel<__half, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
     }
     return cudaGetLastError();
 }

@@ -1,10 +1,12 @@
 // pa_copy.cu -- the byte-moving kernels of the path: slot translation, the
-// slot-mapped K/V row write, and the copy-on-write block copy.
+// slot-mapped K/V row write (plain, or quantizing into an FP8 cache), and the
+// copy-on-write block copy.
 //
 // All three are HBM-bound moves.  Rows and blocks are moved as 16-byte
 // vectors (rows are required to be multiples of 16 bytes), one warp per row
 // or a whole CTA per block pair, so every warp instruction touches whole
 // 32-byte sectors.
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -79,6 +81,50 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     const uint4* src = ((warp & 1) ? v_new : k_new) + s * row_vecs;
     uint4* dst = ((warp & 1) ? v_cache : k_cache) + slot * row_vecs;
     for (int64_t e = lane; e < row_vecs; e += 32) dst[e] = ld_nc_v4(src + e);
+}
+
+// Quantizing write: one warp per (token, KV head, K|V) row of head_dim <=
+// 256 elements.  scale = max|x| / 448 (1 for an all-zero row), code =
+// E4M3(x / scale), nearest with ties to even, held at +-448; the division
+// and maximum in fp32 (IEEE).  The codes go to the row's slot of the code
+// pool, the scale to [slot / block_size][head][slot % block_size].
+constexpr int kQuantWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    write_kv_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, const int64_t* __restrict__ slots,
+                        int64_t n, int32_t hkv, int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes,
+                        uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;  // ((token * hkv + head) * 2 + K|V)
+    if (item >= n * hkv * 2) return;
+    const int is_v = (int)(item & 1);
+    const int64_t row = item >> 1, token = row / hkv;
+    const int32_t h = (int32_t)(row - token * hkv);
+    const int64_t slot = slots[token];
+    if (slot < 0) return;
+    const T* src = (is_v ? v : k) + row * hd;
+    float x[8], amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int d = lane + 32 * j;
+        x[j] = d < hd ? Elt<T>::to_f(src[d]) : 0.f;
+        amax = fmaxf(amax, fabsf(x[j]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    uint8_t* dst = (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int d = lane + 32 * j;
+        if (d < hd) dst[d] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3);
+    }
+    if (lane == 0) {
+        const int64_t blk = slot / bs;
+        (is_v ? v_scales : k_scales)[(blk * hkv + h) * bs + (slot - blk * bs)] = s;
+    }
 }
 
 // One CTA per (pair, layer); its threads stride over the K and V blocks.
@@ -195,6 +241,25 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t
     append_kv_kernel<<<(unsigned)((num_seqs + per_cta - 1) / per_cta), kWriteWarps * 32, 0, stream>>>(
         static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, max_blocks, context_lens,
         num_seqs, block_size, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), row_bytes / 16);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
+                                uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    const int64_t rows = n * num_kv_heads * 2;
+    const unsigned blocks = (unsigned)((rows + kQuantWarps - 1) / kQuantWarps);
+#define PA_QW(T)                                                                                               \
+    write_kv_fp8_kernel<T><<<blocks, kQuantWarps * 32, 0, stream>>>(                                         \
+        static_cast<const T*>(k), static_cast<const T*>(v), slot_mapping, n, num_kv_heads, head_dim, block_size, \
+        k_codes, v_codes, k_scales, v_scales)
+    switch (dtype) {
+        case 0: PA_QW(float); break;
+        case 1: PA_QW(__nv_bfloat16); break;
+        default: PA_QW(__half); break;
+    }
+#undef PA_QW
     return cudaGetLastError();
 }
 

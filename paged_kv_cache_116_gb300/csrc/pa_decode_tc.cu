@@ -30,6 +30,19 @@
 //    movmatrix and O^T += V^T P^T accumulates in fp32 registers.
 //  * Tokens past L in a sequence's last block are masked (scores to -inf,
 //    V operand lanes to zero) so whatever the unused slots hold never leaks.
+//  * Quantized cache (FP8 E4M3 codes, one fp32 scale per token and KV head,
+//    scales laid out [num_blocks, num_kv_heads, block_size]; the handbook-
+//    adjacent "KV cache：容量推导、分页与回收" names a quantized cache as a
+//    per-token size change): the tiles are 1-byte codes (half the bytes of a
+//    16-bit cache) and a 1-D bulk copy brings the tile's 16 K and 16 V scales
+//    with them.  Codes convert exactly to f16 (cvt e4m3x2 -> f16x2) and feed
+//    the same f16 mma.  A key's scale multiplies its score row after the mma;
+//    a value's scale multiplies its softmax weight before P is rounded to the
+//    f16 operand (the normaliser sums the unscaled weights).  The query is
+//    taken as f16(q * scale * log2 e).  The head_dim order inside each mma
+//    k-step (keys) and m-tile (values) is permuted -- consistently on both
+//    operands, since a dot product does not depend on its order -- so every
+//    lane reads contiguous 16-byte pieces of the staged codes.
 //  * Append mode fuses the generation step: the warp that owns a unit's
 //    last block patches the new token's K/V row (prefetched from the inputs)
 //    into the staged tile before its MMAs and stores the same row to the pool
@@ -37,6 +50,7 @@
 //    slot mapping) -- slot translation, write and attention in one launch.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -77,37 +91,61 @@ struct TcParams {
     void* k_pool;
     void* v_pool;
     int32_t block_size;  // tokens per pool block: 8, or a multiple of 16 up to 256
+    // quantized cache only: fp32 scales [num_blocks, num_kv_heads, block_size]
+    const float* k_scales;
+    const float* v_scales;
 };
 
-template <int HD>
+template <int HD, bool FP8>
 struct Geo {
-    static constexpr int CH = HD * 2 / 128;   // 128-byte chunks in one head's row
-    static constexpr int TILE = BS * HD * 2;  // bytes of a K (or V) tile
-    static constexpr int STAGE = 2 * TILE;    // K tile then V tile
-    static constexpr int KS = HD / 16;        // k-steps of K Q^T == m-tiles of V^T P^T
+    static constexpr int ELT = FP8 ? 1 : 2;     // bytes per cached element
+    static constexpr int CH = HD * ELT / 128;   // 128-byte chunks in one head's row
+    static constexpr int TILE = BS * HD * ELT;  // bytes of a K (or V) tile
+    static constexpr int STAGE = 2 * TILE;      // K tile then V tile
+    static constexpr int SCL = FP8 ? 2 * BS * 4 : 0;  // a stage's 16 K then 16 V scales
+    static constexpr int KS = HD / 16;          // k-steps of K Q^T == m-tiles of V^T P^T
 };
 
-// Warps per CTA and stages per warp for each head_dim.
-template <int HD> struct Pipe;
-template <> struct Pipe<64> { static constexpr int NW = 4, R = 6; };
-template <> struct Pipe<128> { static constexpr int NW = 4, R = 3; };
-template <> struct Pipe<256> { static constexpr int NW = 2, R = 3; };
+// Warps per CTA and stages per warp.
+template <int HD, bool FP8> struct Pipe;
+template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6; };
+template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3; };
+template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3; };
+template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 6; };
+template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3; };
 
-template <int HD>
+template <int HD, bool FP8>
 constexpr size_t smem_bytes(int num_seqs) {
-    return 1024 /* alignment slack */ + (size_t)Pipe<HD>::NW * Pipe<HD>::R * (Geo<HD>::STAGE + 8) +
+    return 1024 /* alignment slack */ +
+           (size_t)Pipe<HD, FP8>::NW * Pipe<HD, FP8>::R * (Geo<HD, FP8>::STAGE + Geo<HD, FP8>::SCL + 8) +
            (size_t)(num_seqs + 1) * 4;
 }
 
-template <typename T, int HD, int NT>
-__global__ void __launch_bounds__(Pipe<HD>::NW * 32)
+// Two E4M3 codes (low byte first) -> two f16 values (low half first), exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// T: element type of q and out.  FP8: the cache holds E4M3 codes plus
+// scales (the mma then runs in f16 whatever T is).
+template <typename T, int HD, int NT, bool FP8>
+__global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const TcParams p) {
-    using Gm = Geo<HD>;
-    constexpr int NW = Pipe<HD>::NW, R = Pipe<HD>::R, KS = Gm::KS;
+    using Gm = Geo<HD, FP8>;
+    constexpr int NW = Pipe<HD, FP8>::NW, R = Pipe<HD, FP8>::R, KS = Gm::KS;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * Gm::STAGE);
+    float* scl = reinterpret_cast<float*>(base + (size_t)NW * R * Gm::STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * (Gm::STAGE + Gm::SCL));
     int32_t* prefix = reinterpret_cast<int32_t*>(bars + NW * R);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -165,6 +203,7 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
 
     uint64_t* wbar = bars + warp * R;
     uint8_t* wst = base + (size_t)warp * R * Gm::STAGE;
+    float* wscl = scl + (size_t)warp * R * (Gm::SCL / 4);
     if (lane == 0) {
         for (int r = 0; r < R; ++r) mbar_init(&wbar[r], 1);
         mbar_fence_init();
@@ -225,7 +264,22 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         if (lane == 0) {
             uint8_t* dst = wst + (size_t)slot * Gm::STAGE;
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE);
+            mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE + Gm::SCL);
+            if constexpr (FP8) {
+                // scale of pool row r for KV head ih: [r / bs][ih][r % bs]
+                float* sd = wscl + slot * (Gm::SCL / 4);
+                const int64_t i1 = (int64_t)(row / bsz) * Hkv * bsz + (int64_t)ih * bsz + row % bsz;
+                if (bsz == 8) {
+                    const int64_t i2 = (int64_t)(row2 / 8) * Hkv * 8 + (int64_t)ih * 8 + row2 % 8;
+                    bulk_load(sd, p.k_scales + i1, 32, &wbar[slot]);
+                    bulk_load(sd + 8, p.k_scales + i2, 32, &wbar[slot]);
+                    bulk_load(sd + BS, p.v_scales + i1, 32, &wbar[slot]);
+                    bulk_load(sd + BS + 8, p.v_scales + i2, 32, &wbar[slot]);
+                } else {
+                    bulk_load(sd, p.k_scales + i1, 64, &wbar[slot]);
+                    bulk_load(sd + BS, p.v_scales + i1, 64, &wbar[slot]);
+                }
+            }
 #pragma unroll
             for (int c = 0; c < Gm::CH; ++c) {
                 if (bsz == 8) {  // two 8-row boxes, each a 1024-byte swizzle atom
@@ -282,6 +336,13 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
     bool first_seg = true;
     const T* qbase = static_cast<const T*>(p.q);
 
+    // Quantized cache: lane (g, c4) takes head dims [c4 HD/4, (c4+1) HD/4) of
+    // key rows g and g+8, four per k-step (k-step kk: the mma's k pair
+    // 2c4, 2c4+1 holds dims kb0 + 4kk, +1 and the pair 2c4+8, +9 holds
+    // dims kb0 + 4kk + 2, +3), and head dims [g HD/8, (g+1) HD/8) of value
+    // rows 2c4, 2c4+1, 2c4+8, 2c4+9 (m-tile mt, row g + 8hi: dim vb0 + 2mt + hi).
+    const int kb0 = c4 * (HD / 4), vb0 = g * (HD / 8);
+
     auto begin_unit = [&]() {
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk)
@@ -289,9 +350,18 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
             for (int nt = 0; nt < NT; ++nt) {
                 const int hh = nt * 8 + g;
                 if (hh < G) {
-                    const T* qp = qbase + (((int64_t)cs * p.num_heads + ch * G + hh) * HD + kk * 16 + 2 * c4);
-                    qb[kk][nt][0] = *reinterpret_cast<const uint32_t*>(qp);
-                    qb[kk][nt][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+                    const T* qrow = qbase + ((int64_t)cs * p.num_heads + ch * G + hh) * HD;
+                    if constexpr (FP8) {
+                        float x[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) x[e] = Elt<T>::to_f(qrow[kb0 + 4 * kk + e]) * p.scale_log2;
+                        qb[kk][nt][0] = pack2<__half>(x[0], x[1]);
+                        qb[kk][nt][1] = pack2<__half>(x[2], x[3]);
+                    } else {
+                        const T* qp = qrow + kk * 16 + 2 * c4;
+                        qb[kk][nt][0] = *reinterpret_cast<const uint32_t*>(qp);
+                        qb[kk][nt][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+                    }
                 } else {
                     qb[kk][nt][0] = qb[kk][nt][1] = 0u;
                 }
@@ -303,7 +373,7 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
         }
-        if (p.k_new != nullptr) {
+        if (!FP8 && p.k_new != nullptr) {
 #pragma unroll
             for (int k = 0; k < NPC; ++k) {
                 const int i = lane + 32 * k;
@@ -353,6 +423,9 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         }
     };
 
+    // head dim of accumulator row g + 8 hi of m-tile mt
+    auto odim = [&](int mt, int hi) -> int { return FP8 ? vb0 + 2 * mt + hi : mt * 16 + g + 8 * hi; };
+
     auto finalize = [&](int bend, int nb) {
         float lt[NT][2];
 #pragma unroll
@@ -377,8 +450,8 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                         const float inv = 1.f / lt[nt][e];
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
-                            out[hh * HD + mt * 16 + g] = Elt<T>::from_f(acc[mt][nt][e] * inv);
-                            out[hh * HD + mt * 16 + g + 8] = Elt<T>::from_f(acc[mt][nt][2 + e] * inv);
+                            out[hh * HD + odim(mt, 0)] = Elt<T>::from_f(acc[mt][nt][e] * inv);
+                            out[hh * HD + odim(mt, 1)] = Elt<T>::from_f(acc[mt][nt][2 + e] * inv);
                         }
                     }
                 }
@@ -394,8 +467,8 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                         float* r = rec + hh * (HD + 4);
 #pragma unroll
                         for (int mt = 0; mt < KS; ++mt) {
-                            r[mt * 16 + g] = acc[mt][nt][e];
-                            r[mt * 16 + g + 8] = acc[mt][nt][2 + e];
+                            r[odim(mt, 0)] = acc[mt][nt][e];
+                            r[odim(mt, 1)] = acc[mt][nt][2 + e];
                         }
                         if (g == 0) {
                             r[HD] = mrow[nt][e];
@@ -441,7 +514,7 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         }
         const uint32_t kt = st0 + (uint32_t)slot * Gm::STAGE, vt = kt + Gm::TILE;
         const int valid = min(BS, Lcur - cb * BS);
-        if (p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
+        if (!FP8 && p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
             // the new token: into the staged tiles (its attention input) and the pool
             const int r = valid - 1;
             const int64_t slot_row = (int64_t)last_phys * bsz + (Lcur - 1) % bsz;
@@ -465,23 +538,56 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
         float sc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        if constexpr (FP8) {
+            constexpr int KP = HD / 64;  // 16-byte pieces of a lane's key bytes per row
+            uint4 kw[2][KP];
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(kt + swz(k_tok, kk * 16 + k_dof), a0, a1, a2, a3);
+            for (int hi = 0; hi < 2; ++hi)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+                for (int u = 0; u < KP; ++u) {
+                    const int r = g + 8 * hi, b = kb0 + 16 * u;
+                    const uint32_t a = kt + (b >> 7) * BS * 128 + r * 128 + ((((b & 127) >> 4) ^ (r & 7)) << 4);
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(kw[hi][u].x), "=r"(kw[hi][u].y), "=r"(kw[hi][u].z), "=r"(kw[hi][u].w)
+                                 : "r"(a));
+                }
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const uint32_t w0 = (&kw[0][kk >> 2].x)[kk & 3], w1 = (&kw[1][kk >> 2].x)[kk & 3];
+                const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
+                const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma16816<__half>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+            }
+        } else {
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(kt + swz(k_tok, kk * 16 + k_dof), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+            }
         }
 
         // online softmax over this block (exp2 domain)
         const bool ok0 = g < valid, ok1 = g + 8 < valid;
+        // score multipliers of rows g, g+8 and (quantized cache) value scales
+        float sm0 = p.scale_log2, sm1 = p.scale_log2, vs0 = 1.f, vs1 = 1.f;
+        if constexpr (FP8) {
+            const float* ss = wscl + slot * (Gm::SCL / 4);
+            sm0 = ss[g];
+            sm1 = ss[g + 8];
+            vs0 = ok0 ? ss[BS + g] : 0.f;  // a slot past the context may hold anything
+            vs1 = ok1 ? ss[BS + g + 8] : 0.f;
+        }
         uint32_t pb[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float x0 = ok0 ? sc[nt][0] * p.scale_log2 : -INFINITY;
-            const float x1 = ok0 ? sc[nt][1] * p.scale_log2 : -INFINITY;
-            const float x2 = ok1 ? sc[nt][2] * p.scale_log2 : -INFINITY;
-            const float x3 = ok1 ? sc[nt][3] * p.scale_log2 : -INFINITY;
+            const float x0 = ok0 ? sc[nt][0] * sm0 : -INFINITY;
+            const float x1 = ok0 ? sc[nt][1] * sm0 : -INFINITY;
+            const float x2 = ok1 ? sc[nt][2] * sm1 : -INFINITY;
+            const float x3 = ok1 ? sc[nt][3] * sm1 : -INFINITY;
             float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -503,8 +609,13 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
                 acc[mt][nt][2] *= al0;
                 acc[mt][nt][3] *= al1;
             }
-            pb[nt][0] = movm_t(pack2<T>(p0, p1));
-            pb[nt][1] = movm_t(pack2<T>(p2, p3));
+            if constexpr (FP8) {
+                pb[nt][0] = movm_t(pack2<__half>(p0 * vs0, p1 * vs0));
+                pb[nt][1] = movm_t(pack2<__half>(p2 * vs1, p3 * vs1));
+            } else {
+                pb[nt][0] = movm_t(pack2<T>(p0, p1));
+                pb[nt][1] = movm_t(pack2<T>(p2, p3));
+            }
         }
 
         // O^T += V^T P^T
@@ -513,16 +624,46 @@ __global__ void __launch_bounds__(Pipe<HD>::NW * 32)
             m01 = (2 * c4 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 1 < valid ? 0xffff0000u : 0u);
             m23 = (2 * c4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 9 < valid ? 0xffff0000u : 0u);
         }
+        if constexpr (FP8) {
+            constexpr int VP = HD / 128;  // 16-byte pieces of a lane's value bytes per row
+            uint4 vw[4][VP];              // rows 2c4, 2c4+1, 2c4+8, 2c4+9
 #pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vt + swz(v_tok, mt * 16 + v_dof), a0, a1, a2, a3);
-            a0 &= m01;
-            a1 &= m01;
-            a2 &= m23;
-            a3 &= m23;
+            for (int t = 0; t < 4; ++t)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+                for (int u = 0; u < VP; ++u) {
+                    const int r = 2 * c4 + (t & 1) + 8 * (t >> 1), b = vb0 + 16 * u;
+                    const uint32_t a = vt + (b >> 7) * BS * 128 + r * 128 + ((((b & 127) >> 4) ^ (r & 7)) << 4);
+                    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                 : "=r"(vw[t][u].x), "=r"(vw[t][u].y), "=r"(vw[t][u].z), "=r"(vw[t][u].w)
+                                 : "r"(a));
+                }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                // dims vb0 + 2mt (row g) and + 1 (row g+8): bytes 2mt, 2mt+1 of the lane's value bytes,
+                // interleaved token pair by token pair
+                const int wi = (2 * mt) >> 2;
+                const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                const uint32_t w0 = (&vw[0][wi >> 2].x)[wi & 3], w1 = (&vw[1][wi >> 2].x)[wi & 3];
+                const uint32_t w8 = (&vw[2][wi >> 2].x)[wi & 3], w9 = (&vw[3][wi >> 2].x)[wi & 3];
+                const uint32_t lo = __byte_perm(w0, w1, sel), hi = __byte_perm(w8, w9, sel);
+                const uint32_t a0 = e4m3x2_to_f16x2(lo) & m01, a1 = e4m3x2_to_f16x2(lo >> 16) & m01;
+                const uint32_t a2 = e4m3x2_to_f16x2(hi) & m23, a3 = e4m3x2_to_f16x2(hi >> 16) & m23;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma16816<__half>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
+        } else {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vt + swz(v_tok, mt * 16 + v_dof), a0, a1, a2, a3);
+                a0 &= m01;
+                a1 &= m01;
+                a2 &= m23;
+                a3 &= m23;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            }
         }
         __syncwarp();
         if (ip < n) issue_next();
@@ -571,23 +712,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// The cache as a 3-D tensor: 64 elements (128 bytes) x (Hkv * CH) 128-byte
-// chunks of a token row x num_blocks * 16 token rows; one box = one chunk of
-// one KV head over the 16 rows of a block.
-bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, int num_blocks, int block_size, int num_kv_heads,
-                 int head_dim, std::string* err) {
+// The cache as a 3-D tensor: 128 bytes (64 16-bit elements, or 128 E4M3
+// codes) x (Hkv * CH) 128-byte chunks of a token row x num_blocks *
+// block_size token rows; one box = one chunk of one KV head over the 16 (or
+// 8) rows of a block.
+bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, bool fp8, int num_blocks, int block_size,
+                 int num_kv_heads, int head_dim, std::string* err) {
     auto fn = encode_fn();
     if (!fn) {
         *err = "cuTensorMapEncodeTiled is not available from the driver";
         return false;
     }
-    const int ch = head_dim * 2 / 128;
-    cuuint64_t dims[3] = {64, (cuuint64_t)num_kv_heads * ch, (cuuint64_t)num_blocks * block_size};
-    cuuint64_t strides[2] = {128, (cuuint64_t)num_kv_heads * head_dim * 2};
-    cuuint32_t box[3] = {64, 1, (cuuint32_t)(block_size == 8 ? 8 : BS)};
+    const int elt = fp8 ? 1 : 2;
+    const int ch = head_dim * elt / 128, inner = 128 / elt;
+    cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)num_kv_heads * ch, (cuuint64_t)num_blocks * block_size};
+    cuuint64_t strides[2] = {128, (cuuint64_t)num_kv_heads * head_dim * elt};
+    cuuint32_t box[3] = {(cuuint32_t)inner, 1, (cuuint32_t)(block_size == 8 ? 8 : BS)};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                    const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+    const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                       : (dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUresult r = fn(m, ty, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
@@ -596,36 +740,36 @@ bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, int num_blocks, i
     return true;
 }
 
-template <typename T, int HD, int NT>
+template <typename T, int HD, int NT, bool FP8>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT>);
+    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8>);
 }
 
-template <int HD>
+template <int HD, bool FP8>
 int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t max_context, int64_t override_ctas) {
     // the per-unit count holds up to 65535 partials: keep the grid's warps below that
     if (override_ctas > 0) return (int)(override_ctas < 16000 ? override_ctas : 16000);
     int dev = 0, sms = 0, occ = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const size_t smem = smem_bytes<HD>(num_seqs);
+    const size_t smem = smem_bytes<HD, FP8>(num_seqs);
     cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, Pipe<HD>::NW * 32, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kfn, Pipe<HD, FP8>::NW * 32, smem);
     if (occ < 1) occ = 1;
     int64_t grid = (int64_t)sms * occ;
     // at least two blocks per warp on average when every context is max_context long
     const int64_t wmax = (int64_t)num_seqs * num_kv_heads * ((max_context + BS - 1) / BS);
-    const int64_t cap = (wmax + 2 * Pipe<HD>::NW - 1) / (2 * Pipe<HD>::NW);
+    const int64_t cap = (wmax + 2 * Pipe<HD, FP8>::NW - 1) / (2 * Pipe<HD, FP8>::NW);
     if (grid > cap) grid = cap;
     return (int)(grid < 1 ? 1 : grid);
 }
 
-template <typename T, int HD, int NT>
+template <typename T, int HD, int NT, bool FP8>
 cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* workspace, std::string* err,
                          cudaStream_t stream) {
     CUtensorMap tmK, tmV;
-    if (!make_kv_map(&tmK, a.k_cache, a.dtype, num_blocks, a.block_size, a.num_kv_heads, HD, err) ||
-        !make_kv_map(&tmV, a.v_cache, a.dtype, num_blocks, a.block_size, a.num_kv_heads, HD, err))
+    if (!make_kv_map(&tmK, a.k_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err) ||
+        !make_kv_map(&tmV, a.v_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err))
         return cudaErrorInvalidValue;
     TcParams p;
     p.out = a.out;
@@ -647,16 +791,18 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.k_pool = const_cast<void*>(a.k_cache);
     p.v_pool = const_cast<void*>(a.v_cache);
     p.block_size = a.block_size;
+    p.k_scales = a.k_scales;
+    p.v_scales = a.v_scales;
 
-    const void* kfn = kernel_ptr<T, HD, NT>();
-    const size_t smem = smem_bytes<HD>(a.num_seqs);
+    const void* kfn = kernel_ptr<T, HD, NT, FP8>();
+    const size_t smem = smem_bytes<HD, FP8>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // programmatic dependent launch: the grid may be scheduled while the
     // previous kernel on the stream finishes; the kernel waits for it first
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(Pipe<HD>::NW * 32);
+    cfg.blockDim = dim3(Pipe<HD, FP8>::NW * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -664,7 +810,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT>, tmK, tmV, p);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8>, tmK, tmV, p);
 }
 
 template <typename T>
@@ -672,43 +818,59 @@ cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* 
                          cudaStream_t st) {
     const int G = a.num_heads / a.num_kv_heads;
     const bool two = G > 8;
+    if (a.kv_fp8) {
+        if (a.head_dim == 128)
+            return two ? launch_typed<T, 128, 2, true>(a, num_blocks, grid, ws, err, st)
+                       : launch_typed<T, 128, 1, true>(a, num_blocks, grid, ws, err, st);
+        return two ? launch_typed<T, 256, 2, true>(a, num_blocks, grid, ws, err, st)
+                   : launch_typed<T, 256, 1, true>(a, num_blocks, grid, ws, err, st);
+    }
     switch (a.head_dim) {
-        case 64: return two ? launch_typed<T, 64, 2>(a, num_blocks, grid, ws, err, st)
-                            : launch_typed<T, 64, 1>(a, num_blocks, grid, ws, err, st);
-        case 128: return two ? launch_typed<T, 128, 2>(a, num_blocks, grid, ws, err, st)
-                             : launch_typed<T, 128, 1>(a, num_blocks, grid, ws, err, st);
-        default: return two ? launch_typed<T, 256, 2>(a, num_blocks, grid, ws, err, st)
-                            : launch_typed<T, 256, 1>(a, num_blocks, grid, ws, err, st);
+        case 64: return two ? launch_typed<T, 64, 2, false>(a, num_blocks, grid, ws, err, st)
+                            : launch_typed<T, 64, 1, false>(a, num_blocks, grid, ws, err, st);
+        case 128: return two ? launch_typed<T, 128, 2, false>(a, num_blocks, grid, ws, err, st)
+                             : launch_typed<T, 128, 1, false>(a, num_blocks, grid, ws, err, st);
+        default: return two ? launch_typed<T, 256, 2, false>(a, num_blocks, grid, ws, err, st)
+                            : launch_typed<T, 256, 1, false>(a, num_blocks, grid, ws, err, st);
     }
 }
 
 }  // namespace
 
-bool decode_tc_supported(int dtype, int head_dim, int block_size, int group) {
-    return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128 || head_dim == 256) &&
-           (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) && group >= 1 && group <= 16;
+bool decode_tc_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8) {
+    const bool hd_ok = kv_fp8 ? (head_dim == 128 || head_dim == 256)
+                              : (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    return (dtype == 1 || dtype == 2) && hd_ok && (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) &&
+           group >= 1 && group <= 16;
 }
 
 int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override) {
+                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override, bool kv_fp8) {
     (void)block_size;
     const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
     const bool two = group > 8;
     const bool bf = dtype == 1;
-#define PA_KFN(HD)                                                                                      \
-    (bf ? (two ? kernel_ptr<__nv_bfloat16, HD, 2>() : kernel_ptr<__nv_bfloat16, HD, 1>())              \
-        : (two ? kernel_ptr<__half, HD, 2>() : kernel_ptr<__half, HD, 1>()))
+#define PA_KFN(HD, F8)                                                                                      \
+    (bf ? (two ? kernel_ptr<__nv_bfloat16, HD, 2, F8>() : kernel_ptr<__nv_bfloat16, HD, 1, F8>())          \
+        : (two ? kernel_ptr<__half, HD, 2, F8>() : kernel_ptr<__half, HD, 1, F8>()))
+    if (kv_fp8) {
+        if (head_dim == 128) return grid_for<128, true>(PA_KFN(128, true), s, num_kv_heads, max_context, ctas_override);
+        return grid_for<256, true>(PA_KFN(256, true), s, num_kv_heads, max_context, ctas_override);
+    }
     switch (head_dim) {
-        case 64: return grid_for<64>(PA_KFN(64), s, num_kv_heads, max_context, ctas_override);
-        case 128: return grid_for<128>(PA_KFN(128), s, num_kv_heads, max_context, ctas_override);
-        default: return grid_for<256>(PA_KFN(256), s, num_kv_heads, max_context, ctas_override);
+        case 64: return grid_for<64, false>(PA_KFN(64, false), s, num_kv_heads, max_context, ctas_override);
+        case 128: return grid_for<128, false>(PA_KFN(128, false), s, num_kv_heads, max_context, ctas_override);
+        default: return grid_for<256, false>(PA_KFN(256, false), s, num_kv_heads, max_context, ctas_override);
     }
 #undef PA_KFN
 }
 
-size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas) {
+size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
+                           bool kv_fp8) {
     const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
-    const int nw = head_dim == 256 ? Pipe<256>::NW : (head_dim == 128 ? Pipe<128>::NW : Pipe<64>::NW);
+    int nw;
+    if (kv_fp8) nw = head_dim == 256 ? Pipe<256, true>::NW : Pipe<128, true>::NW;
+    else nw = head_dim == 256 ? Pipe<256, false>::NW : (head_dim == 128 ? Pipe<128, false>::NW : Pipe<64, false>::NW);
     const size_t cnt_bytes = ((size_t)s * num_kv_heads * 8 + 255) & ~(size_t)255;
     return cnt_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
 }

@@ -10,8 +10,8 @@
 
 namespace pa {
 
-// Element size of a pa_dtype (PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2).
-inline int elt_size(int dtype) { return dtype == 0 ? 4 : 2; }
+// Element size of a pa_dtype (PA_F32 = 0, PA_BF16 = 1, PA_F16 = 2, PA_FP8_E4M3 = 3).
+inline int elt_size(int dtype) { return dtype == 0 ? 4 : (dtype == 3 ? 1 : 2); }
 
 // Upper limit of sequences one tensor-core decode launch handles (its
 // per-sequence block-count prefix lives in shared memory); the C ABI splits
@@ -42,6 +42,12 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t
 cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* const* dst_k, void* const* dst_v,
                                int32_t num_layers, const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
                                cudaStream_t stream);
+// Quantizing write: each (token, KV head) row of k / v ([n, Hkv, hd] of
+// dtype) becomes E4M3 codes at its slot of k_codes / v_codes and one fp32
+// scale in k_scales / v_scales [num_blocks, Hkv, block_size].
+cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
+                                int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
+                                uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                                const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
                                cudaStream_t stream);
@@ -70,16 +76,24 @@ struct AttnArgs {
     // the pool and attended from these rows (nullptr: plain decode)
     const void* k_new = nullptr;
     const void* v_new = nullptr;
+    // quantized cache: k_cache / v_cache hold E4M3 codes and these fp32
+    // scales [num_blocks, num_kv_heads, block_size]; dtype is then the type
+    // of q and out only
+    int kv_fp8 = 0;
+    const float* k_scales = nullptr;
+    const float* v_scales = nullptr;
 };
-bool attn_simt_supported(int dtype, int head_dim);
+bool attn_simt_supported(int dtype, int head_dim);  // either cache kind
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);
 
 // ---- tensor-core decode (pa_decode_tc.cu)
-bool decode_tc_supported(int dtype, int head_dim, int block_size, int group);
+// kv_fp8: the cache holds E4M3 codes with scales (AttnArgs::kv_fp8).
+bool decode_tc_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8 = false);
 // Grid size (CTAs) the launch will use for this problem on the current device.
 int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override);
-size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas);
+                   int32_t max_context, int dtype, int32_t group, int64_t ctas_override, bool kv_fp8 = false);
+size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
+                           bool kv_fp8 = false);
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
                              std::string* err, cudaStream_t stream);
 uint32_t decode_tc_status(bool clear);

@@ -94,3 +94,57 @@ def raw_bits(t):
 
 def oracle_bits(a):
     return a.view(np.uint32) if a.dtype == np.float32 else a
+
+
+# ---- quantized (FP8 E4M3) cache -------------------------------------------
+
+FP8_NAN_CODE = 0x7F
+
+
+def oracle_fp8_caches(w):
+    """Oracle code pools [NB, bs, Hkv, hd] (NaN code everywhere) and scale
+    pools [NB, Hkv, bs] (NaN everywhere) after the quantizing write of the
+    workload's cached rows and then its new rows."""
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    sshape = (w.num_blocks, w.num_kv_heads, w.block_size)
+    kc = np.full(shape, FP8_NAN_CODE, np.uint8)
+    vc = kc.copy()
+    ks = np.full(sshape, np.nan, np.float32)
+    vs = ks.copy()
+    slots = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
+    oracle.write_kv_fp8(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), w.dtype, slots, kc, vc, ks, vs)
+    slots = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
+    oracle.write_kv_fp8(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), w.dtype, slots, kc, vc, ks, vs)
+    return kc, vc, ks, vs
+
+
+def device_fp8_caches(w, dev):
+    """The same pools built on the device through pa_slot_mapping and
+    pa_write_kv_fp8."""
+    import torch
+    import paged_kv_cache_116_gb300 as pa
+
+    shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
+    sshape = (w.num_blocks, w.num_kv_heads, w.block_size)
+    kc = torch.full(shape, FP8_NAN_CODE, dtype=torch.uint8, device=dev)
+    vc = torch.full_like(kc, FP8_NAN_CODE)
+    ks = torch.full(sshape, float("nan"), dtype=torch.float32, device=dev)
+    vs = torch.full_like(ks, float("nan"))
+    bt = torch.from_numpy(w.block_tables).to(dev)
+    if w.pre_pos.shape[0]:
+        slots = pa.pa_slot_mapping(torch.from_numpy(w.pre_block_tables).to(dev),
+                                   torch.from_numpy(w.pre_seq_idx).to(dev), torch.from_numpy(w.pre_pos).to(dev),
+                                   w.block_size)
+        pa.pa_write_kv_fp8(w.pre_k.to(dev), w.pre_v.to(dev), slots, kc, vc, ks, vs)
+    slots = pa.pa_slot_mapping(bt, torch.from_numpy(w.new_seq_idx).to(dev), torch.from_numpy(w.new_pos).to(dev),
+                               w.block_size)
+    pa.pa_write_kv_fp8(w.new_k.to(dev), w.new_v.to(dev), slots, kc, vc, ks, vs)
+    return kc, vc, ks, vs, bt
+
+
+def oracle_fp8_attention(w, kc, vc, ks, vs, seq_select=None):
+    out = oracle.paged_attention_fp8(W.raw_numpy(w.q), w.dtype, kc, vc, ks, vs, w.block_tables, w.seq_lens,
+                                     w.query_start_loc, w.scale, w.causal)
+    if seq_select is not None:
+        out = out[np.asarray(seq_select, bool)]
+    return out

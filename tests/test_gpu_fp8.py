@@ -1,0 +1,266 @@
+"""GPU parity of the quantized (FP8 E4M3) cache: pa_write_kv_fp8 against the
+oracle's quantizing write (codes and scales bit for bit, NaN canaries in the
+untouched slots included), pa_decode_fp8 against the oracle's attention over
+the codes' exact values (tolerance of the query type: |gpu - exact| <= atol +
+rtol |exact|, helpers.ATOL / RTOL), and the copy-on-write block copy of code
+and scale pools.  Both decode kernels (tensor-core and CUDA-core) are run.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_116_gb300 import workloads as W
+
+from helpers import (FP8_NAN_CODE, device_fp8_caches, oracle_fp8_attention, oracle_fp8_caches, within_tol)
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import paged_kv_cache_116_gb300 as pa
+
+    return pa
+
+
+def run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=0, ctas=0, lens=None, max_context=None):
+    pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, ctas)
+    try:
+        seq_lens = w.seq_lens if lens is None else lens
+        mc = int(seq_lens.max()) if max_context is None else max_context
+        ws_bytes = pa.pa_decode_fp8_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                   w.block_size, mc, W.TORCH_DTYPES[w.dtype])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype],
+                         device=DEV)
+        pa.pa_decode_fp8(out, w.q.to(DEV), kc, vc, ks, vs, bt, torch.from_numpy(seq_lens).to(DEV), mc, w.scale,
+                         workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+        return out
+    finally:
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 0)
+        pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, 0)
+
+
+def compare(w, out, exact):
+    ok, err = within_tol(out.double().cpu().numpy(), exact, w.dtype)
+    assert ok, "max error %.3g beyond tolerance (%s)" % (err, w.name)
+    return err
+
+
+def assert_pools_equal(dev_pools, ora_pools):
+    kc, vc, ks, vs = dev_pools
+    okc, ovc, oks, ovs = ora_pools
+    assert np.array_equal(kc.cpu().numpy(), okc) and np.array_equal(vc.cpu().numpy(), ovc)
+    assert np.array_equal(ks.cpu().numpy().view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(vs.cpu().numpy().view(np.uint32), ovs.view(np.uint32))
+
+
+# ---------------------------------------------------------------- the quantizing write
+
+WRITE_CASES = [
+    ("tiny_f32", lambda: W.tiny_decode()),
+    ("bf16_g4", lambda: W.decode_workload("w_bf16", "bf16", 16, 32, 8, 128, [1, 15, 16, 17, 300], seed=31)),
+    ("f16_mha", lambda: W.decode_workload("w_f16", "f16", 16, 8, 8, 128, [40, 3], std=0.5, seed=32)),
+    ("bs8_hd64", lambda: W.decode_workload("w_bs8", "bf16", 8, 4, 2, 64, [9, 8, 1, 30], seed=33)),
+    ("bs32_hd96", lambda: W.decode_workload("w_bs32", "f16", 32, 6, 3, 96, [70, 33], seed=34)),
+    ("hd256", lambda: W.decode_workload("w_256", "bf16", 16, 4, 1, 256, [20, 48], std=3.0, seed=35)),
+]
+
+
+@pytest.mark.parametrize("name,make", WRITE_CASES)
+def test_write_kv_fp8_matches_oracle_bit_for_bit(pa, name, make):
+    w = make()
+    kc, vc, ks, vs, _ = device_fp8_caches(w, DEV)
+    torch.cuda.synchronize()
+    assert_pools_equal((kc, vc, ks, vs), oracle_fp8_caches(w))
+
+
+def test_write_kv_fp8_special_rows(pa):
+    """An all-zero row keeps scale 1 and zero codes; beside a huge (or a
+    unit) element the rest of a row rounds to small or signed-zero codes;
+    negative slots write nothing."""
+    hkv, hd, bs, nb = 2, 128, 16, 4
+    k = torch.randn(5, hkv, hd, dtype=torch.float32)
+    v = torch.randn(5, hkv, hd, dtype=torch.float32)
+    k[0] = 0.0
+    v[1, 0, 7] = 3.0e4
+    k[3, 1] = -1e-30  # next to 1.0 these round to (signed) zero codes
+    k[3, 1, 0] = 1.0
+    slots = torch.tensor([3, 17, -1, 63, 40], dtype=torch.int64)
+    dk = torch.full((nb, bs, hkv, hd), FP8_NAN_CODE, dtype=torch.uint8, device=DEV)
+    dv = torch.full_like(dk, FP8_NAN_CODE)
+    dks = torch.full((nb, hkv, bs), float("nan"), device=DEV)
+    dvs = torch.full_like(dks, float("nan"))
+    pa.pa_write_kv_fp8(k.to(DEV), v.to(DEV), slots.to(DEV), dk, dv, dks, dvs)
+    torch.cuda.synchronize()
+    ok = np.full((nb, bs, hkv, hd), FP8_NAN_CODE, np.uint8)
+    ov = ok.copy()
+    oks = np.full((nb, hkv, bs), np.nan, np.float32)
+    ovs = oks.copy()
+    oracle.write_kv_fp8(k.numpy(), v.numpy(), "f32", slots.numpy(), ok, ov, oks, ovs)
+    assert_pools_equal((dk, dv, dks, dvs), (ok, ov, oks, ovs))
+    assert oks[0, 0, 3] == 1.0 and np.all(ok[0, 3, 0] == 0)
+    assert np.all(ok[3, 15, 1, 1:] == 0x80) and ok[3, 15, 1, 0] == 0x7E  # slot 63
+
+
+def test_write_kv_fp8_check_mode(pa):
+    dk = torch.zeros((4, 16, 2, 128), dtype=torch.uint8, device=DEV)
+    dv = torch.zeros_like(dk)
+    dks = torch.zeros((4, 2, 16), device=DEV)
+    dvs = torch.zeros_like(dks)
+    k = torch.randn(2, 2, 128, device=DEV, dtype=torch.bfloat16)
+    pa.pa_set_check_mode(True)
+    try:
+        for bad in ([5, 5], [0, 64]):
+            with pytest.raises(pa.PAError, match="PA_ERR_INDEX"):
+                pa.pa_write_kv_fp8(k, k, torch.tensor(bad, device=DEV), dk, dv, dks, dvs)
+        pa.pa_write_kv_fp8(k, k, torch.tensor([0, 63], device=DEV), dk, dv, dks, dvs)
+    finally:
+        pa.pa_set_check_mode(False)
+
+
+# ---------------------------------------------------------------- decode over the quantized cache
+
+def test_gqa_decode_batch_fp8_full(pa):
+    """The 64-sequence GQA batch (bf16 queries, Hq 32, Hkv 8, head_dim 128,
+    block size 16) over an FP8 cache, every output element."""
+    w = W.gqa_decode_batch(device=DEV)
+    pools = device_fp8_caches(w, DEV)
+    kc, vc, ks, vs, bt = pools
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    exact = oracle_fp8_attention(w, *opools)
+    for kernel in (0, 1):
+        compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=kernel), exact)
+
+
+def test_mha_decode_fp8_32seq(pa):
+    """The 13B-style MHA shape (f16, Hq = Hkv = 40, N(0, 0.5) values) on the
+    first 32 sequences of its lognormal length mix."""
+    lens = W.mha_lengths(128, 0)[:32]
+    w = W.decode_workload("mha_fp8", "f16", 16, 40, 40, 128, lens, std=0.5, seed=0, device=DEV)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
+
+
+def test_tiny_decode_fp8_fp32_queries(pa):
+    """fp32 queries run on the CUDA-core kernel and meet the fp32 bound."""
+    w = W.tiny_decode()
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    assert compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact) < 1e-5
+
+
+FP8_CASES = []
+_r = np.random.default_rng(808)
+for _i in range(12):
+    _hd = int(_r.choice([128, 256, 64]))
+    _g = int(_r.choice([1, 2, 4, 6, 8, 12, 16]))
+    _hkv = int(_r.choice([1, 2, 4]))
+    _dt = str(_r.choice(["bf16", "f16"]))
+    _bs = int(_r.choice([8, 16, 16, 32, 64]))
+    _lens = _r.integers(1, 3 * _bs + 9, int(_r.integers(1, 8))).tolist()
+    _lens[0] = int(_r.choice([1, _bs, _bs + 1, 2 * _bs]))
+    FP8_CASES.append((_dt, _hd, _g, _hkv, _bs, _lens, 900 + _i))
+
+
+@pytest.mark.parametrize("dt,hd,g,hkv,bs,lens,seed", FP8_CASES)
+def test_random_small_fp8_decode_both_kernels(pa, dt, hd, g, hkv, bs, lens, seed):
+    w = W.decode_workload("fp8_rand", dt, bs, g * hkv, hkv, hd, lens, seed=seed)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    exact = oracle_fp8_attention(w, *opools)
+    tc_ok = hd in (128, 256)
+    for kernel in ((1, 2) if tc_ok else (1,)):
+        for ctas in ((0, 1, 5) if kernel == 2 else (0,)):
+            compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=kernel, ctas=ctas), exact)
+    if not tc_ok:
+        with pytest.raises(pa.PAError, match="PA_ERR_UNSUPPORTED"):
+            run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=2)
+
+
+@pytest.mark.parametrize("bs", [8, 32, 128, 256])
+def test_fp8_decode_block_sizes(pa, bs):
+    w = W.decode_workload("fp8_bs", "bf16", bs, 16, 4, 128, [1, bs - 1, bs, bs + 1, 3 * bs + 5], seed=bs + 7)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    for kernel in (1, 2):
+        compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=kernel), exact)
+
+
+def test_fp8_zero_length_sequence_gives_zero_row(pa):
+    w = W.decode_workload("fp8_z", "bf16", 16, 8, 2, 128, [5, 1, 40], seed=19)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    lens0 = np.array([5, 0, 40], np.int32)
+    for kernel in (1, 2):
+        out = run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=kernel, lens=lens0, max_context=40)
+        assert torch.count_nonzero(out[1]).item() == 0
+        ok, err = within_tol(out[[0, 2]].double().cpu().numpy(), exact[[0, 2]], "bf16")
+        assert ok, err
+
+
+def test_fp8_permuting_physical_blocks_is_bit_identical(pa):
+    w = W.decode_workload("fp8_perm", "bf16", 16, 32, 8, 128, [700, 33, 1, 250, 16], seed=15)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    base = run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=2)
+    perm = torch.from_numpy(np.random.default_rng(2).permutation(w.num_blocks)).to(DEV)
+    moved = []
+    for t in (kc, vc, ks, vs):
+        u = torch.empty_like(t)
+        u[perm] = t
+        moved.append(u)
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_decode_fp8(pa, w, *moved, bt2, kernel=2)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
+def test_fp8_split_count_invariance_within_tolerance(pa):
+    w = W.decode_workload("fp8_split", "f16", 16, 32, 8, 128, [2000, 1500, 37], seed=16)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    for c in (1, 2, 7, 40, 300):
+        compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=2, ctas=c), exact)
+
+
+def test_fp8_decode_rejects_misaligned_scales(pa):
+    w = W.decode_workload("fp8_al", "bf16", 16, 8, 2, 128, [20], seed=17)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    flat = torch.zeros(ks.numel() + 1, device=DEV)
+    bad = flat[1:].view(ks.shape)  # 4-byte offset
+    with pytest.raises(pa.PAError, match="PA_ERR_INVALID_ARG"):
+        run_decode_fp8(pa, w, kc, vc, bad, vs, bt)
+
+
+# ---------------------------------------------------------------- copy-on-write of a quantized pool
+
+def test_copy_blocks_of_fp8_pools_is_bit_exact(pa):
+    """Code pools copy as PA_FP8_E4M3 blocks, scale pools as fp32 blocks of
+    head_dim 1; two layers; compared with the oracle's block copy."""
+    w = W.decode_workload("fp8_cow", "bf16", 16, 8, 2, 128, [40, 17, 100], seed=18)
+    layers = [device_fp8_caches(w, DEV) for _ in range(2)]
+    opools = oracle_fp8_caches(w)
+    pairs = np.array([[int(w.block_tables[0, 0]), int(w.block_tables[1, 1])],
+                      [int(w.block_tables[2, 3]), int(w.block_tables[0, 2])]], np.int64)
+    # destinations must not be read elsewhere in this call: they are not sources
+    assert not set(pairs[:, 1]) & set(pairs[:, 0])
+    dp = torch.from_numpy(pairs).to(DEV)
+    pa.pa_copy_blocks([l[0] for l in layers], [l[1] for l in layers], dp)
+    pa.pa_copy_blocks([l[2] for l in layers], [l[3] for l in layers], dp)
+    torch.cuda.synchronize()
+    okc, ovc, oks, ovs = (a.copy() for a in opools)
+    oracle.copy_blocks([okc], [ovc], pairs)
+    oracle.copy_blocks([oks], [ovs], pairs)
+    for l in layers:
+        assert_pools_equal(l[:4], (okc, ovc, oks, ovs))
