@@ -8,6 +8,10 @@ A step is one pass of the path over one batch, through the C ABI:
   mixed_varlen:     pa_copy_blocks (copy-on-write of the shared tails) ->
                     pa_slot_mapping -> pa_write_kv (every new token) ->
                     pa_varlen (prefill chunks + decode rows)
+  --kv-dtype fp8:   a decode workload over the quantized cache (E4M3 codes,
+                    one fp32 scale per token and KV head): pa_slot_mapping ->
+                    pa_write_kv_fp8 -> pa_decode_fp8; its K/V bytes are the
+                    codes plus the scales
 Inputs are resident in HBM.  Enough copies of the K/V pool to exceed twice
 the 129 MB L2 alternate between steps, so no step reads a pool the previous
 one left in L2.  The step is captured once per pool copy as a CUDA graph and
@@ -61,6 +65,8 @@ def parse():
                     help="measure pa_swap_blocks (device pool <-> pinned host pool) instead of the attention step")
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as pa_slot_mapping + pa_write_kv + pa_decode instead of pa_decode_append")
+    ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
+                    help="fp8: decode workloads over an FP8 E4M3 cache (queries keep the workload's type)")
     return ap.parse_args()
 
 
@@ -188,6 +194,37 @@ def oracle_step(w, kc, vc, q):
                                   w.causal)
 
 
+def oracle_setup_fp8(w):
+    """Oracle-side quantized pool (codes and scales) of a host decode workload."""
+    import numpy as np
+
+    import oracle
+    from paged_kv_cache_116_gb300 import workloads as W
+
+    kc = np.full((w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim), 0x7F, np.uint8)
+    vc = kc.copy()
+    ks = np.full((w.num_blocks, w.num_kv_heads, w.block_size), np.nan, np.float32)
+    vs = ks.copy()
+    s = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
+    oracle.write_kv_fp8(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), w.dtype, s, kc, vc, ks, vs)
+    s = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
+    oracle.write_kv_fp8(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), w.dtype, s, kc, vc, ks, vs)
+    return (kc, vc, ks, vs), W.raw_numpy(w.q)
+
+
+def oracle_step_fp8(w, pools, q):
+    import oracle
+
+    return oracle.paged_attention_fp8(q, w.dtype, *pools, w.block_tables, w.seq_lens, w.query_start_loc, w.scale,
+                                      w.causal)
+
+
+def fp8_kv_bytes(w):
+    """Bytes of the quantized cache a decode step reads: per context token and
+    KV head, head_dim codes and one fp32 scale, for K and for V."""
+    return int(w.seq_lens.astype("int64").sum()) * w.num_kv_heads * 2 * (w.head_dim + 4)
+
+
 def host_sample_workload(name):
     """A bounded sample of a workload with the same generators, values drawn
     on the host: its first requests (or, for the mixed step, fewer chunks and
@@ -201,24 +238,32 @@ def host_sample_workload(name):
             "mixed_varlen": lambda: W.mixed_varlen(num_chunks=1, num_groups=4)}[name]()
 
 
-def cpu_sample(name, budget_s=10.0):
+def oracle_runner(w, fp8):
+    """(one oracle step as a callable, K/V bytes it reads) for a host workload."""
+    if fp8:
+        pools, q = oracle_setup_fp8(w)
+        return (lambda: oracle_step_fp8(w, pools, q)), fp8_kv_bytes(w)
+    kc, vc, q = oracle_setup(w)
+    return (lambda: oracle_step(w, kc, vc, q)), w.kv_bytes_read()
+
+
+def cpu_sample(name, budget_s=10.0, fp8=False):
     """The oracle (as it stands) on a bounded sample of the workload,
     repeated for about budget_s seconds."""
     import oracle
 
     w = host_sample_workload(name)
-    kc, vc, q = oracle_setup(w)
-    per_step = w.kv_bytes_read()
+    run, per_step = oracle_runner(w, fp8)
     reps, t = 0, time.perf_counter()
     while True:
-        oracle_step(w, kc, vc, q)
+        run()
         reps += 1
         el = time.perf_counter() - t
         if el >= budget_s:
             break
     return {"value": per_step * reps / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": "%d requests of the same generators (%d context tokens) x %d, fp64 C oracle with OpenMP, "
-                      "%.1f s" % (w.num_seqs, int(w.seq_lens.sum()), reps, el),
+            "sample": "%d requests of the same generators (%d context tokens) x %d, fp64 C oracle with OpenMP%s, "
+                      "%.1f s" % (w.num_seqs, int(w.seq_lens.sum()), reps, ", FP8 cache" if fp8 else "", el),
             "seq_per_s": w.num_seqs * reps / el}
 
 
@@ -229,22 +274,23 @@ def run_reference(args, rank):
         return
     import oracle
 
+    fp8 = args.kv_dtype == "fp8"
     w = host_sample_workload(args.workload)
-    kc, vc, q = oracle_setup(w)
-    step_bytes = w.kv_bytes_read()
+    run, step_bytes = oracle_runner(w, fp8)
     for _ in range(args.warmup):
-        oracle_step(w, kc, vc, q)
+        run()
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle_step(w, kc, vc, q)
+        run()
     dt = time.perf_counter() - t
     value = step_bytes * args.steps / dt / 1e9
-    desc = "%d requests of the %s generators per step, fp64 C oracle with OpenMP" % (w.num_seqs, args.workload)
+    desc = "%d requests of the %s generators per step, fp64 C oracle with OpenMP%s" % (
+        w.num_seqs, args.workload, " over an FP8 cache" if fp8 else "")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "sample_requests": w.num_seqs},
+        "config": {"workload": w.name + ("_fp8cache" if fp8 else ""), "sample_requests": w.num_seqs},
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
@@ -392,12 +438,15 @@ def main():
     tdt = W.TORCH_DTYPES[w.dtype]
     S, hq, hkv, hd, bs = w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     decode = w.is_decode and w.cow_pairs.shape[0] == 0
+    fp8 = args.kv_dtype == "fp8"
+    if fp8 and not decode:
+        raise SystemExit("--kv-dtype fp8 applies to the decode workloads")
     max_ctx, max_q = int(w.seq_lens.max()), int(w.query_lens.max())
-    kv_bytes = w.kv_bytes_read()
+    kv_bytes = fp8_kv_bytes(w) if fp8 else w.kv_bytes_read()
     N = int(w.query_lens.sum())
 
     # resident pools, filled through the library; enough copies to defeat L2
-    pool_bytes = 2 * w.num_blocks * bs * hkv * hd * w.elt
+    pool_bytes = 2 * w.num_blocks * bs * hkv * (hd + 4 if fp8 else hd * w.elt)
     copies = 1 if args.no_rotate else min(16, max(2, math.ceil(2 * L2_BYTES / pool_bytes)))
     l2_note = ("inputs larger than L2: %d pool copies of %.3f GB alternate between steps" % (copies, pool_bytes / 1e9)
                if copies * pool_bytes > L2_BYTES else
@@ -411,11 +460,19 @@ def main():
     pre_k = w.pre_k.to(dev) if pre_slots is not None else None
     pre_v = w.pre_v.to(dev) if pre_slots is not None else None
     for c in range(copies):
-        kc = torch.full((w.num_blocks, bs, hkv, hd), float("nan"), dtype=tdt, device=dev)
-        vc = torch.full_like(kc, float("nan"))
+        if fp8:
+            kc = torch.full((w.num_blocks, bs, hkv, hd), 0x7F, dtype=torch.uint8, device=dev)  # NaN codes
+            vc = torch.full_like(kc, 0x7F)
+            ks = torch.full((w.num_blocks, hkv, bs), float("nan"), dtype=torch.float32, device=dev)
+            vs = torch.full_like(ks, float("nan"))
+            pool = (kc, vc, ks, vs)
+        else:
+            kc = torch.full((w.num_blocks, bs, hkv, hd), float("nan"), dtype=tdt, device=dev)
+            vc = torch.full_like(kc, float("nan"))
+            pool = (kc, vc)
         if pre_slots is not None:
-            pa.pa_write_kv(pre_k, pre_v, pre_slots, kc, vc)
-        pools.append((kc, vc))
+            (pa.pa_write_kv_fp8 if fp8 else pa.pa_write_kv)(pre_k, pre_v, pre_slots, *pool)
+        pools.append(pool)
     w.pre_k = w.pre_v = pre_k = pre_v = None
     bt = torch.from_numpy(w.block_tables).to(dev)
     lens = torch.from_numpy(w.seq_lens).to(dev)
@@ -427,29 +484,32 @@ def main():
     out = torch.empty_like(q)
     slot_buf = torch.empty(N, dtype=torch.int64, device=dev)
     if decode:
-        ws_bytes = pa.pa_decode_workspace_size(S, hq, hkv, hd, bs, max_ctx, tdt)
+        ws_bytes = (pa.pa_decode_fp8_workspace_size if fp8 else pa.pa_decode_workspace_size)(S, hq, hkv, hd, bs,
+                                                                                              max_ctx, tdt)
     else:
         ws_bytes = pa.pa_varlen_workspace_size(S, N, max_q, hq, hkv, hd, bs, max_ctx, tdt)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
-    def attend(kc, vc, qq, tables, ll, cuq, st):
-        if decode:
-            pa.pa_decode(out, qq, kc, vc, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
+    def attend(pool, qq, tables, ll, cuq, st):
+        if fp8:
+            pa.pa_decode_fp8(out, qq, *pool, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
+        elif decode:
+            pa.pa_decode(out, qq, *pool, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
         else:
-            pa.pa_varlen(out, qq, kc, vc, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
+            pa.pa_varlen(out, qq, *pool, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
                          workspace=ws, stream=st)
 
-    fused = decode and not args.unfused
+    fused = decode and not args.unfused and not fp8
 
     def run_step_unfused(i, t_in):
-        kc, vc = pools[i % copies]
+        pool = pools[i % copies]
         st = torch.cuda.current_stream()
         d_q, d_k, d_v, d_bt, d_lens, d_cu, d_seq, d_pos, d_pairs = t_in
         if d_pairs.shape[0]:
-            pa.pa_copy_blocks(kc, vc, d_pairs, stream=st)
+            pa.pa_copy_blocks(pool[0], pool[1], d_pairs, stream=st)
         pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=st)
-        pa.pa_write_kv(d_k, d_v, slot_buf, kc, vc, stream=st)
-        attend(kc, vc, d_q, d_bt, d_lens, d_cu, st)
+        (pa.pa_write_kv_fp8 if fp8 else pa.pa_write_kv)(d_k, d_v, slot_buf, *pool, stream=st)
+        attend(pool, d_q, d_bt, d_lens, d_cu, st)
 
     def run_step(i, t_in):
         """One pass of the path through the C ABI on the current stream."""
@@ -468,11 +528,10 @@ def main():
         run_step(i, dev_in)
 
     def kernel_only(i):
-        kc, vc = pools[i % copies]
-        attend(kc, vc, q, bt, lens, cu, torch.cuda.current_stream())
+        attend(pools[i % copies], q, bt, lens, cu, torch.cuda.current_stream())
 
-    tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in (64, 128, 256) and hq // hkv <= 16 and
-                 (bs == 8 or (bs % 16 == 0 and bs <= 256)))
+    tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in ((128, 256) if fp8 else (64, 128, 256)) and
+                 hq // hkv <= 16 and (bs == 8 or (bs % 16 == 0 and bs <= 256)))
     launches_per_step = (1 if tc_decode else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
@@ -568,13 +627,13 @@ def main():
         nblk = int(sum((L + bs - 1) // bs for L in w.seq_lens.tolist()))
         alg = kv_bytes + 2 * S * hq * hd * w.elt + nblk * 4 + S * 4
         achieved = alg / (kern_ms / 1e3) / 1e9
-        tc_ok = (w.dtype in ("bf16", "f16") and hd in (64, 128, 256) and hq // hkv <= 16 and
-                 (bs == 8 or (bs % 16 == 0 and bs <= 256)))
-        roof = {"bound": "hbm", "kernel": ("decode_tc_kernel (pa_decode, split merge included)" if tc_ok else
-                                           "attn_simt_kernel (pa_decode, CUDA-core path)"),
+        call = "pa_decode_fp8" if fp8 else "pa_decode"
+        roof = {"bound": "hbm", "kernel": ("decode_tc_kernel%s (%s, split merge included)" % (
+                    "<FP8>" if fp8 else "", call) if tc_decode else "attn_simt_kernel (%s, CUDA-core path)" % call),
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
-                "traffic": traffic_record(args.workload, "pa_decode_tc.cu"), "kernel_us": kern_ms * 1e3}
+                "traffic": traffic_record(args.workload + ("_fp8" if fp8 else ""), "pa_decode_tc.cu"),
+                "kernel_us": kern_ms * 1e3}
     else:
         fl = varlen_flops(w)
         achieved = fl / (kern_ms / 1e3) / 1e12
@@ -589,15 +648,17 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": {"workload": w.name, "num_seqs": S, "new_tokens": N, "num_heads": hq, "num_kv_heads": hkv,
+            "vs_baseline": None, "dtype": ("e4m3 cache, %s q/out" % w.dtype) if fp8 else w.dtype, "data": "synthetic",
+            "config": {"workload": w.name + ("_fp8cache" if fp8 else ""), "num_seqs": S, "new_tokens": N, "num_heads": hq, "num_kv_heads": hkv,
                        "head_dim": hd, "block_size": bs, "num_blocks": w.num_blocks,
                        "total_context": int(w.seq_lens.sum()), "cow_pairs": int(w.cow_pairs.shape[0]),
                        "kv_bytes_per_step": kv_bytes,
                        "l2": l2_note,
                        "step": ("pa_decode_append (slot translation + K/V write + decode, one call)" if fused else
-                                ("pa_copy_blocks + " if pairs.shape[0] else "") + "pa_slot_mapping + pa_write_kv + " +
-                                ("pa_decode" if decode else "pa_varlen")) + ", replayed as a CUDA graph",
+                                ("pa_copy_blocks + " if pairs.shape[0] else "") + "pa_slot_mapping + " +
+                                ("pa_write_kv_fp8 + pa_decode_fp8" if fp8 else
+                                 "pa_write_kv + " + ("pa_decode" if decode else "pa_varlen"))) +
+                               ", replayed as a CUDA graph",
                        "seed": 0},
             "seq_per_s": seq_per_s,
             "eager_ms_per_step": eager_ms,
@@ -608,7 +669,7 @@ def main():
             "e2e": e2e,
         }
         if not args.no_extras:
-            line["cpu_baseline"] = cpu_sample(args.workload)
+            line["cpu_baseline"] = cpu_sample(args.workload, fp8=fp8)
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()

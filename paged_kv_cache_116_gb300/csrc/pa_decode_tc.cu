@@ -14,7 +14,9 @@
 //    bytes whatever the length mix.  A unit cut between warps leaves partial
 //    softmax states (m, l, unnormalised o) in the workspace; the last of the
 //    unit's warps to finish (an epoch-tagged atomic count per unit, so the
-//    workspace never needs clearing) merges them by their log-sum-exp, in
+//    workspace never needs clearing; the last one zeroes the count, so a
+//    CUDA-graph replay of the same launch counts afresh) merges them by their
+//    log-sum-exp, in
 //    a fixed order ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
 //    apart and merged by the online-softmax rule).  The cut depends only on
 //    the lengths, never on physical block ids.
@@ -106,13 +108,14 @@ struct Geo {
     static constexpr int KS = HD / 16;          // k-steps of K Q^T == m-tiles of V^T P^T
 };
 
-// Warps per CTA and stages per warp.
+// Warps per CTA, stages per warp, and CTAs per SM the register budget is
+// sized for (__launch_bounds__).
 template <int HD, bool FP8> struct Pipe;
-template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6; };
-template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3; };
-template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3; };
-template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 6; };
-template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3; };
+template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6, MINB = 1; };
+template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3, MINB = 1; };
+template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3, MINB = 1; };
+template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 6, MINB = 1; };
+template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3, MINB = 1; };
 
 template <int HD, bool FP8>
 constexpr size_t smem_bytes(int num_seqs) {
@@ -137,7 +140,7 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 // T: element type of q and out.  FP8: the cache holds E4M3 codes plus
 // scales (the mma then runs in f16 whatever T is).
 template <typename T, int HD, int NT, bool FP8>
-__global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32)
+__global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const TcParams p) {
     using Gm = Geo<HD, FP8>;
@@ -261,37 +264,27 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32)
         const int32_t row = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
         const int32_t row2 = __shfl_sync(0xffffffffu, tbl_cur2, ip & 31);
         const int slot = ip % R;
-        if (lane == 0) {
-            uint8_t* dst = wst + (size_t)slot * Gm::STAGE;
+        // The stage's copies go out from several lanes in one instruction
+        // (a TMA unit takes lane-parallel copies faster than a sequence of
+        // copies from one thread): lanes [0, nbox) each load one 128-byte x
+        // 16-row (or 8-row) box of K or V, the next lanes the K and V scales.
+        const int halves = bsz == 8 ? 2 : 1;  // 8-token blocks: two 8-row boxes per chunk
+        const int nbox = Gm::CH * 2 * halves;
+        const int nops = nbox + (FP8 ? 2 * halves : 0);
+        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE + Gm::SCL);
+        if (lane < nops) {
             fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE + Gm::SCL);
-            if constexpr (FP8) {
-                // scale of pool row r for KV head ih: [r / bs][ih][r % bs]
-                float* sd = wscl + slot * (Gm::SCL / 4);
-                const int64_t i1 = (int64_t)(row / bsz) * Hkv * bsz + (int64_t)ih * bsz + row % bsz;
-                if (bsz == 8) {
-                    const int64_t i2 = (int64_t)(row2 / 8) * Hkv * 8 + (int64_t)ih * 8 + row2 % 8;
-                    bulk_load(sd, p.k_scales + i1, 32, &wbar[slot]);
-                    bulk_load(sd + 8, p.k_scales + i2, 32, &wbar[slot]);
-                    bulk_load(sd + BS, p.v_scales + i1, 32, &wbar[slot]);
-                    bulk_load(sd + BS + 8, p.v_scales + i2, 32, &wbar[slot]);
-                } else {
-                    bulk_load(sd, p.k_scales + i1, 64, &wbar[slot]);
-                    bulk_load(sd + BS, p.v_scales + i1, 64, &wbar[slot]);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < Gm::CH; ++c) {
-                if (bsz == 8) {  // two 8-row boxes, each a 1024-byte swizzle atom
-                    tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
-                    tma_load_3d(dst + c * BS * 128 + 1024, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row2, pol);
-                    tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
-                    tma_load_3d(dst + Gm::TILE + c * BS * 128 + 1024, &tmV, &wbar[slot], 0, ih * Gm::CH + c,
-                                row2, pol);
-                } else {
-                    tma_load_3d(dst + c * BS * 128, &tmK, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
-                    tma_load_3d(dst + Gm::TILE + c * BS * 128, &tmV, &wbar[slot], 0, ih * Gm::CH + c, row, pol);
-                }
+            if (lane < nbox) {
+                const int hf = lane % halves, c = (lane / halves) % Gm::CH, is_v = lane / (halves * Gm::CH);
+                uint8_t* dst = wst + (size_t)slot * Gm::STAGE + is_v * Gm::TILE + c * BS * 128 + hf * 1024;
+                tma_load_3d(dst, is_v ? &tmV : &tmK, &wbar[slot], 0, ih * Gm::CH + c, hf ? row2 : row, pol);
+            } else if constexpr (FP8) {
+                // scales of pool row r for KV head ih: [r / bs][ih][r % bs]
+                const int o = lane - nbox, hf = o % halves, is_v = o / halves;
+                const int32_t r = hf ? row2 : row;
+                const int64_t si = (int64_t)(r / bsz) * Hkv * bsz + (int64_t)ih * bsz + r % bsz;
+                float* sd = wscl + slot * (Gm::SCL / 4) + is_v * BS + hf * 8;
+                bulk_load(sd, (is_v ? p.v_scales : p.k_scales) + si, halves == 2 ? 32 : 64, &wbar[slot]);
             }
         }
         ++ip;
@@ -494,6 +487,10 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32)
                     cur = prev;
                 }
                 last = ((int)(want & 0xffffull) == expected) ? 1 : 0;
+                // The unit's count is complete: leave it at zero, so that a
+                // replay of this very launch (a CUDA graph keeps its epoch)
+                // starts the count afresh instead of continuing it.
+                if (last) atomicExch(cnt, 0ull);
             }
             last = __shfl_sync(0xffffffffu, last, 0);
             if (last) {
@@ -731,8 +728,12 @@ bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, bool fp8, int num
     cuuint32_t estr[3] = {1, 1, 1};
     const CUtensorMapDataType ty = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                        : (dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    // L2 fills of 256 bytes suit a 16-bit head row (two 128-byte chunks); a
+    // code row is one 128-byte chunk, and a 256-byte fill would drag in the
+    // neighbouring head's row
+    const CUtensorMapL2promotion promo = fp8 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
     CUresult r = fn(m, ty, 3, const_cast<void*>(cache), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                    CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         *err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
         return false;

@@ -148,3 +148,30 @@ def oracle_fp8_attention(w, kc, vc, ks, vs, seq_select=None):
     if seq_select is not None:
         out = out[np.asarray(seq_select, bool)]
     return out
+
+
+# ---- CUDA-graph replay -------------------------------------------------
+
+def graph_replays_match_eager(decode_fn, q, dev):
+    """decode_fn(out, q, ws) captured once in a CUDA graph and replayed with
+    new queries each time must give, bit for bit, what an eager call gives:
+    units split across warps have to be merged on every replay, not only on
+    the first."""
+    import torch
+
+    out = torch.empty_like(q)
+    ref = torch.empty_like(q)
+    ws_graph = torch.empty(1 << 24, dtype=torch.uint8, device=dev)
+    ws_eager = torch.empty(1 << 24, dtype=torch.uint8, device=dev)
+    decode_fn(out, q, ws_graph)  # first call outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        decode_fn(out, q, ws_graph)
+    gen = torch.Generator(device=dev).manual_seed(77)
+    for _ in range(4):
+        q.copy_(torch.randn(q.shape, generator=gen, device=dev).to(q.dtype))
+        g.replay()
+        decode_fn(ref, q, ws_eager)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))

@@ -12,7 +12,7 @@ import torch
 import oracle
 from paged_kv_cache_116_gb300 import workloads as W
 
-from helpers import device_caches, oracle_attention, oracle_caches, within_tol
+from helpers import device_caches, graph_replays_match_eager, oracle_attention, oracle_caches, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -250,3 +250,14 @@ def test_decode_append_block_sizes(pa, bs):
 
     assert np.array_equal(raw_bits(kc), oracle_bits(okc)) and np.array_equal(raw_bits(vc), oracle_bits(ovc))
     compare(w, out, oracle_attention(w, okc, ovc))
+
+
+# ---------------------------------------------------------------- CUDA-graph replay
+
+def test_graph_replays_of_decode_follow_new_queries(pa):
+    w = W.decode_workload("graph", "bf16", 16, 32, 8, 128, [2000, 1500, 37, 700, 16], seed=41)
+    kc, vc, bt = device_caches(w, DEV)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    graph_replays_match_eager(
+        lambda out, q, ws: pa.pa_decode(out, q, kc, vc, bt, lens, mc, w.scale, workspace=ws), w.q.to(DEV).clone(), DEV)

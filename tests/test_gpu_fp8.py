@@ -12,7 +12,8 @@ import torch
 import oracle
 from paged_kv_cache_116_gb300 import workloads as W
 
-from helpers import (FP8_NAN_CODE, device_fp8_caches, oracle_fp8_attention, oracle_fp8_caches, within_tol)
+from helpers import (FP8_NAN_CODE, device_fp8_caches, graph_replays_match_eager, oracle_fp8_attention,
+                     oracle_fp8_caches, within_tol)
 
 pytestmark = pytest.mark.gpu
 
@@ -264,3 +265,13 @@ def test_copy_blocks_of_fp8_pools_is_bit_exact(pa):
     oracle.copy_blocks([oks], [ovs], pairs)
     for l in layers:
         assert_pools_equal(l[:4], (okc, ovc, oks, ovs))
+
+
+def test_graph_replays_of_fp8_decode_follow_new_queries(pa):
+    w = W.decode_workload("fp8_graph", "bf16", 16, 32, 8, 128, [2000, 1500, 37, 700, 16], seed=42)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    graph_replays_match_eager(
+        lambda out, q, ws: pa.pa_decode_fp8(out, q, kc, vc, ks, vs, bt, lens, mc, w.scale, workspace=ws),
+        w.q.to(DEV).clone(), DEV)
