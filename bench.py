@@ -9,9 +9,10 @@ A step is one pass of the path over one batch, through the C ABI:
                     pa_slot_mapping -> pa_write_kv (every new token) ->
                     pa_varlen (prefill chunks + decode rows)
   --kv-dtype fp8:   a decode workload over the quantized cache (E4M3 codes,
-                    one fp32 scale per token and KV head): pa_slot_mapping ->
-                    pa_write_kv_fp8 -> pa_decode_fp8; its K/V bytes are the
-                    codes plus the scales
+                    one fp32 scale per token and KV head): pa_decode_append_fp8
+                    (the new rows quantized into their slots, then the decode;
+                    --unfused: pa_slot_mapping -> pa_write_kv_fp8 ->
+                    pa_decode_fp8); its K/V bytes are the codes plus the scales
 Inputs are resident in HBM.  Enough copies of the K/V pool to exceed twice
 the 129 MB L2 alternate between steps, so no step reads a pool the previous
 one left in L2.  The step is captured once per pool copy as a CUDA graph and
@@ -499,7 +500,7 @@ def main():
             pa.pa_varlen(out, qq, *pool, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
                          workspace=ws, stream=st)
 
-    fused = decode and not args.unfused and not fp8
+    fused = decode and not args.unfused
 
     def run_step_unfused(i, t_in):
         pool = pools[i % copies]
@@ -515,10 +516,10 @@ def main():
         """One pass of the path through the C ABI on the current stream."""
         if not fused:
             return run_step_unfused(i, t_in)
-        kc, vc = pools[i % copies]
         d_q, d_k, d_v, d_bt, d_lens = t_in[:5]
-        pa.pa_decode_append(out, d_q, d_k, d_v, kc, vc, d_bt, d_lens, max_ctx, w.scale, workspace=ws,
-                            stream=torch.cuda.current_stream())
+        (pa.pa_decode_append_fp8 if fp8 else pa.pa_decode_append)(
+            out, d_q, d_k, d_v, *pools[i % copies], d_bt, d_lens, max_ctx, w.scale, workspace=ws,
+            stream=torch.cuda.current_stream())
 
     dev_in = (q, new_k, new_v, bt, lens, cu, seq_idx, pos, pairs)
     if fused:
@@ -532,7 +533,8 @@ def main():
 
     tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in ((128, 256) if fp8 else (64, 128, 256)) and
                  hq // hkv <= 16 and (bs == 8 or (bs % 16 == 0 and bs <= 256)))
-    launches_per_step = (1 if tc_decode else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
+    fused_in_kernel = tc_decode and (not fp8 or hd == 128)  # the append happens inside the decode kernel
+    launches_per_step = (1 if fused_in_kernel else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -654,7 +656,9 @@ def main():
                        "total_context": int(w.seq_lens.sum()), "cow_pairs": int(w.cow_pairs.shape[0]),
                        "kv_bytes_per_step": kv_bytes,
                        "l2": l2_note,
-                       "step": ("pa_decode_append (slot translation + K/V write + decode, one call)" if fused else
+                       "step": ("%s (slot translation + K/V %s + decode, one call)" % (
+                                    "pa_decode_append_fp8" if fp8 else "pa_decode_append",
+                                    "quantizing write" if fp8 else "write") if fused else
                                 ("pa_copy_blocks + " if pairs.shape[0] else "") + "pa_slot_mapping + " +
                                 ("pa_write_kv_fp8 + pa_decode_fp8" if fp8 else
                                  "pa_write_kv + " + ("pa_decode" if decode else "pa_varlen"))) +

@@ -280,6 +280,23 @@ PA_API pa_status pa_decode_append(void* out, const void* q, const void* k_new, c
                                   int dtype, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_decode_append_fp8 -- pa_decode_append over a quantized cache: each
+ * sequence's new rows k_new[s], v_new[s] (of dtype, the query type) are
+ * quantized as pa_write_kv_fp8 does it into the slot of position L-1 (codes
+ * and scales), and out[s] is pa_decode_fp8 over positions 0..L-1 after that
+ * write ("分页 KV Cache", §分页注意力: the step writes the new K/V, then
+ * attends).  One kernel launch on the tensor-core path with head_dim 128;
+ * otherwise a quantizing write kernel, then the decode.  Sequences with
+ * L = 0 get a zero row and no write.  Same workspace as pa_decode_fp8.
+ */
+PA_API pa_status pa_decode_append_fp8(void* out, const void* q, const void* k_new, const void* v_new,
+                                      void* k_codes, void* v_codes, float* k_scales, float* v_scales,
+                                      const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                                      int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t num_blocks, int32_t block_size, int32_t max_context, float scale,
+                                      int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * pa_varlen -- the handbook's paged_attention: a batch of requests, each
  * with seq_lens[i] tokens of context after this step of which the last
  * n_i = cu_seqlens_q[i+1] - cu_seqlens_q[i] are new; request i's queries

@@ -22,7 +22,8 @@ POOL_DTYPE_CODE = {**DTYPE_CODE, torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: 
 EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
-           "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8")
+           "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8",
+           "pa_decode_append_fp8")
 
 
 class PAError(RuntimeError):
@@ -55,6 +56,8 @@ def lib():
         "pa_write_kv": ([vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, ci, vp], ci),
         "pa_write_kv_fp8": ([vp, vp, vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, ci, vp], ci),
         "pa_decode_fp8_workspace_size": ([i32, i32, i32, i32, i32, i32, ci], sz),
+        "pa_decode_append_fp8": ([vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf,
+                                  ci, vp, sz, vp], ci),
         "pa_decode_fp8": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp, sz,
                            vp], ci),
         "pa_copy_blocks": ([vp, vp, i32, vp, i32, i32, i32, i32, i32, ci, vp], ci),
@@ -239,6 +242,22 @@ def pa_decode_fp8(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, co
                              _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), S, hq, hkv, hd, nb, bs,
                              max_context, float(scale), _dtype(q), _ptr(workspace), ws_bytes, _stream(stream))
     _check(st, "pa_decode_fp8")
+    return out
+
+
+def pa_decode_append_fp8(out, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens,
+                         max_context, scale, workspace=None, stream=None):
+    """The generation step over a quantized cache: each sequence's new rows k_new, v_new
+    [S, Hkv, hd] (query type) are quantized into the slot of position L-1, then decoded."""
+    _dev(out, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_tables, context_lens, workspace)
+    nb, bs, hkv, hd = k_codes.shape
+    S, hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_decode_append_fp8(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_codes), _ptr(v_codes),
+                                    _ptr(k_scales), _ptr(v_scales), _ptr(block_tables), block_tables.shape[1],
+                                    _ptr(context_lens), S, hq, hkv, hd, nb, bs, max_context, float(scale), _dtype(q),
+                                    _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pa_decode_append_fp8")
     return out
 
 

@@ -431,13 +431,22 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
     pa_status sel;
     const bool tc = use_decode_tc(dtype, head_dim, block_size, G, fp8, &sel);
     if (sel != PA_OK) return sel;
+    // The tensor-core kernel fuses the append for 16-bit caches and for code
+    // caches of head_dim 128; otherwise the new rows are written (quantized
+    // for a code cache) by a separate kernel first, then attended from the pool.
+    const bool fused_append = append && tc && (!fp8 || head_dim == 128);
+    if (append && !fused_append) {
+        cudaError_t e = fp8 ? pa::launch_append_kv_fp8(k_new, v_new, dtype, block_tables, max_blocks, context_lens,
+                                                       num_seqs, num_kv_heads, head_dim, block_size,
+                                                       static_cast<uint8_t*>(const_cast<void*>(k_cache)),
+                                                       static_cast<uint8_t*>(const_cast<void*>(v_cache)),
+                                                       const_cast<float*>(k_scales), const_cast<float*>(v_scales), st)
+                            : pa::launch_append_kv(k_new, v_new, block_tables, max_blocks, context_lens, num_seqs,
+                                                   block_size, const_cast<void*>(k_cache),
+                                                   const_cast<void*>(v_cache), row_bytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, "pa_decode_append launch");
+    }
     if (!tc) {
-        if (append) {  // write the new rows first, then attend from the pool
-            cudaError_t e = pa::launch_append_kv(k_new, v_new, block_tables, max_blocks, context_lens, num_seqs,
-                                                 block_size, const_cast<void*>(k_cache), const_cast<void*>(v_cache),
-                                                 row_bytes, st);
-            if (e != cudaSuccess) return cuda_fail(e, "pa_decode_append launch");
-        }
         cudaError_t e = pa::launch_attn_simt(a, st);
         return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_decode launch");
     }
@@ -458,7 +467,7 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
         c.q = static_cast<const uint8_t*>(q) + (int64_t)s0 * num_heads * head_dim * elt;
         c.block_tables = block_tables + (int64_t)s0 * max_blocks;
         c.seq_lens = context_lens + s0;
-        if (append) {
+        if (fused_append) {
             c.k_new = static_cast<const uint8_t*>(k_new) + (int64_t)s0 * row_bytes;
             c.v_new = static_cast<const uint8_t*>(v_new) + (int64_t)s0 * row_bytes;
         }
@@ -500,6 +509,18 @@ pa_status pa_decode_append(void* out, const void* q, const void* k_new, const vo
                            float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
     if (num_seqs > 0 && (!k_new || !v_new)) return fail(PA_ERR_INVALID_ARG, "null pointer");
     return decode_impl(out, q, k_new, v_new, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks,
+                       context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context,
+                       scale, dtype, workspace, workspace_bytes, stream);
+}
+
+pa_status pa_decode_append_fp8(void* out, const void* q, const void* k_new, const void* v_new, void* k_codes,
+                               void* v_codes, float* k_scales, float* v_scales, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                               int32_t max_context, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                               void* stream) {
+    if (num_seqs > 0 && (!k_new || !v_new || !k_scales || !v_scales)) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    return decode_impl(out, q, k_new, v_new, k_codes, v_codes, k_scales, v_scales, block_tables, max_blocks,
                        context_lens, num_seqs, num_heads, num_kv_heads, head_dim, num_blocks, block_size, max_context,
                        scale, dtype, workspace, workspace_bytes, stream);
 }

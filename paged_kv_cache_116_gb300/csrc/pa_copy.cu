@@ -90,21 +90,11 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
 // pool, the scale to [slot / block_size][head][slot % block_size].
 constexpr int kQuantWarps = 8;
 
+// One warp quantizes one row of hd <= 256 elements (src in T) into codes at
+// dst and its scale at *scale.
 template <typename T>
-__global__ void __launch_bounds__(kQuantWarps * 32)
-    write_kv_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, const int64_t* __restrict__ slots,
-                        int64_t n, int32_t hkv, int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes,
-                        uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales) {
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;  // ((token * hkv + head) * 2 + K|V)
-    if (item >= n * hkv * 2) return;
-    const int is_v = (int)(item & 1);
-    const int64_t row = item >> 1, token = row / hkv;
-    const int32_t h = (int32_t)(row - token * hkv);
-    const int64_t slot = slots[token];
-    if (slot < 0) return;
-    const T* src = (is_v ? v : k) + row * hd;
+__device__ __forceinline__ void quantize_row(const T* __restrict__ src, int32_t hd, uint8_t* __restrict__ dst,
+                                             float* __restrict__ scale, int lane) {
     float x[8], amax = 0.f;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -115,16 +105,57 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-    uint8_t* dst = (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         const int d = lane + 32 * j;
         if (d < hd) dst[d] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3);
     }
-    if (lane == 0) {
-        const int64_t blk = slot / bs;
-        (is_v ? v_scales : k_scales)[(blk * hkv + h) * bs + (slot - blk * bs)] = s;
-    }
+    if (lane == 0) *scale = s;
+}
+
+// Warp item -> (token or sequence, KV head, K|V): item = (row * 2 + is_v), row = t * hkv + h.
+template <typename T>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    write_kv_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, const int64_t* __restrict__ slots,
+                        int64_t n, int32_t hkv, int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes,
+                        uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;
+    if (item >= n * hkv * 2) return;
+    const int is_v = (int)(item & 1);
+    const int64_t row = item >> 1, token = row / hkv;
+    const int32_t h = (int32_t)(row - token * hkv);
+    const int64_t slot = slots[token];
+    if (slot < 0) return;
+    const int64_t blk = slot / bs;
+    quantize_row((is_v ? v : k) + row * hd, hd, (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd,
+                 (is_v ? v_scales : k_scales) + (blk * hkv + h) * bs + (slot - blk * bs), lane);
+}
+
+// The generation step's quantizing write: sequence s's new rows k_new[s],
+// v_new[s] go to the slot of position context_lens[s] - 1 (length-0
+// sequences are skipped).
+template <typename T>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    append_kv_fp8_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
+                         const int32_t* __restrict__ block_tables, int32_t max_blocks,
+                         const int32_t* __restrict__ context_lens, int32_t num_seqs, int32_t hkv, int32_t hd,
+                         int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                         float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;
+    if (item >= (int64_t)num_seqs * hkv * 2) return;
+    const int is_v = (int)(item & 1);
+    const int64_t row = item >> 1, s = row / hkv;
+    const int32_t h = (int32_t)(row - s * hkv);
+    const int32_t L = context_lens[s];
+    if (L <= 0) return;
+    const int64_t pos = L - 1, logical = pos / bs, off = pos - logical * bs;
+    const int64_t blk = block_tables[s * max_blocks + logical], slot = blk * bs + off;
+    quantize_row((is_v ? v_new : k_new) + row * hd, hd, (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd,
+                 (is_v ? v_scales : k_scales) + (blk * hkv + h) * bs + off, lane);
 }
 
 // One CTA per (pair, layer); its threads stride over the K and V blocks.
@@ -260,6 +291,26 @@ cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const i
         default: PA_QW(__half); break;
     }
 #undef PA_QW
+    return cudaGetLastError();
+}
+
+cudaError_t launch_append_kv_fp8(const void* k_new, const void* v_new, int dtype, const int32_t* block_tables,
+                                 int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
+                                 uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream) {
+    if (num_seqs == 0) return cudaSuccess;
+    const int64_t rows = (int64_t)num_seqs * num_kv_heads * 2;
+    const unsigned blocks = (unsigned)((rows + kQuantWarps - 1) / kQuantWarps);
+#define PA_QA(T)                                                                                              \
+    append_kv_fp8_kernel<T><<<blocks, kQuantWarps * 32, 0, stream>>>(                                       \
+        static_cast<const T*>(k_new), static_cast<const T*>(v_new), block_tables, max_blocks, context_lens,  \
+        num_seqs, num_kv_heads, head_dim, block_size, k_codes, v_codes, k_scales, v_scales)
+    switch (dtype) {
+        case 0: PA_QA(float); break;
+        case 1: PA_QA(__nv_bfloat16); break;
+        default: PA_QA(__half); break;
+    }
+#undef PA_QA
     return cudaGetLastError();
 }
 

@@ -20,11 +20,12 @@
 //    a fixed order ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
 //    apart and merged by the online-softmax rule).  The cut depends only on
 //    the lengths, never on physical block ids.
-//  * Each warp runs its own R-deep ring of shared-memory stages.  One lane
-//    issues TMA tile loads (cp.async.bulk.tensor, 128-byte swizzle) of the
-//    K and V tiles of a 16-token block -- rows of one KV head, gathered
-//    through the block table -- completing on an mbarrier; block-table
-//    entries for the next 64 blocks sit in registers.
+//  * Each warp runs its own R-deep ring of shared-memory stages (one or two
+//    16-token tiles each).  Several lanes issue, in one instruction, the TMA
+//    loads (cp.async.bulk.tensor, 128-byte swizzle) of a stage's K and V
+//    boxes -- rows of one KV head, gathered through the block table --
+//    completing on the stage's mbarrier; block-table entries for the next
+//    64 tiles sit in registers.
 //  * The G query heads of the unit are packed as the N side of
 //    mma.m16n8k16 (padded to 8 or 16): S^T = K Q^T with the 16 tokens as M,
 //    so each K/V byte is read once for the whole group; the fp32 scores get
@@ -45,11 +46,14 @@
 //    k-step (keys) and m-tile (values) is permuted -- consistently on both
 //    operands, since a dot product does not depend on its order -- so every
 //    lane reads contiguous 16-byte pieces of the staged codes.
-//  * Append mode fuses the generation step: the warp that owns a unit's
-//    last block patches the new token's K/V row (prefetched from the inputs)
-//    into the staged tile before its MMAs and stores the same row to the pool
-//    at slot = table[(L-1) / 16] * 16 + (L-1) % 16 ("分页 KV Cache", §块表与
+//  * Append mode fuses the generation step: the warp that owns a unit's last
+//    block patches the new token's K/V row (prefetched from the inputs) into
+//    the staged tile before its MMAs and stores the same row to the pool at
+//    slot = table[(L-1) / bs] * bs + (L-1) % bs ("分页 KV Cache", §块表与
 //    slot mapping) -- slot translation, write and attention in one launch.
+//    With a code cache (head_dim 128) the new rows are quantized in the
+//    kernel exactly as the quantizing write does, codes and scale going to
+//    the pool and to the staged tile.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp8.h>
@@ -98,24 +102,32 @@ struct TcParams {
     const float* v_scales;
 };
 
+// Warps per CTA, stages per warp, 16-token tiles per stage, and CTAs per SM
+// the register budget is sized for (__launch_bounds__).  A stage of about
+// 8 KB keeps the per-stage costs (barrier round trip, copy issue) small
+// against the bytes it brings: 16-bit head_dim-128 tiles are 8 KB, code
+// tiles half that, so code stages hold two tiles.  The code path is bound
+// by its per-tile conversion chain rather than by memory, so it runs three
+// CTAs (12 warps) per SM on two stages each (measured: 12 warps beat 8 and
+// 16 on the 64-sequence GQA batch).
+template <int HD, bool FP8> struct Pipe;
+template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6, TPS = 1, MINB = 1; };
+template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3, TPS = 1, MINB = 1; };
+template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3, TPS = 1, MINB = 1; };
+template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 2, TPS = 2, MINB = 3; };
+template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3, TPS = 1, MINB = 1; };
+
 template <int HD, bool FP8>
 struct Geo {
     static constexpr int ELT = FP8 ? 1 : 2;     // bytes per cached element
     static constexpr int CH = HD * ELT / 128;   // 128-byte chunks in one head's row
     static constexpr int TILE = BS * HD * ELT;  // bytes of a K (or V) tile
-    static constexpr int STAGE = 2 * TILE;      // K tile then V tile
-    static constexpr int SCL = FP8 ? 2 * BS * 4 : 0;  // a stage's 16 K then 16 V scales
-    static constexpr int KS = HD / 16;          // k-steps of K Q^T == m-tiles of V^T P^T
+    static constexpr int TPS = Pipe<HD, FP8>::TPS;
+    static constexpr int STAGE = TPS * 2 * TILE;  // per tile: K tile then V tile
+    static constexpr int TSCL = FP8 ? 2 * BS : 0;  // floats per tile: 16 K then 16 V scales
+    static constexpr int SCL = TPS * TSCL * 4;     // scale bytes of a stage
+    static constexpr int KS = HD / 16;           // k-steps of K Q^T == m-tiles of V^T P^T
 };
-
-// Warps per CTA, stages per warp, and CTAs per SM the register budget is
-// sized for (__launch_bounds__).
-template <int HD, bool FP8> struct Pipe;
-template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6, MINB = 1; };
-template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3, MINB = 1; };
-template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3, MINB = 1; };
-template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 6, MINB = 1; };
-template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3, MINB = 1; };
 
 template <int HD, bool FP8>
 constexpr size_t smem_bytes(int num_seqs) {
@@ -253,41 +265,8 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     int win = 0, ip = 0;
     int is_, ih, ib;
     locate(f0, is_, ih, ib);
-    auto issue_next = [&]() {
-        const int w = ip >> 5;
-        if (w != win) {
-            tbl_cur = tbl_next;
-            tbl_cur2 = tbl_next2;
-            tbl_next = table_entry((int64_t)(w + 1) * 32 + lane, tbl_next2);
-            win = w;
-        }
-        const int32_t row = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
-        const int32_t row2 = __shfl_sync(0xffffffffu, tbl_cur2, ip & 31);
-        const int slot = ip % R;
-        // The stage's copies go out from several lanes in one instruction
-        // (a TMA unit takes lane-parallel copies faster than a sequence of
-        // copies from one thread): lanes [0, nbox) each load one 128-byte x
-        // 16-row (or 8-row) box of K or V, the next lanes the K and V scales.
-        const int halves = bsz == 8 ? 2 : 1;  // 8-token blocks: two 8-row boxes per chunk
-        const int nbox = Gm::CH * 2 * halves;
-        const int nops = nbox + (FP8 ? 2 * halves : 0);
-        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], Gm::STAGE + Gm::SCL);
-        if (lane < nops) {
-            fence_proxy_async_smem();
-            if (lane < nbox) {
-                const int hf = lane % halves, c = (lane / halves) % Gm::CH, is_v = lane / (halves * Gm::CH);
-                uint8_t* dst = wst + (size_t)slot * Gm::STAGE + is_v * Gm::TILE + c * BS * 128 + hf * 1024;
-                tma_load_3d(dst, is_v ? &tmV : &tmK, &wbar[slot], 0, ih * Gm::CH + c, hf ? row2 : row, pol);
-            } else if constexpr (FP8) {
-                // scales of pool row r for KV head ih: [r / bs][ih][r % bs]
-                const int o = lane - nbox, hf = o % halves, is_v = o / halves;
-                const int32_t r = hf ? row2 : row;
-                const int64_t si = (int64_t)(r / bsz) * Hkv * bsz + (int64_t)ih * bsz + r % bsz;
-                float* sd = wscl + slot * (Gm::SCL / 4) + is_v * BS + hf * 8;
-                bulk_load(sd, (is_v ? p.v_scales : p.k_scales) + si, halves == 2 ? 32 : 64, &wbar[slot]);
-            }
-        }
-        ++ip;
+    // advance the issue cursor by one tile
+    auto advance = [&]() {
         if (++ib == prefix[is_ + 1] - prefix[is_]) {
             ib = 0;
             if (++ih == Hkv) {
@@ -298,7 +277,59 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
             }
         }
     };
-    for (int r = 0; r < R && r < n; ++r) issue_next();
+    constexpr int TPS = Gm::TPS;
+    static_assert(TPS == 1 || TPS == 2, "a stage holds one or two tiles");
+    // Issue one stage: tiles ip .. ip+TPS-1 that exist (ip is a multiple of
+    // TPS, so they share one 32-tile table window).
+    auto issue_next = [&]() {
+        const int w = ip >> 5;
+        if (w != win) {
+            tbl_cur = tbl_next;
+            tbl_cur2 = tbl_next2;
+            tbl_next = table_entry((int64_t)(w + 1) * 32 + lane, tbl_next2);
+            win = w;
+        }
+        const int nt_stage = min(TPS, n - ip);
+        const int32_t row0 = __shfl_sync(0xffffffffu, tbl_cur, ip & 31);
+        const int32_t row20 = __shfl_sync(0xffffffffu, tbl_cur2, ip & 31);
+        const int32_t row1 = TPS > 1 ? __shfl_sync(0xffffffffu, tbl_cur, (ip + 1) & 31) : 0;
+        const int32_t row21 = TPS > 1 ? __shfl_sync(0xffffffffu, tbl_cur2, (ip + 1) & 31) : 0;
+        const int ih0 = ih;
+        advance();
+        const int ih1 = ih;
+        if (TPS > 1 && nt_stage > 1) advance();
+        const int slot = (ip / TPS) % R;
+        // The stage's copies go out from several lanes in one instruction
+        // (a TMA unit takes lane-parallel copies faster than a sequence of
+        // copies from one thread): per tile, nbox lanes each load one
+        // 128-byte x 16-row (or 8-row) box of K or V, and (code tiles) the
+        // next lanes its K and V scales.
+        const int halves = bsz == 8 ? 2 : 1;  // 8-token blocks: two 8-row boxes per chunk
+        const int nbox = Gm::CH * 2 * halves;
+        const int per = nbox + (FP8 ? 2 * halves : 0);
+        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], nt_stage * (2 * Gm::TILE + Gm::TSCL * 4));
+        const int j = lane / per, o = lane - j * per;
+        if (j < nt_stage) {
+            const int32_t row = j ? row1 : row0, row2 = j ? row21 : row20;
+            const int ihj = j ? ih1 : ih0;
+            fence_proxy_async_smem();
+            if (o < nbox) {
+                const int hf = o % halves, c = (o / halves) % Gm::CH, is_v = o / (halves * Gm::CH);
+                uint8_t* dst = wst + (size_t)slot * Gm::STAGE + j * 2 * Gm::TILE + is_v * Gm::TILE + c * BS * 128 +
+                               hf * 1024;
+                tma_load_3d(dst, is_v ? &tmV : &tmK, &wbar[slot], 0, ihj * Gm::CH + c, hf ? row2 : row, pol);
+            } else if constexpr (FP8) {
+                // scales of pool row r for KV head ihj: [r / bs][ihj][r % bs]
+                const int q = o - nbox, hf = q % halves, is_v = q / halves;
+                const int32_t r = hf ? row2 : row;
+                const int64_t si = (int64_t)(r / bsz) * Hkv * bsz + (int64_t)ihj * bsz + r % bsz;
+                float* sd = wscl + slot * (Gm::SCL / 4) + j * Gm::TSCL + is_v * BS + hf * 8;
+                bulk_load(sd, (is_v ? p.v_scales : p.k_scales) + si, halves == 2 ? 32 : 64, &wbar[slot]);
+            }
+        }
+        ip += nt_stage;
+    };
+    for (int r = 0; r < R && ip < n; ++r) issue_next();
 
     // ---- consumer side
     const int g = lane >> 2, c4 = lane & 3;
@@ -366,7 +397,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
         }
-        if (!FP8 && p.k_new != nullptr) {
+        if (p.k_new != nullptr) {
 #pragma unroll
             for (int k = 0; k < NPC; ++k) {
                 const int i = lane + 32 * k;
@@ -503,13 +534,14 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     begin_unit();
     const uint32_t st0 = smem_u32(wst);
     for (int i = 0; i < n; ++i) {
-        const int slot = i % R;
-        if (!mbar_wait_bounded(&wbar[slot], (uint32_t)(i / R) & 1u, kMaxPolls)) {
+        const int stg = i / TPS, sub = i - stg * TPS, slot = stg % R;
+        if (sub == 0 && !mbar_wait_bounded(&wbar[slot], (uint32_t)(stg / R) & 1u, kMaxPolls)) {
             if (lane == 0) atomicOr(&g_decode_status, kStatusTimeout);
-            for (int j = i + 1; j < ip; ++j) mbar_wait_bounded(&wbar[j % R], (uint32_t)(j / R) & 1u, kMaxPolls);
+            for (int sj = stg + 1; sj * TPS < ip; ++sj)
+                mbar_wait_bounded(&wbar[sj % R], (uint32_t)(sj / R) & 1u, kMaxPolls);
             return;
         }
-        const uint32_t kt = st0 + (uint32_t)slot * Gm::STAGE, vt = kt + Gm::TILE;
+        const uint32_t kt = st0 + (uint32_t)slot * Gm::STAGE + sub * 2 * Gm::TILE, vt = kt + Gm::TILE;
         const int valid = min(BS, Lcur - cb * BS);
         if (!FP8 && p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
             // the new token: into the staged tiles (its attention input) and the pool
@@ -529,6 +561,46 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 }
             }
             __syncwarp();
+        }
+        if constexpr (FP8 && HD == 128) {
+            if (p.k_new != nullptr && cb == prefix[cs + 1] - prefix[cs] - 1) {
+                // the new token, quantized as the quantizing write does it
+                // (scale = max|x| / 448, code = E4M3(x / scale)): lanes 0-15
+                // hold 8 elements each of the K row, lanes 16-31 of the V
+                // row; codes and scale go to the pool and the staged tile.
+                static_assert(NPC == 1 && PPT == 16, "one 16-byte piece of the new rows per lane");
+                const int r = valid - 1, j = lane & 15, is_v = lane >> 4;
+                const int64_t off = (Lcur - 1) % bsz, slot_row = (int64_t)last_phys * bsz + off;
+                float x[8], amax = 0.f;
+                const uint32_t w4[4] = {newp[0].x, newp[0].y, newp[0].z, newp[0].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const T lo = *reinterpret_cast<const T*>(&w4[e]);
+                    const T hi = *(reinterpret_cast<const T*>(&w4[e]) + 1);
+                    x[2 * e] = Elt<T>::to_f(lo);
+                    x[2 * e + 1] = Elt<T>::to_f(hi);
+                    amax = fmaxf(amax, fmaxf(fabsf(x[2 * e]), fabsf(x[2 * e + 1])));
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sq = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+                uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    cw[e >> 2] |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[e], sq), __NV_SATFINITE, __NV_E4M3)
+                                  << (8 * (e & 3));
+                uint8_t* pool = static_cast<uint8_t*>(is_v ? p.v_pool : p.k_pool);
+                *reinterpret_cast<uint2*>(pool + (slot_row * Hkv + ch) * HD + 8 * j) = make_uint2(cw[0], cw[1]);
+                const int b = 8 * j;
+                const uint32_t dst = (is_v ? vt : kt) + r * 128 + ((((b & 127) >> 4) ^ (r & 7)) << 4) + (b & 15);
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(dst), "r"(cw[0]), "r"(cw[1]) : "memory");
+                if (j == 0) {
+                    float* sp = const_cast<float*>(is_v ? p.v_scales : p.k_scales);
+                    sp[((int64_t)last_phys * Hkv + ch) * bsz + off] = sq;
+                    wscl[slot * (Gm::SCL / 4) + sub * Gm::TSCL + is_v * BS + r] = sq;
+                }
+                __syncwarp();
+            }
         }
 
         // S^T = K Q^T : 16 tokens x (8 NT) heads, fp32
@@ -572,7 +644,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
         // score multipliers of rows g, g+8 and (quantized cache) value scales
         float sm0 = p.scale_log2, sm1 = p.scale_log2, vs0 = 1.f, vs1 = 1.f;
         if constexpr (FP8) {
-            const float* ss = wscl + slot * (Gm::SCL / 4);
+            const float* ss = wscl + slot * (Gm::SCL / 4) + sub * Gm::TSCL;
             sm0 = ss[g];
             sm1 = ss[g + 8];
             vs0 = ok0 ? ss[BS + g] : 0.f;  // a slot past the context may hold anything
@@ -599,12 +671,16 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
             const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
             lrow[nt][0] = fmaf(lrow[nt][0], al0, p0 + p2);
             lrow[nt][1] = fmaf(lrow[nt][1], al1, p1 + p3);
+            // rescale O only when some row's maximum grew (after the first
+            // few tiles it rarely does; the vote is warp-uniform)
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                acc[mt][nt][0] *= al0;
-                acc[mt][nt][1] *= al1;
-                acc[mt][nt][2] *= al0;
-                acc[mt][nt][3] *= al1;
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][nt][0] *= al0;
+                    acc[mt][nt][1] *= al1;
+                    acc[mt][nt][2] *= al0;
+                    acc[mt][nt][3] *= al1;
+                }
             }
             if constexpr (FP8) {
                 pb[nt][0] = movm_t(pack2<__half>(p0 * vs0, p1 * vs0));
@@ -643,8 +719,14 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 const uint32_t w0 = (&vw[0][wi >> 2].x)[wi & 3], w1 = (&vw[1][wi >> 2].x)[wi & 3];
                 const uint32_t w8 = (&vw[2][wi >> 2].x)[wi & 3], w9 = (&vw[3][wi >> 2].x)[wi & 3];
                 const uint32_t lo = __byte_perm(w0, w1, sel), hi = __byte_perm(w8, w9, sel);
-                const uint32_t a0 = e4m3x2_to_f16x2(lo) & m01, a1 = e4m3x2_to_f16x2(lo >> 16) & m01;
-                const uint32_t a2 = e4m3x2_to_f16x2(hi) & m23, a3 = e4m3x2_to_f16x2(hi >> 16) & m23;
+                uint32_t a0 = e4m3x2_to_f16x2(lo), a1 = e4m3x2_to_f16x2(lo >> 16);
+                uint32_t a2 = e4m3x2_to_f16x2(hi), a3 = e4m3x2_to_f16x2(hi >> 16);
+                if (valid < BS) {
+                    a0 &= m01;
+                    a1 &= m01;
+                    a2 &= m23;
+                    a3 &= m23;
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                     mma16816<__half>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
@@ -654,16 +736,18 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
             for (int mt = 0; mt < KS; ++mt) {
                 uint32_t a0, a1, a2, a3;
                 ldsm_x4_t(vt + swz(v_tok, mt * 16 + v_dof), a0, a1, a2, a3);
-                a0 &= m01;
-                a1 &= m01;
-                a2 &= m23;
-                a3 &= m23;
+                if (valid < BS) {
+                    a0 &= m01;
+                    a1 &= m01;
+                    a2 &= m23;
+                    a3 &= m23;
+                }
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
             }
         }
         __syncwarp();
-        if (ip < n) issue_next();
+        if ((sub == TPS - 1 || i == n - 1) && ip < n) issue_next();
 
         const int nb = prefix[cs + 1] - prefix[cs];
         ++cb;

@@ -48,6 +48,12 @@ cudaError_t launch_swap_blocks(void* const* src_k, void* const* src_v, void* con
 cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
                                 uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream);
+// The same for the generation step: sequence s's new rows go to the slot of
+// position context_lens[s] - 1.
+cudaError_t launch_append_kv_fp8(const void* k_new, const void* v_new, int dtype, const int32_t* block_tables,
+                                 int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs,
+                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
+                                 uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
                                const int64_t* block_pairs, int32_t num_pairs, int64_t block_bytes,
                                cudaStream_t stream);

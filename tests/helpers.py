@@ -118,9 +118,9 @@ def oracle_fp8_caches(w):
     return kc, vc, ks, vs
 
 
-def device_fp8_caches(w, dev):
+def device_fp8_caches(w, dev, after_step=True):
     """The same pools built on the device through pa_slot_mapping and
-    pa_write_kv_fp8."""
+    pa_write_kv_fp8 (without the step's new rows unless after_step)."""
     import torch
     import paged_kv_cache_116_gb300 as pa
 
@@ -136,9 +136,10 @@ def device_fp8_caches(w, dev):
                                    torch.from_numpy(w.pre_seq_idx).to(dev), torch.from_numpy(w.pre_pos).to(dev),
                                    w.block_size)
         pa.pa_write_kv_fp8(w.pre_k.to(dev), w.pre_v.to(dev), slots, kc, vc, ks, vs)
-    slots = pa.pa_slot_mapping(bt, torch.from_numpy(w.new_seq_idx).to(dev), torch.from_numpy(w.new_pos).to(dev),
-                               w.block_size)
-    pa.pa_write_kv_fp8(w.new_k.to(dev), w.new_v.to(dev), slots, kc, vc, ks, vs)
+    if after_step:
+        slots = pa.pa_slot_mapping(bt, torch.from_numpy(w.new_seq_idx).to(dev), torch.from_numpy(w.new_pos).to(dev),
+                                   w.block_size)
+        pa.pa_write_kv_fp8(w.new_k.to(dev), w.new_v.to(dev), slots, kc, vc, ks, vs)
     return kc, vc, ks, vs, bt
 
 

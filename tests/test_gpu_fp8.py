@@ -275,3 +275,63 @@ def test_graph_replays_of_fp8_decode_follow_new_queries(pa):
     graph_replays_match_eager(
         lambda out, q, ws: pa.pa_decode_fp8(out, q, kc, vc, ks, vs, bt, lens, mc, w.scale, workspace=ws),
         w.q.to(DEV).clone(), DEV)
+
+
+# ---------------------------------------------------------------- the generation step over a quantized cache
+
+APPEND_FP8_CASES = [
+    ("gqa24_bf16", lambda: W.decode_workload("ap8_gqa", "bf16", 16, 32, 8, 128, W.gqa_batch_lengths(24), seed=61)),
+    ("mha_f16", lambda: W.decode_workload("ap8_mha", "f16", 16, 8, 8, 128, [1, 16, 17, 300, 33], std=0.5, seed=62)),
+    ("g12_bs8", lambda: W.decode_workload("ap8_g12", "bf16", 8, 24, 2, 128, [1, 7, 8, 9, 47, 129], seed=63)),
+    ("bs32", lambda: W.decode_workload("ap8_bs32", "bf16", 32, 8, 2, 128, [1, 31, 32, 33, 100], seed=64)),
+    ("hd256", lambda: W.decode_workload("ap8_256", "bf16", 16, 8, 2, 256, [5, 64, 200], seed=65)),
+    ("hd64", lambda: W.decode_workload("ap8_64", "f16", 16, 8, 2, 64, [3, 40], seed=66)),
+    ("tiny_f32", lambda: W.tiny_decode()),
+]
+
+
+@pytest.mark.parametrize("name,make", APPEND_FP8_CASES)
+@pytest.mark.parametrize("kernel", [0, 1])
+def test_decode_append_fp8_equals_quantizing_write_then_decode(pa, name, make, kernel):
+    """One call quantizes each sequence's new token into the slot of position
+    L-1 and attends: the code and scale pools must equal the oracle's after
+    its quantizing write (bit for bit, untouched slots included) and the
+    output must match the oracle's attention over them."""
+    w = make()
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV, after_step=False)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, kernel)
+    try:
+        ws_bytes = pa.pa_decode_fp8_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                   w.block_size, mc, W.TORCH_DTYPES[w.dtype])
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype],
+                         device=DEV)
+        pa.pa_decode_append_fp8(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc,
+                                vc, ks, vs, bt, lens, mc, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_DECODE_KERNEL, 0)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    compare(w, out, oracle_fp8_attention(w, *opools))
+
+
+def test_decode_append_fp8_zero_length_sequence(pa):
+    w = W.decode_workload("ap8_z", "bf16", 16, 8, 2, 128, [5, 1, 40], seed=67)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV, after_step=False)
+    before = [t.clone() for t in (kc, vc, ks, vs)]
+    lens0 = torch.tensor([5, 0, 40], dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(pa.pa_decode_fp8_workspace_size(3, 8, 2, 128, 16, 40, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.full((3, 8, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    pa.pa_decode_append_fp8(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc, vc, ks,
+                            vs, bt, lens0, 40, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out[1]).item() == 0
+    # sequence 1 wrote nothing: its block (and every other untouched slot) is as before
+    blk = int(w.block_tables[1, 0])
+    assert torch.equal(kc[blk], before[0][blk]) and torch.equal(ks[blk].view(torch.int32),
+                                                                before[2][blk].view(torch.int32))
