@@ -533,7 +533,10 @@ def main():
 
     tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in ((128, 256) if fp8 else (64, 128, 256)) and
                  hq // hkv <= 16 and (bs == 8 or (bs % 16 == 0 and bs <= 256)))
-    fused_in_kernel = tc_decode and (not fp8 or hd == 128)  # the append happens inside the decode kernel
+    # the append happens inside the decode kernel (a code cache: head_dim 128 and
+    # no more (sequence, KV head) units than the grid's warps, 3 CTAs x 4 warps per SM)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fused_in_kernel = tc_decode and (not fp8 or (hd == 128 and S * hkv <= sms * 3 * 4))
     launches_per_step = (1 if fused_in_kernel else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):

@@ -431,10 +431,22 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
     pa_status sel;
     const bool tc = use_decode_tc(dtype, head_dim, block_size, G, fp8, &sel);
     if (sel != PA_OK) return sel;
-    // The tensor-core kernel fuses the append for 16-bit caches and for code
-    // caches of head_dim 128; otherwise the new rows are written (quantized
-    // for a code cache) by a separate kernel first, then attended from the pool.
-    const bool fused_append = append && tc && (!fp8 || head_dim == 128);
+    // The tensor-core kernel fuses the append for 16-bit caches, and for code
+    // caches of head_dim 128 when the batch has no more (sequence, KV head)
+    // units than the grid has warps: quantizing inside the kernel costs the
+    // warp that owns a unit's last tile some microseconds (measured: a gain
+    // with 512 units on 1,824 warps, a loss with 5,120), while a separate
+    // quantizing kernel spreads the rows over the whole GPU.  Otherwise the
+    // new rows are written (quantized for a code cache) by a separate kernel
+    // first, then attended from the pool; either way the pool and the output
+    // are the same bit for bit.
+    bool fused_append = append && tc && (!fp8 || head_dim == 128);
+    if (fused_append && fp8) {
+        const int64_t warps = (int64_t)pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context,
+                                                          dtype, G, g_options[PA_OPT_DECODE_CTAS], fp8) *
+                              pa::decode_tc_warps_per_cta(head_dim, fp8);
+        fused_append = (int64_t)num_seqs * num_kv_heads <= warps;
+    }
     if (append && !fused_append) {
         cudaError_t e = fp8 ? pa::launch_append_kv_fp8(k_new, v_new, dtype, block_tables, max_blocks, context_lens,
                                                        num_seqs, num_kv_heads, head_dim, block_size,

@@ -133,7 +133,7 @@ template <int HD, bool FP8>
 constexpr size_t smem_bytes(int num_seqs) {
     return 1024 /* alignment slack */ +
            (size_t)Pipe<HD, FP8>::NW * Pipe<HD, FP8>::R * (Geo<HD, FP8>::STAGE + Geo<HD, FP8>::SCL + 8) +
-           (size_t)(num_seqs + 1) * 4;
+           (size_t)(num_seqs + 1) * 4 + (size_t)num_seqs * 4;
 }
 
 // Two E4M3 codes (low byte first) -> two f16 values (low half first), exact.
@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     float* scl = reinterpret_cast<float*>(base + (size_t)NW * R * Gm::STAGE);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * (Gm::STAGE + Gm::SCL));
     int32_t* prefix = reinterpret_cast<int32_t*>(bars + NW * R);
+    int32_t* lens = prefix + p.num_seqs + 1;  // context lengths, read once per CTA
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
@@ -178,6 +179,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     // ---- blocks per sequence and their exclusive prefix
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
         const int L = p.context_lens[s];
+        lens[s] = L;
         prefix[s + 1] = L > 0 ? (L + BS - 1) / BS : 0;
     }
     if (threadIdx.x == 0) prefix[0] = 0;
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
         locate(f0 + rel, s, h, t);
         const int32_t* tb = p.block_tables + (int64_t)s * p.max_blocks;
         if (bsz == 8) {
-            const int nb8 = (p.context_lens[s] + 7) >> 3;
+            const int nb8 = (lens[s] + 7) >> 3;
             const int32_t r1 = tb[2 * t] * 8;
             row2 = 2 * t + 1 < nb8 ? tb[2 * t + 1] * 8 : r1;
             return r1;
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 
     int cs, ch, cb;
     locate(f0, cs, ch, cb);
-    int seg_b0 = cb, Lcur = p.context_lens[cs];
+    int seg_b0 = cb, Lcur = lens[cs];
     bool first_seg = true;
     const T* qbase = static_cast<const T*>(p.q);
 
@@ -366,6 +368,20 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     // dims kb0 + 4kk + 2, +3), and head dims [g HD/8, (g+1) HD/8) of value
     // rows 2c4, 2c4+1, 2c4+8, 2c4+9 (m-tile mt, row g + 8hi: dim vb0 + 2mt + hi).
     const int kb0 = c4 * (HD / 4), vb0 = g * (HD / 8);
+
+    // the new token's K/V rows of unit (cs, ch), and the pool block of position L-1
+    auto load_new_rows = [&]() {
+#pragma unroll
+        for (int k = 0; k < NPC; ++k) {
+            const int i = lane + 32 * k;
+            if (i < 2 * PPT) {
+                const uint8_t* src = static_cast<const uint8_t*>(i < PPT ? p.k_new : p.v_new) +
+                                     ((int64_t)cs * Hkv + ch) * HD * 2 + (i % PPT) * 16;
+                newp[k] = *reinterpret_cast<const uint4*>(src);
+            }
+        }
+        last_phys = p.block_tables[(int64_t)cs * p.max_blocks + (lens[cs] - 1) / bsz];
+    };
 
     auto begin_unit = [&]() {
 #pragma unroll
@@ -397,18 +413,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
         }
-        if (p.k_new != nullptr) {
-#pragma unroll
-            for (int k = 0; k < NPC; ++k) {
-                const int i = lane + 32 * k;
-                if (i < 2 * PPT) {
-                    const uint8_t* src = static_cast<const uint8_t*>(i < PPT ? p.k_new : p.v_new) +
-                                         ((int64_t)cs * Hkv + ch) * HD * 2 + (i % PPT) * 16;
-                    newp[k] = *reinterpret_cast<const uint4*>(src);
-                }
-            }
-            last_phys = p.block_tables[(int64_t)cs * p.max_blocks + (p.context_lens[cs] - 1) / bsz];
-        }
+        if (p.k_new != nullptr) load_new_rows();
     };
 
     // Combine the partial records of unit (cs, ch) held by warps w0..w1, in
@@ -763,7 +768,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                     do {
                         ++cs;
                     } while (cs < S && prefix[cs + 1] == prefix[cs]);
-                    Lcur = p.context_lens[cs];
+                    Lcur = lens[cs];
                 }
                 begin_unit();
             }
@@ -950,12 +955,15 @@ int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int
 #undef PA_KFN
 }
 
+int decode_tc_warps_per_cta(int32_t head_dim, bool kv_fp8) {
+    if (kv_fp8) return head_dim == 256 ? Pipe<256, true>::NW : Pipe<128, true>::NW;
+    return head_dim == 256 ? Pipe<256, false>::NW : (head_dim == 128 ? Pipe<128, false>::NW : Pipe<64, false>::NW);
+}
+
 size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
                            bool kv_fp8) {
     const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
-    int nw;
-    if (kv_fp8) nw = head_dim == 256 ? Pipe<256, true>::NW : Pipe<128, true>::NW;
-    else nw = head_dim == 256 ? Pipe<256, false>::NW : (head_dim == 128 ? Pipe<128, false>::NW : Pipe<64, false>::NW);
+    const int nw = decode_tc_warps_per_cta(head_dim, kv_fp8);
     const size_t cnt_bytes = ((size_t)s * num_kv_heads * 8 + 255) & ~(size_t)255;
     return cnt_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
 }

@@ -98,6 +98,7 @@ bool decode_tc_supported(int dtype, int head_dim, int block_size, int group, boo
 // Grid size (CTAs) the launch will use for this problem on the current device.
 int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                    int32_t max_context, int dtype, int32_t group, int64_t ctas_override, bool kv_fp8 = false);
+int decode_tc_warps_per_cta(int32_t head_dim, bool kv_fp8 = false);
 size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
                            bool kv_fp8 = false);
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,

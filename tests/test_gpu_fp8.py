@@ -335,3 +335,27 @@ def test_decode_append_fp8_zero_length_sequence(pa):
     blk = int(w.block_tables[1, 0])
     assert torch.equal(kc[blk], before[0][blk]) and torch.equal(ks[blk].view(torch.int32),
                                                                 before[2][blk].view(torch.int32))
+
+
+@pytest.mark.parametrize("ctas", [1, 5, 37, 200])
+def test_decode_append_fp8_any_split(pa, ctas):
+    """The fused step with the batch cut at many places: whichever warp ends
+    up owning a unit's last tile quantizes and writes the new rows."""
+    w = W.decode_workload("ap8_split", "bf16", 16, 16, 4, 128, [1, 2, 3, 4, 5, 40, 47, 48, 49, 300, 1000], seed=71)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV, after_step=False)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, ctas)
+    try:
+        ws = torch.empty(max(pa.pa_decode_fp8_workspace_size(w.num_seqs, 16, 4, 128, 16, mc, torch.bfloat16), 16),
+                         dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, 16, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        pa.pa_decode_append_fp8(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc,
+                                vc, ks, vs, bt, lens, mc, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, 0)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    compare(w, out, oracle_fp8_attention(w, *opools))
