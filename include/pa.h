@@ -150,9 +150,9 @@ PA_API pa_status pa_write_kv(const void* k, const void* v, const int64_t* slot_m
  * scales a decode tile needs are contiguous.  A negative slot skips token i;
  * slots must be distinct (check mode rejects duplicates and out-of-pool
  * slots).  Bit-exact against that definition.
- *   k, v:              device [n, num_kv_heads, head_dim] of dtype (PA_F32/BF16/F16)
+ *   k, v:              device [n, num_kv_heads, head_dim] of dtype (PA_F32/BF16/F16), 16-byte aligned
  *   slot_mapping:      device int64 [n]
- *   k_codes, v_codes:  device uint8 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_codes, v_codes:  device uint8 [num_blocks, block_size, num_kv_heads, head_dim], 16-byte aligned
  *   k_scales, v_scales: device fp32 [num_blocks, num_kv_heads, block_size]
  * head_dim <= 256.
  */

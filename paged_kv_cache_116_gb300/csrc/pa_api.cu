@@ -212,6 +212,8 @@ pa_status pa_write_kv_fp8(const void* k, const void* v, const int64_t* slot_mapp
     if (n == 0) return PA_OK;
     if (!k || !v || !slot_mapping || !k_codes || !v_codes || !k_scales || !v_scales)
         return fail(PA_ERR_INVALID_ARG, "null pointer");
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_codes) || !aligned16(v_codes))
+        return fail(PA_ERR_INVALID_ARG, "k, v and the code pools must be 16-byte aligned");
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
         pa_status err = check_slots(slot_mapping, n, num_blocks, block_size, st);

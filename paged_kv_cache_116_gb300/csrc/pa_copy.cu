@@ -7,6 +7,8 @@
 // or a whole CTA per block pair, so every warp instruction touches whole
 // 32-byte sectors.
 #include <cuda_fp8.h>
+
+#include <algorithm>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -83,79 +85,184 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
     for (int64_t e = lane; e < row_vecs; e += 32) dst[e] = ld_nc_v4(src + e);
 }
 
-// Quantizing write: one warp per (token, KV head, K|V) row of head_dim <=
-// 256 elements.  scale = max|x| / 448 (1 for an all-zero row), code =
+// Quantizing write.  scale = max|x| / 448 (1 for an all-zero row), code =
 // E4M3(x / scale), nearest with ties to even, held at +-448; the division
-// and maximum in fp32 (IEEE).  The codes go to the row's slot of the code
-// pool, the scale to [slot / block_size][head][slot % block_size].
+// and maximum in fp32 (IEEE).  A row's codes go to its slot of the code pool,
+// its scale to [slot / block_size][head][slot % block_size].  Rows are
+// (token or sequence, KV head, K|V), numbered item = row * 2 + is_v with
+// row = t * hkv + h.
 constexpr int kQuantWarps = 8;
+constexpr int kQuantMaxCtas = 4096;
 
-// One warp quantizes one row of hd <= 256 elements (src in T) into codes at
-// dst and its scale at *scale.
-template <typename T>
-__device__ __forceinline__ void quantize_row(const T* __restrict__ src, int32_t hd, uint8_t* __restrict__ dst,
-                                             float* __restrict__ scale, int lane) {
-    float x[8], amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int d = lane + 32 * j;
-        x[j] = d < hd ? Elt<T>::to_f(src[d]) : 0.f;
-        amax = fmaxf(amax, fabsf(x[j]));
+// Where row `item` goes: the element source, the code destination and the
+// scale slot; false for a skipped token (negative slot, or length 0).
+struct QuantDst {
+    int64_t src_row;
+    uint8_t* codes;
+    float* scale;
+};
+struct SlotRows {  // pa_write_kv_fp8: slots given per token
+    const int64_t* slots;
+    __device__ bool slot_of(int64_t t, int32_t bs, int64_t& blk, int64_t& off) const {
+        const int64_t slot = slots[t];
+        if (slot < 0) return false;
+        blk = slot / bs;
+        off = slot - blk * bs;
+        return true;
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int d = lane + 32 * j;
-        if (d < hd) dst[d] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3);
+};
+struct AppendRows {  // the generation step: position context_lens[s] - 1 of sequence s
+    const int32_t* block_tables;
+    int32_t max_blocks;
+    const int32_t* context_lens;
+    __device__ bool slot_of(int64_t s, int32_t bs, int64_t& blk, int64_t& off) const {
+        const int32_t L = context_lens[s];
+        if (L <= 0) return false;
+        const int64_t pos = L - 1, logical = pos / bs;
+        off = pos - logical * bs;
+        blk = block_tables[s * max_blocks + logical];
+        return true;
     }
-    if (lane == 0) *scale = s;
+};
+template <typename Rows>
+__device__ __forceinline__ bool quant_dst(const Rows& rows, int64_t item, int32_t hkv, int32_t hd, int32_t bs,
+                                          uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
+                                          QuantDst& d) {
+    const int is_v = (int)(item & 1);
+    const int64_t row = item >> 1, t = row / hkv;
+    const int32_t h = (int32_t)(row - t * hkv);
+    int64_t blk, off;
+    if (!rows.slot_of(t, bs, blk, off)) return false;
+    d.src_row = row;
+    d.codes = (is_v ? v_codes : k_codes) + ((blk * bs + off) * hkv + h) * hd;
+    d.scale = (is_v ? v_scales : k_scales) + (blk * hkv + h) * bs + off;
+    return true;
 }
 
-// Warp item -> (token or sequence, KV head, K|V): item = (row * 2 + is_v), row = t * hkv + h.
-template <typename T>
-__global__ void __launch_bounds__(kQuantWarps * 32)
-    write_kv_fp8_kernel(const T* __restrict__ k, const T* __restrict__ v, const int64_t* __restrict__ slots,
-                        int64_t n, int32_t hkv, int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes,
-                        uint8_t* __restrict__ v_codes, float* __restrict__ k_scales, float* __restrict__ v_scales) {
-    pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;
-    if (item >= n * hkv * 2) return;
-    const int is_v = (int)(item & 1);
-    const int64_t row = item >> 1, token = row / hkv;
-    const int32_t h = (int32_t)(row - token * hkv);
-    const int64_t slot = slots[token];
-    if (slot < 0) return;
-    const int64_t blk = slot / bs;
-    quantize_row((is_v ? v : k) + row * hd, hd, (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd,
-                 (is_v ? v_scales : k_scales) + (blk * hkv + h) * bs + (slot - blk * bs), lane);
+// Main form, head_dim = 8 * EPL: eight lanes per row, four rows per warp at a
+// time; each lane loads its EPL consecutive elements with vector loads and
+// stores its EPL codes with vector stores.
+template <int BYTES>
+__device__ __forceinline__ void copy_vec(void* dst, const void* src) {
+    static_assert(BYTES % 4 == 0, "whole words");
+    if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+        for (int i = 0; i < BYTES / 16; ++i)
+            reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(src)[i];
+    } else if constexpr (BYTES % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < BYTES / 8; ++i)
+            reinterpret_cast<uint2*>(dst)[i] = reinterpret_cast<const uint2*>(src)[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < BYTES / 4; ++i)
+            reinterpret_cast<uint32_t*>(dst)[i] = reinterpret_cast<const uint32_t*>(src)[i];
+    }
 }
 
-// The generation step's quantizing write: sequence s's new rows k_new[s],
-// v_new[s] go to the slot of position context_lens[s] - 1 (length-0
-// sequences are skipped).
-template <typename T>
+template <typename T, int EPL, typename Rows>
 __global__ void __launch_bounds__(kQuantWarps * 32)
-    append_kv_fp8_kernel(const T* __restrict__ k_new, const T* __restrict__ v_new,
-                         const int32_t* __restrict__ block_tables, int32_t max_blocks,
-                         const int32_t* __restrict__ context_lens, int32_t num_seqs, int32_t hkv, int32_t hd,
-                         int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
-                         float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    quant_rows8_kernel(const T* __restrict__ k, const T* __restrict__ v, Rows rows, int64_t n_items, int32_t hkv,
+                       int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                       float* __restrict__ k_scales, float* __restrict__ v_scales) {
     pdl_launch_dependents();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t item = blockIdx.x * (int64_t)kQuantWarps + warp;
-    if (item >= (int64_t)num_seqs * hkv * 2) return;
-    const int is_v = (int)(item & 1);
-    const int64_t row = item >> 1, s = row / hkv;
-    const int32_t h = (int32_t)(row - s * hkv);
-    const int32_t L = context_lens[s];
-    if (L <= 0) return;
-    const int64_t pos = L - 1, logical = pos / bs, off = pos - logical * bs;
-    const int64_t blk = block_tables[s * max_blocks + logical], slot = blk * bs + off;
-    quantize_row((is_v ? v_new : k_new) + row * hd, hd, (is_v ? v_codes : k_codes) + (slot * hkv + h) * hd,
-                 (is_v ? v_scales : k_scales) + (blk * hkv + h) * bs + off, lane);
+    constexpr int HD = 8 * EPL;
+    const int lane = threadIdx.x & 31, sub = lane >> 3, l8 = lane & 7;
+    const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
+    for (int64_t q = blockIdx.x * (int64_t)kQuantWarps + (threadIdx.x >> 5); q * 4 < n_items; q += nwarps) {
+        const int64_t item = q * 4 + sub;
+        QuantDst d;
+        const bool live = item < n_items && quant_dst(rows, item, hkv, HD, bs, k_codes, v_codes, k_scales, v_scales, d);
+        float x[EPL];
+        float amax = 0.f;
+        if (live) {
+            T e[EPL];
+            copy_vec<EPL * (int)sizeof(T)>(e, ((item & 1) ? v : k) + d.src_row * HD + l8 * EPL);
+#pragma unroll
+            for (int i = 0; i < EPL; ++i) {
+                x[i] = Elt<T>::to_f(e[i]);
+                amax = fmaxf(amax, fabsf(x[i]));
+            }
+        }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (!live) continue;
+        const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+        uint32_t c[EPL / 4];
+#pragma unroll
+        for (int i = 0; i < EPL / 4; ++i) {
+            c[i] = 0u;
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                c[i] |= (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[4 * i + t], s), __NV_SATFINITE, __NV_E4M3)
+                        << (8 * t);
+        }
+        copy_vec<EPL>(d.codes + l8 * EPL, c);
+        if (l8 == 0) *d.scale = s;
+    }
+}
+
+// Any head_dim <= 256: one warp per row, element by element.
+template <typename T, typename Rows>
+__global__ void __launch_bounds__(kQuantWarps * 32)
+    quant_rows_kernel(const T* __restrict__ k, const T* __restrict__ v, Rows rows, int64_t n_items, int32_t hkv,
+                      int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
+                      float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
+    for (int64_t item = blockIdx.x * (int64_t)kQuantWarps + (threadIdx.x >> 5); item < n_items; item += nwarps) {
+        QuantDst d;
+        if (!quant_dst(rows, item, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales, d)) continue;
+        const T* src = ((item & 1) ? v : k) + d.src_row * hd;
+        float x[8], amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            x[j] = e < hd ? Elt<T>::to_f(src[e]) : 0.f;
+            amax = fmaxf(amax, fabsf(x[j]));
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = lane + 32 * j;
+            if (e < hd) d.codes[e] = (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(x[j], s), __NV_SATFINITE, __NV_E4M3);
+        }
+        if (lane == 0) *d.scale = s;
+    }
+}
+
+template <typename T, typename Rows>
+cudaError_t launch_quant(const void* k, const void* v, const Rows& rows, int64_t n_items, int32_t hkv, int32_t hd,
+                         int32_t bs, uint8_t* k_codes, uint8_t* v_codes, float* k_scales, float* v_scales,
+                         cudaStream_t stream) {
+    if (n_items == 0) return cudaSuccess;
+    const T* kt = static_cast<const T*>(k);
+    const T* vt = static_cast<const T*>(v);
+    const int64_t per_cta = kQuantWarps * ((hd % 8 == 0 && hd <= 256) ? 4 : 1);
+    const unsigned grid = (unsigned)std::min<int64_t>((n_items + per_cta - 1) / per_cta, kQuantMaxCtas);
+    const dim3 block(kQuantWarps * 32);
+    switch (hd % 8 == 0 ? hd / 8 : 0) {
+        case 4: quant_rows8_kernel<T, 4><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
+        case 8: quant_rows8_kernel<T, 8><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
+        case 16: quant_rows8_kernel<T, 16><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
+        case 32: quant_rows8_kernel<T, 32><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
+        default: quant_rows_kernel<T><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales); break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename Rows>
+cudaError_t launch_quant_dtype(int dtype, const void* k, const void* v, const Rows& rows, int64_t n_items,
+                               int32_t hkv, int32_t hd, int32_t bs, uint8_t* k_codes, uint8_t* v_codes,
+                               float* k_scales, float* v_scales, cudaStream_t stream) {
+    switch (dtype) {
+        case 0: return launch_quant<float>(k, v, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales, stream);
+        case 1: return launch_quant<__nv_bfloat16>(k, v, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales, stream);
+        default: return launch_quant<__half>(k, v, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales, stream);
+    }
 }
 
 // One CTA per (pair, layer); its threads stride over the K and V blocks.
@@ -278,40 +385,17 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t
 cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
                                 uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream) {
-    if (n == 0) return cudaSuccess;
-    const int64_t rows = n * num_kv_heads * 2;
-    const unsigned blocks = (unsigned)((rows + kQuantWarps - 1) / kQuantWarps);
-#define PA_QW(T)                                                                                               \
-    write_kv_fp8_kernel<T><<<blocks, kQuantWarps * 32, 0, stream>>>(                                         \
-        static_cast<const T*>(k), static_cast<const T*>(v), slot_mapping, n, num_kv_heads, head_dim, block_size, \
-        k_codes, v_codes, k_scales, v_scales)
-    switch (dtype) {
-        case 0: PA_QW(float); break;
-        case 1: PA_QW(__nv_bfloat16); break;
-        default: PA_QW(__half); break;
-    }
-#undef PA_QW
-    return cudaGetLastError();
+    return launch_quant_dtype(dtype, k, v, SlotRows{slot_mapping}, n * num_kv_heads * 2, num_kv_heads, head_dim,
+                              block_size, k_codes, v_codes, k_scales, v_scales, stream);
 }
 
 cudaError_t launch_append_kv_fp8(const void* k_new, const void* v_new, int dtype, const int32_t* block_tables,
                                  int32_t max_blocks, const int32_t* context_lens, int32_t num_seqs,
                                  int32_t num_kv_heads, int32_t head_dim, int32_t block_size, uint8_t* k_codes,
                                  uint8_t* v_codes, float* k_scales, float* v_scales, cudaStream_t stream) {
-    if (num_seqs == 0) return cudaSuccess;
-    const int64_t rows = (int64_t)num_seqs * num_kv_heads * 2;
-    const unsigned blocks = (unsigned)((rows + kQuantWarps - 1) / kQuantWarps);
-#define PA_QA(T)                                                                                              \
-    append_kv_fp8_kernel<T><<<blocks, kQuantWarps * 32, 0, stream>>>(                                       \
-        static_cast<const T*>(k_new), static_cast<const T*>(v_new), block_tables, max_blocks, context_lens,  \
-        num_seqs, num_kv_heads, head_dim, block_size, k_codes, v_codes, k_scales, v_scales)
-    switch (dtype) {
-        case 0: PA_QA(float); break;
-        case 1: PA_QA(__nv_bfloat16); break;
-        default: PA_QA(__half); break;
-    }
-#undef PA_QA
-    return cudaGetLastError();
+    return launch_quant_dtype(dtype, k_new, v_new, AppendRows{block_tables, max_blocks, context_lens},
+                              (int64_t)num_seqs * num_kv_heads * 2, num_kv_heads, head_dim, block_size, k_codes,
+                              v_codes, k_scales, v_scales, stream);
 }
 
 cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
