@@ -95,6 +95,28 @@ def traffic_record(workload, kernel_file):
     return None
 
 
+# ---------------------------------------------------------------- ranks
+
+def max_over_ranks(x, device=None):
+    """The largest of every rank's x (the slowest rank's time); x itself
+    without a process group.  Collective: every rank must call it."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step_per_rank, world, steps, ms):
+    """Units per second over the whole job: every rank processes its own
+    replica of the batch (weak scaling), so the job handles world x the
+    units of one rank in the slowest rank's time."""
+    return units_per_step_per_rank * world * steps / (ms / 1e3)
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons while running."""
 
@@ -585,13 +607,10 @@ def main():
                   if unfused_graphs else None)
     eager_steps = min(args.steps, 2000)
     eager_ms = timed(step, eager_steps) / eager_steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_step = ms / args.steps
-    value = kv_bytes * world * args.steps / (ms / 1e3) / 1e9
-    seq_per_s = S * world * args.steps / (ms / 1e3)
+    value = whole_job_rate(kv_bytes, world, args.steps, ms) / 1e9
+    seq_per_s = whole_job_rate(S, world, args.steps, ms)
 
     # e2e: each step's inputs from pinned host memory -> H2D, the step, the
     # output D2H to pinned memory; captured and replayed like the step
@@ -618,11 +637,8 @@ def main():
         torch.cuda.synchronize()
         e_steps = min(args.steps, 5000)
         e_ms = timed(lambda i: e2e_graphs[i % copies].replay(), e_steps)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": kv_bytes * world * e_steps / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e_ms = max_over_ranks(e_ms, dev)
+        e2e = {"value": whole_job_rate(kv_bytes, world, e_steps, e_ms) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / e_steps,
                "how": "pinned-host inputs -> H2D copies -> the step's C-ABI calls -> D2H output, "
                       "replayed as a CUDA graph per step"}
