@@ -103,6 +103,14 @@ PA_API pa_status pa_set_check_mode(int on);
  * the device. */
 PA_API pa_status pa_device_status(int clear);
 
+/* Exercises that failure path without a fault (library self-test; the pages
+ * have no counterpart): one CTA waits on a shared-memory barrier that nothing
+ * completes, with the same bounded wait the decode kernel uses, gives up
+ * after `polls` polls (1 .. 2^20), sets the timeout bit and returns; a
+ * following pa_device_status reports PA_ERR_TIMEOUT (and clears it on
+ * request).  Nothing else is touched and the context stays usable. */
+PA_API pa_status pa_selftest_wait_timeout(int32_t polls, void* stream);
+
 /*
  * pa_slot_mapping -- slot of each new token.
  *   slot_out[i] = block_tables[seq_idx[i] * max_blocks + positions[i] / block_size]

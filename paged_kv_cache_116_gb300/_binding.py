@@ -23,7 +23,7 @@ EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option"
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
            "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8",
-           "pa_decode_append_fp8")
+           "pa_decode_append_fp8", "pa_selftest_wait_timeout")
 
 
 class PAError(RuntimeError):
@@ -52,6 +52,7 @@ def lib():
         "pa_get_option": ([ci], i64),
         "pa_set_check_mode": ([ci], ci),
         "pa_device_status": ([ci], ci),
+        "pa_selftest_wait_timeout": ([i32, vp], ci),
         "pa_slot_mapping": ([vp, i32, i32, vp, vp, i64, i32, vp, vp], ci),
         "pa_write_kv": ([vp, vp, vp, i64, vp, vp, i32, i32, i32, i32, ci, vp], ci),
         "pa_write_kv_fp8": ([vp, vp, vp, i64, vp, vp, vp, vp, i32, i32, i32, i32, ci, vp], ci),
@@ -128,6 +129,12 @@ def pa_get_option(option):
 
 def pa_set_check_mode(on):
     _check(lib().pa_set_check_mode(1 if on else 0), "pa_set_check_mode")
+
+
+def pa_selftest_wait_timeout(polls=1000, stream=None):
+    """Run the bounded-wait self-test (a wait nothing completes gives up and sets the
+    timeout bit that pa_device_status reports)."""
+    _check(lib().pa_selftest_wait_timeout(polls, _stream(stream)), "pa_selftest_wait_timeout")
 
 
 def pa_device_status(clear=True):

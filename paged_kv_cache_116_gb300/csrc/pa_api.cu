@@ -155,6 +155,12 @@ pa_status pa_device_status(int clear) {
     return PA_OK;
 }
 
+pa_status pa_selftest_wait_timeout(int32_t polls, void* stream) {
+    if (polls < 1 || polls > (1 << 20)) return fail(PA_ERR_INVALID_ARG, "polls must be in [1, 2^20]");
+    cudaError_t e = pa::launch_selftest_wait((uint32_t)polls, as_stream(stream));
+    return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_selftest_wait_timeout launch");
+}
+
 pa_status pa_slot_mapping(const int32_t* block_tables, int32_t num_seqs, int32_t max_blocks, const int32_t* seq_idx,
                           const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
                           void* stream) {

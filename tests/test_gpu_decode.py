@@ -261,3 +261,19 @@ def test_graph_replays_of_decode_follow_new_queries(pa):
     mc = int(w.seq_lens.max())
     graph_replays_match_eager(
         lambda out, q, ws: pa.pa_decode(out, q, kc, vc, bt, lens, mc, w.scale, workspace=ws), w.q.to(DEV).clone(), DEV)
+
+
+# ---------------------------------------------------------------- failure detection
+
+def test_bounded_wait_expiry_is_reported_and_the_context_survives(pa):
+    """A barrier wait that nothing completes gives up after its bound, the
+    kernel sets the timeout bit, pa_device_status reports PA_ERR_TIMEOUT and
+    clears it, and the next decode runs normally."""
+    pa.pa_device_status(clear=True)
+    pa.pa_selftest_wait_timeout(2000)
+    with pytest.raises(pa.PAError, match="PA_ERR_TIMEOUT"):
+        pa.pa_device_status(clear=True)
+    pa.pa_device_status(clear=True)  # cleared: no error now
+    w = W.decode_workload("after_timeout", "bf16", 16, 8, 2, 128, [40, 3, 200], seed=81)
+    kc, vc, bt = device_caches(w, DEV)
+    compare(w, run_decode(pa, w, kc, vc, bt), oracle_attention(w))
