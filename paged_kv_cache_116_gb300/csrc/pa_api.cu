@@ -150,7 +150,8 @@ pa_status pa_device_status(int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pa_device_status");
     const uint32_t bits =
-        pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0) | pa::varlen_umma_status(clear != 0);
+        pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0) | pa::varlen_umma_status(clear != 0) |
+        pa::selftest_status(clear != 0);
     if (bits & 1u) return fail(PA_ERR_TIMEOUT, "a kernel's bounded barrier wait ran out");
     return PA_OK;
 }

@@ -975,25 +975,6 @@ cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_cta
                         : launch_dtype<__half>(a, num_blocks, grid_ctas, workspace, err, stream);
 }
 
-namespace {
-// One CTA waits on a shared-memory barrier that nothing completes, with the
-// decode kernel's bounded wait, and records the expiry as that kernel would.
-__global__ void selftest_wait_kernel(uint32_t polls) {
-    __shared__ uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-    }
-    __syncthreads();
-    if (threadIdx.x == 0 && !mbar_wait_bounded(&bar, 0u, polls)) atomicOr(&g_decode_status, kStatusTimeout);
-}
-}  // namespace
-
-cudaError_t launch_selftest_wait(uint32_t polls, cudaStream_t stream) {
-    selftest_wait_kernel<<<1, 32, 0, stream>>>(polls);
-    return cudaGetLastError();
-}
-
 uint32_t decode_tc_status(bool clear) {
     unsigned int v = 0;
     cudaMemcpyFromSymbol(&v, g_decode_status, sizeof(v));

@@ -104,9 +104,11 @@ size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
                              std::string* err, cudaStream_t stream);
 uint32_t decode_tc_status(bool clear);
-// One CTA that waits on a barrier nothing completes for `polls` polls and sets
-// the decode status word's timeout bit (pa_selftest_wait_timeout).
+// ---- self-test of the failure path (pa_selftest.cu): one CTA waits on a
+// barrier nothing completes for `polls` polls and sets its status word's
+// timeout bit (pa_selftest_wait_timeout).
 cudaError_t launch_selftest_wait(uint32_t polls, cudaStream_t stream);
+uint32_t selftest_status(bool clear);
 
 // ---- tensor-core varlen (pa_varlen_tc.cu)
 bool varlen_tc_supported(int dtype, int head_dim, int block_size);
