@@ -277,3 +277,30 @@ def test_bounded_wait_expiry_is_reported_and_the_context_survives(pa):
     w = W.decode_workload("after_timeout", "bf16", 16, 8, 2, 128, [40, 3, 200], seed=81)
     kc, vc, bt = device_caches(w, DEV)
     compare(w, run_decode(pa, w, kc, vc, bt), oracle_attention(w))
+
+
+# ---------------------------------------------------------------- batches beyond one launch
+
+def test_more_sequences_than_one_launch_takes(pa):
+    """5,000 sequences: the library cuts the batch into launches of at most
+    4,096 sequences on one workspace; every row matches the oracle, for the
+    plain decode and the fused generation step."""
+    lens = np.random.default_rng(91).integers(1, 60, 5000).tolist()
+    w = W.decode_workload("many", "bf16", 16, 8, 2, 128, lens, seed=91)
+    kc, vc, bt = device_caches(w, DEV)
+    okc, ovc = oracle_caches(w)
+    exact = oracle_attention(w, okc, ovc)
+    compare(w, run_decode(pa, w, kc, vc, bt), exact)
+    # the generation step from the pre-step pool
+    kc2, vc2, _ = device_caches(w, DEV, after_step=False)
+    mc = int(w.seq_lens.max())
+    ws = torch.empty(max(pa.pa_decode_workspace_size(w.num_seqs, 8, 2, 128, 16, mc, torch.bfloat16), 16),
+                     dtype=torch.uint8, device=DEV)
+    out = torch.full((w.num_seqs, 8, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    pa.pa_decode_append(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc2, vc2,
+                        bt, torch.from_numpy(w.seq_lens).to(DEV), mc, w.scale, workspace=ws)
+    torch.cuda.synchronize()
+    from helpers import oracle_bits, raw_bits
+
+    assert np.array_equal(raw_bits(kc2), oracle_bits(okc)) and np.array_equal(raw_bits(vc2), oracle_bits(ovc))
+    compare(w, out, exact)

@@ -359,3 +359,11 @@ def test_decode_append_fp8_any_split(pa, ctas):
     opools = oracle_fp8_caches(w)
     assert_pools_equal((kc, vc, ks, vs), opools)
     compare(w, out, oracle_fp8_attention(w, *opools))
+
+
+def test_fp8_decode_more_sequences_than_one_launch_takes(pa):
+    lens = np.random.default_rng(92).integers(1, 60, 5000).tolist()
+    w = W.decode_workload("many8", "bf16", 16, 8, 2, 128, lens, seed=92)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
