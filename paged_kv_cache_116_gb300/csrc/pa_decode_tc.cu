@@ -106,13 +106,19 @@ struct TcParams {
 // the register budget is sized for (__launch_bounds__).  A stage of about
 // 8 KB keeps the per-stage costs (barrier round trip, copy issue) small
 // against the bytes it brings: 16-bit head_dim-128 tiles are 8 KB, code
-// tiles half that, so code stages hold two tiles.  The code path is bound
-// by its per-tile conversion chain rather than by memory, so it runs three
-// CTAs (12 warps) per SM on two stages each (measured: 12 warps beat 8 and
-// 16 on the 64-sequence GQA batch).
+// tiles half that, so code stages hold two tiles.  16-bit head_dim 128: one
+// CTA of 8 warps x 2 stages per SM, 128 KB in flight per SM -- measured
+// against 8, 10, 12, 16 and 24 stages per SM with 4-16 warps, this is the
+// fastest on the GQA, long-context and MHA batches (88.8 / 175.9 / 192.4 us
+// against 94.7 / 188.4 / 207.1 us for 2 CTAs x 4 warps x 3 stages): once HBM
+// is saturated, more bytes in flight only lengthen the queues, which shows
+// at the start and in the tail.  The code path is bound by its per-tile
+// conversion chain rather than by memory, so it runs three CTAs (12 warps)
+// per SM on two stages each (measured: 12 warps beat 8 and 16 on the
+// 64-sequence GQA batch).
 template <int HD, bool FP8> struct Pipe;
 template <> struct Pipe<64, false> { static constexpr int NW = 4, R = 6, TPS = 1, MINB = 1; };
-template <> struct Pipe<128, false> { static constexpr int NW = 4, R = 3, TPS = 1, MINB = 1; };
+template <> struct Pipe<128, false> { static constexpr int NW = 8, R = 2, TPS = 1, MINB = 1; };
 template <> struct Pipe<256, false> { static constexpr int NW = 2, R = 3, TPS = 1, MINB = 1; };
 template <> struct Pipe<128, true> { static constexpr int NW = 4, R = 2, TPS = 2, MINB = 3; };
 template <> struct Pipe<256, true> { static constexpr int NW = 4, R = 3, TPS = 1, MINB = 1; };
