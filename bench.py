@@ -180,12 +180,28 @@ def make_workload(name, device, block_size=16):
     return getattr(W, name)(device=device)
 
 
-def varlen_flops(w):
-    """2 x the multiply-adds of Q K^T and P V over the causal (or full) key ranges."""
+def varlen_flops(w, select=None):
+    """2 x the multiply-adds of Q K^T and P V over the causal (or full) key ranges
+    (of the requests in `select`, default all)."""
     total = 0.0
-    for n, L in zip(w.query_lens.tolist(), w.seq_lens.tolist()):
+    idx = range(w.num_seqs) if select is None else select
+    for i in idx:
+        n, L = int(w.query_lens[i]), int(w.seq_lens[i])
         total += n * (L - n) + n * (n + 1) / 2 if w.causal else n * L
     return 4.0 * w.num_heads * w.head_dim * total
+
+
+def unique_kv_bytes(w):
+    """K/V bytes of the distinct pool rows the step's attention reads: a block
+    shared by several requests (a forked prompt) counts once, with the most
+    tokens any reader uses of it."""
+    used = {}
+    for i in range(w.num_seqs):
+        L = int(w.seq_lens[i])
+        for j in range((L + w.block_size - 1) // w.block_size):
+            b = int(w.block_tables[i, j])
+            used[b] = max(used.get(b, 0), min(w.block_size, L - j * w.block_size))
+    return sum(used.values()) * w.num_kv_heads * w.head_dim * 2 * w.elt
 
 
 def oracle_setup(w):
@@ -439,6 +455,7 @@ def main():
             run_swap(args)
         return
 
+    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -603,6 +620,43 @@ def main():
     ms = timed(lambda i: step_graphs[i % copies].replay(), args.steps)
     clk = clocks.stop() if rank == 0 and not args.no_extras else None
     kern_ms = timed(lambda i: kern_graphs[i % copies].replay(), args.steps) / args.steps
+    # the varlen mix's two parts, each as a pa_varlen call of its own over the
+    # same pools (prefill chunks: tensor-bound; decode rows: HBM-bound); in the
+    # mixed call they share one launch, so these times do not add up to it
+    parts = None
+    if not decode and not args.no_extras:
+        parts = {}
+        peaks_p, _ = measured_peaks()
+        for name, sel in (("prefill_chunks", np.where(w.query_lens > 1)[0]),
+                          ("decode_rows", np.where(w.query_lens == 1)[0])):
+            if len(sel) == 0:
+                continue
+            rows = np.concatenate([np.arange(w.query_start_loc[i], w.query_start_loc[i + 1]) for i in sel])
+            qp = q[torch.from_numpy(rows).to(dev).long()].contiguous()
+            op = torch.empty_like(qp)
+            cup = torch.from_numpy(np.concatenate([[0], np.cumsum(w.query_lens[sel])]).astype(np.int32)).to(dev)
+            selt = torch.from_numpy(sel).to(dev).long()
+            btp, lp = bt[selt].contiguous(), lens[selt].contiguous()
+            mqp = int(w.query_lens[sel].max())
+
+            def part_call(i, qp=qp, op=op, cup=cup, btp=btp, lp=lp, mqp=mqp):
+                pa.pa_varlen(op, qp, *pools[i % copies], btp, lp, cup, mqp, max_ctx, w.scale, causal=w.causal,
+                             workspace=ws, stream=torch.cuda.current_stream())
+
+            for i in range(3):
+                part_call(i)
+            pg = capture(part_call)
+            for i in range(3):
+                pg[i % copies].replay()
+            torch.cuda.synchronize()
+            p_ms = timed(lambda i: pg[i % copies].replay(), args.steps) / args.steps
+            fl = varlen_flops(w, sel)
+            kvb = int(sum(int(w.seq_lens[i]) for i in sel)) * hkv * hd * 2 * w.elt
+            parts[name] = {"requests": int(len(sel)), "query_rows": int(len(rows)), "kernel_us": p_ms * 1e3,
+                           "TFLOP/s": fl / (p_ms / 1e3) / 1e12,
+                           "tensor_frac": fl / (p_ms / 1e3) / 1e12 / peaks_p["bf16_tflops"],
+                           "kv_bytes": kvb, "kv_GB/s": kvb / (p_ms / 1e3) / 1e9,
+                           "hbm_frac": kvb / (p_ms / 1e3) / 1e9 / peaks_p["hbm_gbs"]}
     unfused_ms = (timed(lambda i: unfused_graphs[i % copies].replay(), args.steps) / args.steps
                   if unfused_graphs else None)
     eager_steps = min(args.steps, 2000)
@@ -676,6 +730,7 @@ def main():
                 "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": kind + " bf16_tflops (burst)",
                 "algorithmic_flops": fl, "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
+                "unique_kv_bytes": unique_kv_bytes(w), "parts": parts,
                 "traffic": traffic_record(args.workload, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3}
 
     if rank == 0:
