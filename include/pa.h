@@ -86,7 +86,14 @@ typedef enum {
     /* Varlen kernel: 0 automatic (default: the tcgen05 kernel where it
      * applies, else the CUDA-core kernel), 1 the CUDA-core kernel, 2 the
      * mma.sync tensor-core kernel, 3 the tcgen05 (tensor-memory) kernel. */
-    PA_OPT_VARLEN_KERNEL = 3
+    PA_OPT_VARLEN_KERNEL = 3,
+    /* Code-cache decode, head_dim 128: work the two tiles of a pipeline stage
+     * that belong to one (sequence, KV head) as one 32-token step (one
+     * softmax reduction, two independent score chains).  0 automatic
+     * (default: when max_context > 2048, where sequences are long enough
+     * that most stages hold two tiles of one unit), 1 never, 2 always.
+     * Results agree within the tolerance either way. */
+    PA_OPT_FP8_PAIR_STEP = 4
 } pa_option;
 
 PA_API const char* pa_status_string(int status);

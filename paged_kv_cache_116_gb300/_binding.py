@@ -14,7 +14,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_lib", "libpa.so")
 
 PA_F32, PA_BF16, PA_F16, PA_FP8_E4M3 = 0, 1, 2, 3
-PA_OPT_CHECK_MODE, PA_OPT_DECODE_KERNEL, PA_OPT_DECODE_CTAS, PA_OPT_VARLEN_KERNEL = 0, 1, 2, 3
+PA_OPT_CHECK_MODE, PA_OPT_DECODE_KERNEL, PA_OPT_DECODE_CTAS, PA_OPT_VARLEN_KERNEL, PA_OPT_FP8_PAIR_STEP = 0, 1, 2, 3, 4
 DTYPE_CODE = {torch.float32: PA_F32, torch.bfloat16: PA_BF16, torch.float16: PA_F16}
 # pools that only move bytes (copy, swap) may also hold E4M3 codes
 POOL_DTYPE_CODE = {**DTYPE_CODE, torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: PA_FP8_E4M3}

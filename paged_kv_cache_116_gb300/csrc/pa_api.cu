@@ -15,7 +15,8 @@
 namespace {
 
 thread_local std::string g_last_error;
-int64_t g_options[4] = {0, 0, 0, 0};
+int64_t g_options[5] = {0, 0, 0, 0, 0};
+constexpr int32_t kPairMinContext = 2048;  // automatic pair steps above this max_context
 
 pa_status fail(pa_status st, const std::string& msg) {
     g_last_error = msg;
@@ -131,8 +132,9 @@ const char* pa_status_string(int status) {
 const char* pa_last_error(void) { return g_last_error.c_str(); }
 
 pa_status pa_set_option(int option, int64_t value) {
-    if (option < 0 || option > PA_OPT_VARLEN_KERNEL) return fail(PA_ERR_INVALID_ARG, "unknown option");
-    if ((option == PA_OPT_DECODE_KERNEL && value > 2) || (option == PA_OPT_VARLEN_KERNEL && value > 3))
+    if (option < 0 || option > PA_OPT_FP8_PAIR_STEP) return fail(PA_ERR_INVALID_ARG, "unknown option");
+    if ((option == PA_OPT_DECODE_KERNEL && value > 2) || (option == PA_OPT_VARLEN_KERNEL && value > 3) ||
+        (option == PA_OPT_FP8_PAIR_STEP && value > 2))
         return fail(PA_ERR_INVALID_ARG, "unknown kernel choice");
     if (value < 0) return fail(PA_ERR_INVALID_ARG, "option values are non-negative");
     g_options[option] = value;
@@ -140,7 +142,7 @@ pa_status pa_set_option(int option, int64_t value) {
 }
 
 int64_t pa_get_option(int option) {
-    if (option < 0 || option > PA_OPT_VARLEN_KERNEL) return -1;
+    if (option < 0 || option > PA_OPT_FP8_PAIR_STEP) return -1;
     return g_options[option];
 }
 
@@ -474,6 +476,14 @@ static pa_status decode_impl(void* out, const void* q, const void* k_new, const 
     const int grid = pa::decode_tc_grid(num_seqs, num_kv_heads, head_dim, block_size, max_context, dtype, G,
                                         g_options[PA_OPT_DECODE_CTAS], fp8);
     const size_t need = pa::decode_tc_workspace(num_seqs, num_kv_heads, G, head_dim, grid, fp8);
+    // Code cache, head_dim 128: the 32-token pair step pays where units are
+    // long (measured: 8 x 32k tokens 7 % faster, the 64-sequence batch of up
+    // to 3,360 tokens 1 %) and loses where many units are short (128
+    // sequences of mean 480 tokens: 8 % slower, the split then leaves some
+    // warps with many single tiles).  max_context is the host's only view
+    // of the lengths.
+    const int64_t pair_opt = g_options[PA_OPT_FP8_PAIR_STEP];
+    a.pair_steps = fp8 && head_dim == 128 && (pair_opt == 2 || (pair_opt == 0 && max_context > kPairMinContext));
     if (workspace_bytes < need || (need && !workspace))
         return fail(PA_ERR_WORKSPACE, "workspace holds " + std::to_string(workspace_bytes) + " bytes, " +
                                           std::to_string(need) + " needed");

@@ -157,7 +157,7 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 
 // T: element type of q and out.  FP8: the cache holds E4M3 codes plus
 // scales (the mma then runs in f16 whatever T is).
-template <typename T, int HD, int NT, bool FP8>
+template <typename T, int HD, int NT, bool FP8, bool PAIR>
 __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const TcParams p) {
@@ -614,6 +614,160 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
             }
         }
 
+        if constexpr (FP8 && TPS == 2 && PAIR) {
+            // Pair step: when both tiles of this stage belong to the unit (and
+            // the second is not the one the new token goes to), they are
+            // worked as one 32-token step: two independent score chains, one
+            // softmax reduction and rescale, then sixteen P V products.  Tile
+            // a (this one) is full; tile b may end the context.
+            const int nb_u = prefix[cs + 1] - prefix[cs];
+            if (sub == 0 && i + 1 < n && cb + 1 < nb_u && !(p.k_new != nullptr && cb + 1 == nb_u - 1)) {
+                const uint32_t ktb = kt + 2 * Gm::TILE, vtb = ktb + Gm::TILE;
+                const int valid_b = min(BS, Lcur - (cb + 1) * BS);
+                float sa[NT][4], sb[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+                constexpr int KP = HD / 64;
+#pragma unroll
+                for (int u = 0; u < KP; ++u) {
+                    uint4 wa[2], wb[2];
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int r = g + 8 * hi, b = kb0 + 16 * u;
+                        const uint32_t off = (b >> 7) * BS * 128 + r * 128 + ((((b & 127) >> 4) ^ (r & 7)) << 4);
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(wa[hi].x), "=r"(wa[hi].y), "=r"(wa[hi].z), "=r"(wa[hi].w) : "r"(kt + off));
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(wb[hi].x), "=r"(wb[hi].y), "=r"(wb[hi].z), "=r"(wb[hi].w) : "r"(ktb + off));
+                    }
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int kk = 4 * u + q4;
+                        const uint32_t a0w = (&wa[0].x)[q4], a1w = (&wa[1].x)[q4];
+                        const uint32_t b0w = (&wb[0].x)[q4], b1w = (&wb[1].x)[q4];
+                        const uint32_t a0 = e4m3x2_to_f16x2(a0w), a2 = e4m3x2_to_f16x2(a0w >> 16);
+                        const uint32_t a1 = e4m3x2_to_f16x2(a1w), a3 = e4m3x2_to_f16x2(a1w >> 16);
+                        const uint32_t b0 = e4m3x2_to_f16x2(b0w), b2 = e4m3x2_to_f16x2(b0w >> 16);
+                        const uint32_t b1 = e4m3x2_to_f16x2(b1w), b3 = e4m3x2_to_f16x2(b1w >> 16);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816<__half>(sa[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+                            mma16816<__half>(sb[nt], b0, b1, b2, b3, qb[kk][nt][0], qb[kk][nt][1]);
+                        }
+                    }
+                }
+                const float* ssa = wscl + slot * (Gm::SCL / 4);  // tile a's K then V scales
+                const float* ssb = ssa + Gm::TSCL;                // tile b's
+                const bool okb0 = g < valid_b, okb1 = g + 8 < valid_b;
+                const float ka0 = ssa[g], ka1 = ssa[g + 8], kb0s = ssb[g], kb1s = ssb[g + 8];
+                const float va0 = ssa[BS + g], va1 = ssa[BS + g + 8];
+                const float vb0s = okb0 ? ssb[BS + g] : 0.f, vb1s = okb1 ? ssb[BS + g + 8] : 0.f;
+                uint32_t pa[NT][2], pbb[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float xa0 = sa[nt][0] * ka0, xa1 = sa[nt][1] * ka0, xa2 = sa[nt][2] * ka1, xa3 = sa[nt][3] * ka1;
+                    const float xb0 = okb0 ? sb[nt][0] * kb0s : -INFINITY, xb1 = okb0 ? sb[nt][1] * kb0s : -INFINITY;
+                    const float xb2 = okb1 ? sb[nt][2] * kb1s : -INFINITY, xb3 = okb1 ? sb[nt][3] * kb1s : -INFINITY;
+                    float mx0 = fmaxf(fmaxf(xa0, xa2), fmaxf(xb0, xb2)), mx1 = fmaxf(fmaxf(xa1, xa3), fmaxf(xb1, xb3));
+#pragma unroll
+                    for (int off = 4; off < 32; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(mrow[nt][0], mx0), mn1 = fmaxf(mrow[nt][1], mx1);
+                    const float al0 = fast_exp2(mrow[nt][0] - mn0), al1 = fast_exp2(mrow[nt][1] - mn1);
+                    mrow[nt][0] = mn0;
+                    mrow[nt][1] = mn1;
+                    const float pa0 = fast_exp2(xa0 - mn0), pa1 = fast_exp2(xa1 - mn1);
+                    const float pa2 = fast_exp2(xa2 - mn0), pa3 = fast_exp2(xa3 - mn1);
+                    const float pb0 = fast_exp2(xb0 - mn0), pb1 = fast_exp2(xb1 - mn1);
+                    const float pb2 = fast_exp2(xb2 - mn0), pb3 = fast_exp2(xb3 - mn1);
+                    lrow[nt][0] = fmaf(lrow[nt][0], al0, (pa0 + pa2) + (pb0 + pb2));
+                    lrow[nt][1] = fmaf(lrow[nt][1], al1, (pa1 + pa3) + (pb1 + pb3));
+                    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                        for (int mt = 0; mt < KS; ++mt) {
+                            acc[mt][nt][0] *= al0;
+                            acc[mt][nt][1] *= al1;
+                            acc[mt][nt][2] *= al0;
+                            acc[mt][nt][3] *= al1;
+                        }
+                    }
+                    pa[nt][0] = movm_t(pack2<__half>(pa0 * va0, pa1 * va0));
+                    pa[nt][1] = movm_t(pack2<__half>(pa2 * va1, pa3 * va1));
+                    pbb[nt][0] = movm_t(pack2<__half>(pb0 * vb0s, pb1 * vb0s));
+                    pbb[nt][1] = movm_t(pack2<__half>(pb2 * vb1s, pb3 * vb1s));
+                }
+                uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+                if (valid_b < BS) {
+                    m01 = (2 * c4 < valid_b ? 0x0000ffffu : 0u) | (2 * c4 + 1 < valid_b ? 0xffff0000u : 0u);
+                    m23 = (2 * c4 + 8 < valid_b ? 0x0000ffffu : 0u) | (2 * c4 + 9 < valid_b ? 0xffff0000u : 0u);
+                }
+                constexpr int VP = HD / 128;
+#pragma unroll
+                for (int u = 0; u < VP; ++u) {
+                    uint4 va[4], vb[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int r = 2 * c4 + (t & 1) + 8 * (t >> 1), b = vb0 + 16 * u;
+                        const uint32_t off = (b >> 7) * BS * 128 + r * 128 + ((((b & 127) >> 4) ^ (r & 7)) << 4);
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(va[t].x), "=r"(va[t].y), "=r"(va[t].z), "=r"(va[t].w) : "r"(vt + off));
+                        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                                     : "=r"(vb[t].x), "=r"(vb[t].y), "=r"(vb[t].z), "=r"(vb[t].w) : "r"(vtb + off));
+                    }
+#pragma unroll
+                    for (int mq = 0; mq < 8; ++mq) {
+                        const int mt = 8 * u + mq, wi = mq >> 1;
+                        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                        const uint32_t la = __byte_perm((&va[0].x)[wi], (&va[1].x)[wi], sel);
+                        const uint32_t ha = __byte_perm((&va[2].x)[wi], (&va[3].x)[wi], sel);
+                        const uint32_t lb = __byte_perm((&vb[0].x)[wi], (&vb[1].x)[wi], sel);
+                        const uint32_t hb = __byte_perm((&vb[2].x)[wi], (&vb[3].x)[wi], sel);
+                        const uint32_t a0 = e4m3x2_to_f16x2(la), a1 = e4m3x2_to_f16x2(la >> 16);
+                        const uint32_t a2 = e4m3x2_to_f16x2(ha), a3 = e4m3x2_to_f16x2(ha >> 16);
+                        uint32_t b0 = e4m3x2_to_f16x2(lb), b1 = e4m3x2_to_f16x2(lb >> 16);
+                        uint32_t b2 = e4m3x2_to_f16x2(hb), b3 = e4m3x2_to_f16x2(hb >> 16);
+                        if (valid_b < BS) {
+                            b0 &= m01;
+                            b1 &= m01;
+                            b2 &= m23;
+                            b3 &= m23;
+                        }
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            mma16816<__half>(acc[mt][nt], a0, a1, a2, a3, pa[nt][0], pa[nt][1]);
+                            mma16816<__half>(acc[mt][nt], b0, b1, b2, b3, pbb[nt][0], pbb[nt][1]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (ip < n) issue_next();
+                ++i;  // tile b is done too
+                cb += 2;
+                const bool unit_done = (cb == nb_u);
+                if (unit_done || i == n - 1) {
+                    finalize(cb, nb_u);
+                    first_seg = false;
+                    if (unit_done && i < n - 1) {
+                        cb = 0;
+                        seg_b0 = 0;
+                        if (++ch == Hkv) {
+                            ch = 0;
+                            do {
+                                ++cs;
+                            } while (cs < S && prefix[cs + 1] == prefix[cs]);
+                            Lcur = lens[cs];
+                        }
+                        begin_unit();
+                    }
+                }
+                continue;
+            }
+        }
+
         // S^T = K Q^T : 16 tokens x (8 NT) heads, fp32
         float sc[NT][4];
 #pragma unroll
@@ -836,9 +990,9 @@ bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, bool fp8, int num
     return true;
 }
 
-template <typename T, int HD, int NT, bool FP8>
+template <typename T, int HD, int NT, bool FP8, bool PAIR = false>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8>);
+    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8, PAIR>);
 }
 
 template <int HD, bool FP8>
@@ -860,7 +1014,7 @@ int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t ma
     return (int)(grid < 1 ? 1 : grid);
 }
 
-template <typename T, int HD, int NT, bool FP8>
+template <typename T, int HD, int NT, bool FP8, bool PAIR = false>
 cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* workspace, std::string* err,
                          cudaStream_t stream) {
     CUtensorMap tmK, tmV;
@@ -890,7 +1044,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.k_scales = a.k_scales;
     p.v_scales = a.v_scales;
 
-    const void* kfn = kernel_ptr<T, HD, NT, FP8>();
+    const void* kfn = kernel_ptr<T, HD, NT, FP8, PAIR>();
     const size_t smem = smem_bytes<HD, FP8>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -906,7 +1060,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8>, tmK, tmV, p);
+    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8, PAIR>, tmK, tmV, p);
 }
 
 template <typename T>
@@ -917,7 +1071,8 @@ cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     if (a.kv_fp8) {
         if (a.head_dim == 128)
             return two ? launch_typed<T, 128, 2, true>(a, num_blocks, grid, ws, err, st)
-                       : launch_typed<T, 128, 1, true>(a, num_blocks, grid, ws, err, st);
+                       : a.pair_steps ? launch_typed<T, 128, 1, true, true>(a, num_blocks, grid, ws, err, st)
+                                      : launch_typed<T, 128, 1, true>(a, num_blocks, grid, ws, err, st);
         return two ? launch_typed<T, 256, 2, true>(a, num_blocks, grid, ws, err, st)
                    : launch_typed<T, 256, 1, true>(a, num_blocks, grid, ws, err, st);
     }

@@ -88,6 +88,9 @@ struct AttnArgs {
     int kv_fp8 = 0;
     const float* k_scales = nullptr;
     const float* v_scales = nullptr;
+    // code cache, head_dim 128: the two tiles of a stage that belong to one
+    // unit worked as one 32-token step
+    int pair_steps = 0;
 };
 bool attn_simt_supported(int dtype, int head_dim);  // either cache kind
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream);

@@ -46,6 +46,9 @@ def test_status_strings_and_options(lib):
     assert lib.pa_set_option(2, 17) == 0 and lib.pa_get_option(2) == 17
     assert lib.pa_set_option(2, 0) == 0
     assert lib.pa_set_option(99, 1) == 1  # unknown option
+    assert lib.pa_set_option(4, 2) == 0 and lib.pa_get_option(4) == 2  # FP8 pair step: always
+    assert lib.pa_set_option(4, 3) == 1  # no such choice
+    assert lib.pa_set_option(4, 0) == 0
     assert lib.pa_set_option(0, -1) == 1  # negative value
 
 

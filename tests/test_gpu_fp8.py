@@ -361,6 +361,80 @@ def test_decode_append_fp8_any_split(pa, ctas):
     compare(w, out, oracle_fp8_attention(w, *opools))
 
 
+# ---------------------------------------------------------------- the 32-token pair step
+
+PAIR_CASES = [
+    # (dtype, block_size, G, Hkv, lengths): odd and even tile counts, a last
+    # tile of 1..16 tokens, one-tile units, 8-token blocks
+    ("bf16", 16, 4, 8, [1, 16, 17, 31, 32, 33, 48, 300, 2047, 3360]),
+    ("f16", 16, 1, 8, [2, 15, 64, 65, 129, 1000]),
+    ("bf16", 8, 8, 2, [1, 7, 8, 9, 16, 17, 40, 257]),
+    ("f16", 32, 6, 2, [31, 32, 33, 95, 96, 97, 500]),
+    ("bf16", 64, 2, 4, [1, 63, 64, 65, 700]),
+]
+
+
+@pytest.mark.parametrize("dt,bs,g,hkv,lens", PAIR_CASES)
+def test_fp8_pair_step_never_and_always_match_oracle(pa, dt, bs, g, hkv, lens):
+    """The code-cache kernel with and without the pair step (head_dim 128,
+    G <= 8), over several splits of the batch, against the oracle."""
+    w = W.decode_workload("fp8_pair", dt, bs, g * hkv, hkv, 128, lens, seed=bs * 31 + g)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
+    try:
+        for mode in (1, 2):
+            pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, mode)
+            for ctas in (0, 1, 5, 37):
+                compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=2, ctas=ctas), exact)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 0)
+
+
+@pytest.mark.parametrize("ctas", [0, 1, 5, 37])
+def test_fp8_pair_step_with_the_new_token(pa, ctas):
+    """The fused generation step with pair steps forced: the tile the new
+    token goes to is worked alone, the pools match the oracle bit for bit."""
+    w = W.decode_workload("ap8_pair", "bf16", 16, 32, 8, 128, [1, 2, 16, 17, 33, 300, 1001, 2048], seed=73)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV, after_step=False)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    mc = int(w.seq_lens.max())
+    pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 2)
+    pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, ctas)
+    try:
+        ws = torch.empty(max(pa.pa_decode_fp8_workspace_size(w.num_seqs, 32, 8, 128, 16, mc, torch.bfloat16), 16),
+                         dtype=torch.uint8, device=DEV)
+        out = torch.full((w.num_seqs, 32, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        pa.pa_decode_append_fp8(out, w.q.to(DEV), w.new_k.to(DEV).contiguous(), w.new_v.to(DEV).contiguous(), kc,
+                                vc, ks, vs, bt, lens, mc, w.scale, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 0)
+        pa.pa_set_option(pa.PA_OPT_DECODE_CTAS, 0)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    compare(w, out, oracle_fp8_attention(w, *opools))
+
+
+def test_fp8_pair_step_permuting_physical_blocks_is_bit_identical(pa):
+    w = W.decode_workload("fp8_pperm", "bf16", 16, 32, 8, 128, [700, 33, 1, 250, 16, 2500], seed=74)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 2)
+    try:
+        base = run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=2)
+        perm = torch.from_numpy(np.random.default_rng(3).permutation(w.num_blocks)).to(DEV)
+        moved = []
+        for t in (kc, vc, ks, vs):
+            u = torch.empty_like(t)
+            u[perm] = t
+            moved.append(u)
+        bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+        again = run_decode_fp8(pa, w, *moved, bt2, kernel=2)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 0)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
 def test_fp8_decode_more_sequences_than_one_launch_takes(pa):
     lens = np.random.default_rng(92).integers(1, 60, 5000).tolist()
     w = W.decode_workload("many8", "bf16", 16, 8, 2, 128, lens, seed=92)
