@@ -40,7 +40,7 @@ def _rank_main(rank, world, port, times, out):
 def test_two_gloo_ranks_take_the_slowest_time_and_sum_the_work():
     world, port = 2, _free_port()
     times = [12.5, 20.0]  # ms over the timed steps, rank 1 is slower
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a threaded test process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)
