@@ -46,6 +46,10 @@
 //    k-step (keys) and m-tile (values) is permuted -- consistently on both
 //    operands, since a dot product does not depend on its order -- so every
 //    lane reads contiguous 16-byte pieces of the staged codes.
+//  * Pair step (code cache, head_dim 128; a separate instance the host picks
+//    for long contexts): when both tiles of a stage belong to one unit they
+//    are worked as one 32-token step -- two independent score chains, one
+//    softmax reduction and rescale test, sixteen P V products.
 //  * Append mode fuses the generation step: the warp that owns a unit's last
 //    block patches the new token's K/V row (prefetched from the inputs) into
 //    the staged tile before its MMAs and stores the same row to the pool at
