@@ -228,11 +228,11 @@ def oracle_setup(w):
     return kc, vc, W.raw_numpy(w.q)
 
 
-def oracle_step(w, kc, vc, q):
+def oracle_step(w, kc, vc, q, num_threads=0):
     import oracle
 
     return oracle.paged_attention(q, kc, vc, w.block_tables, w.seq_lens, w.query_start_loc, w.scale, w.dtype,
-                                  w.causal)
+                                  w.causal, num_threads=num_threads)
 
 
 def oracle_setup_fp8(w):
@@ -253,11 +253,11 @@ def oracle_setup_fp8(w):
     return (kc, vc, ks, vs), W.raw_numpy(w.q)
 
 
-def oracle_step_fp8(w, pools, q):
+def oracle_step_fp8(w, pools, q, num_threads=0):
     import oracle
 
     return oracle.paged_attention_fp8(q, w.dtype, *pools, w.block_tables, w.seq_lens, w.query_start_loc, w.scale,
-                                      w.causal)
+                                      w.causal, num_threads=num_threads)
 
 
 def fp8_kv_bytes(w):
@@ -280,12 +280,13 @@ def host_sample_workload(name):
 
 
 def oracle_runner(w, fp8):
-    """(one oracle step as a callable, K/V bytes it reads) for a host workload."""
+    """(one oracle step as a callable taking a thread count, 0 = all cores;
+    K/V bytes it reads) for a host workload."""
     if fp8:
         pools, q = oracle_setup_fp8(w)
-        return (lambda: oracle_step_fp8(w, pools, q)), fp8_kv_bytes(w)
+        return (lambda nt=0: oracle_step_fp8(w, pools, q, nt)), fp8_kv_bytes(w)
     kc, vc, q = oracle_setup(w)
-    return (lambda: oracle_step(w, kc, vc, q)), w.kv_bytes_read()
+    return (lambda nt=0: oracle_step(w, kc, vc, q, nt)), w.kv_bytes_read()
 
 
 def cpu_sample(name, budget_s=10.0, fp8=False):
@@ -295,17 +296,26 @@ def cpu_sample(name, budget_s=10.0, fp8=False):
 
     w = host_sample_workload(name)
     run, per_step = oracle_runner(w, fp8)
-    reps, t = 0, time.perf_counter()
-    while True:
-        run()
-        reps += 1
-        el = time.perf_counter() - t
-        if el >= budget_s:
-            break
-    return {"value": per_step * reps / el / 1e9, "unit": "GB/s", "cores": oracle.max_threads(), "kind": "oracle",
+    cores = oracle.max_threads()
+
+    def timed_reps(nt, budget):
+        reps, t = 0, time.perf_counter()
+        while True:
+            run(nt)
+            reps += 1
+            el = time.perf_counter() - t
+            if el >= budget:
+                return reps, el
+
+    reps, el = timed_reps(0, budget_s)
+    # then one core (last: the oracle's thread count persists in the process)
+    reps1, el1 = timed_reps(1, budget_s / 3)
+    return {"value": per_step * reps / el / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "%d requests of the same generators (%d context tokens) x %d, fp64 C oracle with OpenMP%s, "
                       "%.1f s" % (w.num_seqs, int(w.seq_lens.sum()), reps, ", FP8 cache" if fp8 else "", el),
-            "seq_per_s": w.num_seqs * reps / el}
+            "seq_per_s": w.num_seqs * reps / el,
+            "single_core": {"value": per_step * reps1 / el1 / 1e9, "unit": "GB/s",
+                            "seq_per_s": w.num_seqs * reps1 / el1, "reps": reps1}}
 
 
 def run_reference(args, rank):
@@ -623,6 +633,17 @@ def main():
     ms = timed(lambda i: step_graphs[i % copies].replay(), args.steps)
     clk = clocks.stop() if rank == 0 and not args.no_extras else None
     kern_ms = timed(lambda i: kern_graphs[i % copies].replay(), args.steps) / args.steps
+    # the median of 51 launches timed one by one (CUDA events around each replay)
+    kern_med_us = None
+    if not args.no_extras:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(51)]
+        torch.cuda.synchronize()
+        for j, (ea, eb) in enumerate(evs):
+            ea.record()
+            kern_graphs[j % copies].replay()
+            eb.record()
+        torch.cuda.synchronize()
+        kern_med_us = statistics.median(ea.elapsed_time(eb) for ea, eb in evs) * 1e3
     # the varlen mix's two parts, each as a pa_varlen call of its own over the
     # same pools (prefill chunks: tensor-bound; decode rows: HBM-bound); in the
     # mixed call they share one launch, so these times do not add up to it
@@ -768,7 +789,7 @@ def main():
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
                 "traffic": traffic_record(args.workload + ("_fp8" if fp8 else ""), "pa_decode_tc.cu"),
-                "kernel_us": kern_ms * 1e3}
+                "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
     else:
         fl = varlen_flops(w)
         achieved = fl / (kern_ms / 1e3) / 1e12
@@ -778,7 +799,8 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": kind + " bf16_tflops (burst)",
                 "algorithmic_flops": fl, "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
                 "unique_kv_bytes": unique_kv_bytes(w), "parts": parts,
-                "traffic": traffic_record(args.workload, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3}
+                "traffic": traffic_record(args.workload, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3,
+                "kernel_us_median_of_51": kern_med_us}
 
     if rank == 0:
         line = {
