@@ -41,3 +41,25 @@ def test_varlen_flops_of_the_parts_add_up():
     # a decode row attends to all L keys: 4 Hq hd L flops
     i = int(dec[0])
     assert bench.varlen_flops(w, [i]) == 4.0 * w.num_heads * w.head_dim * int(w.seq_lens[i])
+
+
+def test_reference_arm_prints_the_contract_line(capsys):
+    """The reference arm (the CPU oracle, rank 0) prints one JSON line with
+    the GPU arm's metric, unit and workload name, and no host copies."""
+    import json
+
+    class Args:
+        workload = "tiny_decode"
+        kv_dtype = "native"
+        steps = 2
+        warmup = 1
+
+    bench.run_reference(Args(), rank=0)
+    lines = [ln for ln in capsys.readouterr().out.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "GB/s"
+    assert d["value"] > 0 and d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == W.tiny_decode().name
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
