@@ -85,7 +85,8 @@ typedef enum {
     PA_OPT_DECODE_CTAS = 2,
     /* Varlen kernel: 0 automatic (default: the tcgen05 kernel where it
      * applies, else the CUDA-core kernel), 1 the CUDA-core kernel, 2 the
-     * mma.sync tensor-core kernel, 3 the tcgen05 (tensor-memory) kernel. */
+     * tcgen05 (tensor-memory) kernel (PA_ERR_UNSUPPORTED where it does not
+     * apply). */
     PA_OPT_VARLEN_KERNEL = 3,
     /* Code-cache decode, head_dim 128: work the two tiles of a pipeline stage
      * that belong to one (sequence, KV head) as one 32-token step (one
@@ -352,9 +353,17 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
  * until process exit.  A problem whose scratch (pa_decode_workspace_size
  * with default options) exceeds 8 MiB returns PA_ERR_WORKSPACE before
  * anything is enqueued.  The call allocates nothing.  The first call with a
- * device current looks up that device's array address; make it before any
- * stream capture.  All calls on a device share the array: calls whose
+ * device current looks up that device's array address (again after the
+ * device's context was replaced, e.g. by cudaDeviceReset); make it before
+ * any stream capture.  All calls on a device share the array: calls whose
  * kernels overlap on the GPU race and must be ordered by the caller.
+ * Check mode (PA_OPT_CHECK_MODE) applies as for pa_decode: lengths and
+ * tables are copied to the host and validated (PA_ERR_INDEX) before launch.
+ * The array need not start at zero: per-unit counts carry a tag that each
+ * call makes afresh.  After a bounded wait ran out (pa_device_status ->
+ * PA_ERR_TIMEOUT), counts may be left part-way: before launching that same
+ * work again with the same tag (a re-run of an already-recorded launch),
+ * call pa_decode_noalloc_reset.
  */
 PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int32_t max_blocks,
@@ -362,6 +371,16 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
                                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                    int32_t block_size, int32_t max_context, float scale, int dtype,
                                    void* stream);
+
+/*
+ * pa_decode_noalloc_reset -- zeroes the current device's pa_decode_noalloc
+ * scratch array (8 MiB) on `stream` with cudaMemsetAsync; allocates nothing.
+ * The pages have no counterpart.  Needed only after PA_ERR_TIMEOUT (see
+ * pa_decode_noalloc); ordered like any other work on the stream, so it must
+ * not overlap a pa_decode_noalloc kernel on another stream.  Returns
+ * PA_ERR_CUDA if the array's address cannot be had or the memset fails.
+ */
+PA_API pa_status pa_decode_noalloc_reset(void* stream);
 
 #ifdef __cplusplus
 }

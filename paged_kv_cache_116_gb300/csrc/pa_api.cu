@@ -112,6 +112,17 @@ namespace pa {
 // Sets the reason pa_last_error() reports (used by entry points defined in
 // other translation units).
 void record_error(const std::string& msg) { g_last_error = msg; }
+
+bool check_mode_on() { return check_mode(); }
+
+int check_decode_indices(const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t num_blocks, int32_t block_size, int32_t max_context,
+                         cudaStream_t stream) {
+    pa_status err = PA_OK;
+    std::vector<int32_t> lens;
+    if (!to_host(lens, context_lens, num_seqs, stream, &err)) return err;
+    return check_tables(block_tables, num_seqs, max_blocks, lens, num_blocks, block_size, max_context, stream);
+}
 }  // namespace pa
 
 extern "C" {
@@ -133,7 +144,7 @@ const char* pa_last_error(void) { return g_last_error.c_str(); }
 
 pa_status pa_set_option(int option, int64_t value) {
     if (option < 0 || option > PA_OPT_FP8_PAIR_STEP) return fail(PA_ERR_INVALID_ARG, "unknown option");
-    if ((option == PA_OPT_DECODE_KERNEL && value > 2) || (option == PA_OPT_VARLEN_KERNEL && value > 3) ||
+    if ((option == PA_OPT_DECODE_KERNEL && value > 2) || (option == PA_OPT_VARLEN_KERNEL && value > 2) ||
         (option == PA_OPT_FP8_PAIR_STEP && value > 2))
         return fail(PA_ERR_INVALID_ARG, "unknown kernel choice");
     if (value < 0) return fail(PA_ERR_INVALID_ARG, "option values are non-negative");
@@ -152,8 +163,7 @@ pa_status pa_device_status(int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "pa_device_status");
     const uint32_t bits =
-        pa::decode_tc_status(clear != 0) | pa::varlen_tc_status(clear != 0) | pa::varlen_umma_status(clear != 0) |
-        pa::selftest_status(clear != 0);
+        pa::decode_tc_status(clear != 0) | pa::varlen_umma_status(clear != 0) | pa::selftest_status(clear != 0);
     if (bits & 1u) return fail(PA_ERR_TIMEOUT, "a kernel's bounded barrier wait ran out");
     return PA_OK;
 }
@@ -582,14 +592,12 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
-    const bool tc_ok = pa::varlen_tc_supported(dtype, head_dim, block_size);
     const bool um_ok = pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
     const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
-    if ((want == 2 && !tc_ok) || (want == 3 && !um_ok))
-        return fail(PA_ERR_UNSUPPORTED, "the tensor-core varlen kernels take bf16/f16 and head_dim 64/128; "
-                                        "mma.sync takes block_size 16, tcgen05 8 or a multiple of 16");
-    const bool use_um = um_ok && (want == 3 || want == 0);
-    const bool use_tc = !use_um && tc_ok && (want == 2 || want == 0);
+    if (want == 2 && !um_ok)
+        return fail(PA_ERR_UNSUPPORTED, "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128 and "
+                                        "block_size 8 or a multiple of 16");
+    const bool use_um = um_ok && (want == 2 || want == 0);
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
         pa_status err = PA_OK;
@@ -626,10 +634,9 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.dtype = dtype;
-    if (use_um || use_tc) {
+    if (use_um) {
         std::string err;
-        cudaError_t e = use_um ? pa::launch_varlen_umma(a, num_blocks, &err, st)
-                               : pa::launch_varlen_tc(a, num_blocks, &err, st);
+        cudaError_t e = pa::launch_varlen_umma(a, num_blocks, &err, st);
         if (e != cudaSuccess)
             return err.empty() ? cuda_fail(e, "pa_varlen launch") : fail(PA_ERR_CUDA, "pa_varlen: " + err);
         return PA_OK;

@@ -1,6 +1,7 @@
 // pa_decode_noalloc.cu -- pa_decode_noalloc: the tensor-core decode with its
 // scratch in a fixed device array owned by the library instead of a
-// caller-supplied workspace.
+// caller-supplied workspace; and pa_decode_noalloc_reset, which clears that
+// array.
 //
 // Who needs it: callers that must not allocate device memory at the time
 // they run the decode -- an inference runtime or plugin host that owns all
@@ -12,12 +13,19 @@
 //
 // The scratch is one file-scope array per device (kNoAllocScratchBytes,
 // 8 MiB), present from module load until the process exits.  Its device
-// address is looked up once per device with cudaGetSymbolAddress, on the
-// first call made with that device current; make that first call before any
-// stream capture.  Every call on a device shares the array, so two calls
-// whose kernels overlap on the GPU (different streams without ordering)
-// race on it.  Nothing in it has to start at zero: the per-unit counts carry
-// a per-launch tag, and stale contents from an earlier call are ignored.
+// address is looked up with cudaGetSymbolAddress on the first call made
+// with that device current, and again whenever the device's context has
+// changed since (after cudaDeviceReset the module is loaded afresh and the
+// old address is gone); make that first call before any stream capture.
+// Every call on a device shares the array, so two calls whose kernels
+// overlap on the GPU (different streams without ordering) race on it.
+// Nothing in it has to start at zero for an ordinary call: the per-unit
+// counts carry a per-launch tag, and counts left by an earlier launch are
+// ignored.  A launch that gave up on a bounded wait (PA_ERR_TIMEOUT) can
+// leave a count part-way; that is harmless for later calls (new tags) but
+// not for a re-run of that same launch, which carries the same tag --
+// pa_decode_noalloc_reset zeroes the array first.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -35,30 +43,69 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+// The array's device address per device, with the id of the context it was
+// looked up in.
+struct ScratchSlot {
+    void* addr = nullptr;
+    unsigned long long ctx_id = 0;
+};
 std::mutex g_setup_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchSlot g_scratch[kMaxDevices];
 
 pa_status noalloc_fail(pa_status st, const std::string& msg) {
     pa::record_error(msg);  // read back with pa_last_error()
     return st;
 }
 
-// Device address of this device's scratch array (set up on first use).
+// Id of the calling thread's current context (0 if the driver cannot say).
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+        get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of this device's scratch array (looked up on first use,
+// and again when the device's context has changed).
 pa_status scratch_for_current_device(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return noalloc_fail(PA_ERR_CUDA, std::string("cudaGetDevice: ") + cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return noalloc_fail(PA_ERR_UNSUPPORTED, "device ordinal beyond 63");
+    // Before the first runtime call that needs it, no context may be current
+    // yet (id 0); the runtime makes the primary context current inside
+    // cudaGetSymbolAddress, and the id is read again after it.
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    ScratchSlot& slot = g_scratch[dev];
+    const unsigned long long id = current_context_id();
+    if (slot.addr == nullptr || (id != 0 && id != slot.ctx_id)) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr)
             return noalloc_fail(PA_ERR_CUDA, std::string("cudaGetSymbolAddress of the scratch array: ") +
                                                  cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        slot.addr = p;
+        slot.ctx_id = current_context_id();
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return PA_OK;
 }
 
@@ -98,6 +145,13 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
                                                   " bytes of scratch; pa_decode_noalloc holds at most " +
                                                   std::to_string(kNoAllocScratchBytes) +
                                                   " (use pa_decode with a workspace)");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (pa::check_mode_on()) {
+        // host copies of the lengths and tables only; nothing on the device
+        const int st = pa::check_decode_indices(block_tables, max_blocks, context_lens, num_seqs, num_blocks,
+                                                block_size, max_context, s);
+        if (st != PA_OK) return static_cast<pa_status>(st);
+    }
     void* scratch = nullptr;
     pa_status st = scratch_for_current_device(&scratch);
     if (st != PA_OK) return st;
@@ -121,7 +175,6 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
     a.causal = 1;
     a.dtype = dtype;
     const int64_t elt = pa::elt_size(dtype);
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int32_t s0 = 0; s0 < num_seqs; s0 += pa::kDecodeMaxSeqsPerLaunch) {
         pa::AttnArgs c = a;
         const int32_t cnt = std::min(num_seqs - s0, pa::kDecodeMaxSeqsPerLaunch);
@@ -136,6 +189,17 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
         if (e != cudaSuccess)
             return noalloc_fail(PA_ERR_CUDA, "pa_decode_noalloc: " + (err.empty() ? std::string(cudaGetErrorString(e)) : err));
     }
+    return PA_OK;
+}
+
+pa_status pa_decode_noalloc_reset(void* stream) {
+    void* scratch = nullptr;
+    pa_status st = scratch_for_current_device(&scratch);
+    if (st != PA_OK) return st;
+    // a memset node on the caller's stream: no allocation
+    cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess)
+        return noalloc_fail(PA_ERR_CUDA, std::string("pa_decode_noalloc_reset: ") + cudaGetErrorString(e));
     return PA_OK;
 }
 

@@ -28,6 +28,16 @@ constexpr uint32_t kMaxPolls = 1u << 24;
 // Reason reported by pa_last_error() for the calling thread (pa_api.cu).
 void record_error(const std::string& msg);
 
+// Check mode (PA_OPT_CHECK_MODE) for entry points outside pa_api.cu: whether
+// it is on, and the decode's index validation (lengths in [0, max_context],
+// tables long enough, block ids in [0, num_blocks)) on host copies of the
+// index arrays.  Returns a pa_status value (PA_OK, PA_ERR_INDEX or
+// PA_ERR_CUDA) and records the reason for pa_last_error().
+bool check_mode_on();
+int check_decode_indices(const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t num_blocks, int32_t block_size, int32_t max_context,
+                         cudaStream_t stream);
+
 // ---- copy kernels (pa_copy.cu)
 cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks, const int32_t* seq_idx,
                                 const int64_t* positions, int64_t n, int32_t block_size, int64_t* slot_out,
@@ -112,11 +122,6 @@ uint32_t decode_tc_status(bool clear);
 // timeout bit (pa_selftest_wait_timeout).
 cudaError_t launch_selftest_wait(uint32_t polls, cudaStream_t stream);
 uint32_t selftest_status(bool clear);
-
-// ---- tensor-core varlen (pa_varlen_tc.cu)
-bool varlen_tc_supported(int dtype, int head_dim, int block_size);
-cudaError_t launch_varlen_tc(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream);
-uint32_t varlen_tc_status(bool clear);
 
 // ---- tcgen05 varlen (pa_varlen_umma.cu)
 bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group);

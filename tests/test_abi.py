@@ -50,6 +50,9 @@ def test_status_strings_and_options(lib):
     assert lib.pa_set_option(4, 3) == 1  # no such choice
     assert lib.pa_set_option(4, 0) == 0
     assert lib.pa_set_option(0, -1) == 1  # negative value
+    assert lib.pa_set_option(3, 2) == 0 and lib.pa_get_option(3) == 2  # varlen: the tcgen05 kernel
+    assert lib.pa_set_option(3, 3) == 1  # no such varlen kernel
+    assert lib.pa_set_option(3, 0) == 0
 
 
 def test_argument_errors_need_no_gpu(lib):

@@ -74,14 +74,13 @@ def test_gqa_decode_batch_full(pa, kernel):
     compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel), exact)
 
 
-def test_long_context_decode_sampled(pa):
+def test_long_context_decode_full(pa):
+    """8 x 32,768 tokens: every unit is split over many warps and merged;
+    all eight sequences' outputs against the oracle."""
     w = W.long_context_decode(device=DEV)
     kc, vc, bt = device_caches(w, DEV)
-    sel = np.zeros(w.num_seqs, np.uint8)
-    sel[[0, 5]] = 1
-    okc, ovc = oracle_caches(w)
-    exact = oracle_attention(w, okc, ovc, seq_select=sel)
-    compare(w, run_decode(pa, w, kc, vc, bt), exact, rows=np.where(sel)[0])
+    exact = oracle_attention(w)
+    compare(w, run_decode(pa, w, kc, vc, bt), exact)
 
 
 def test_mha_decode_fp16_full(pa):

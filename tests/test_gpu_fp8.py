@@ -144,14 +144,29 @@ def test_gqa_decode_batch_fp8_full(pa):
         compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt, kernel=kernel), exact)
 
 
-def test_mha_decode_fp8_32seq(pa):
-    """The 13B-style MHA shape (f16, Hq = Hkv = 40, N(0, 0.5) values) on the
-    first 32 sequences of its lognormal length mix."""
-    lens = W.mha_lengths(128, 0)[:32]
-    w = W.decode_workload("mha_fp8", "f16", 16, 40, 40, 128, lens, std=0.5, seed=0, device=DEV)
+def test_mha_decode_fp8_full(pa):
+    """The 13B-style MHA batch (f16, Hq = Hkv = 40, N(0, 0.5) values, all 128
+    sequences of its lognormal length mix) over an FP8 cache."""
+    w = W.mha_decode(device=DEV)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal((kc, vc, ks, vs), opools)
+    exact = oracle_fp8_attention(w, *opools)
+    compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+def test_long_context_decode_fp8_full(pa, pair):
+    """8 x 32,768 tokens over an FP8 cache, all eight sequences, with the
+    32-token pair step off (1) and on (2)."""
+    w = W.long_context_decode(device=DEV)
     kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
     exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
-    compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
+    pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, pair)
+    try:
+        compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
+    finally:
+        pa.pa_set_option(pa.PA_OPT_FP8_PAIR_STEP, 0)
 
 
 def test_tiny_decode_fp8_fp32_queries(pa):

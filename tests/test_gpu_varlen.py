@@ -125,21 +125,20 @@ for _i in range(12):
 
 @pytest.mark.parametrize("dt,hd,g,hkv,lens,qlens,seed", TC_CASES)
 def test_random_varlen_tensor_core_kernels(pa, dt, hd, g, hkv, lens, qlens, seed):
-    """Both tensor-core kernels: mma.sync (2) and tcgen05 with tensor memory (3)."""
+    """The tcgen05 kernel (option 2), with and without a workspace argument."""
     w = W.varlen_workload("rand_tc", dt, 16, g * hkv, hkv, hd, lens, qlens, seed=100 + seed)
     kc, vc, bt = device_caches(w, DEV)
     for causal in (True, False):
         exact = oracle_attention(w, causal=causal)
-        for kernel in (2, 3):
-            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=kernel), exact)
-        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3, routed=True), exact)
+        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2), exact)
+        compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2, routed=True), exact)
 
 
 def test_varlen_kernels_agree_on_mixed_step(pa):
     w = W.mixed_varlen(num_chunks=4, num_groups=6, device=DEV)
     kc, vc, bt = device_caches(w, DEV)
     exact = oracle_attention(w)
-    for kernel in (1, 2, 3):
+    for kernel in (1, 2):
         got = run_varlen(pa, w, kc, vc, bt, kernel=kernel).double().cpu().numpy()
         assert within_tol(got, exact, w.dtype)[0], "kernel %d" % kernel
 
@@ -147,11 +146,11 @@ def test_varlen_kernels_agree_on_mixed_step(pa):
 def test_mixed_varlen_full_tcgen05(pa):
     w = W.mixed_varlen(device=DEV)
     kc, vc, bt = device_caches(w, DEV)
-    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=3, routed=True), oracle_attention(w))
+    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=2, routed=True), oracle_attention(w))
     pa.pa_device_status(clear=True)  # raises if a kernel recorded a timeout
 
 
-@pytest.mark.parametrize("kernel,routed", [(2, False), (3, False), (3, True)])
+@pytest.mark.parametrize("kernel,routed", [(1, False), (2, False), (2, True)])
 def test_varlen_permutation_bit_identical(pa, kernel, routed):
     w = W.varlen_workload("perm_v", "bf16", 16, 12, 2, 128, [300, 81, 17, 1000], [1, 81, 5, 130], seed=3)
     kc, vc, bt = device_caches(w, DEV)
@@ -177,4 +176,4 @@ def test_varlen_tcgen05_block_sizes(pa, bs):
     for causal in (True, False):
         exact = oracle_attention(w, causal=causal)
         for routed in (False, True):
-            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=3, routed=routed), exact)
+            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2, routed=routed), exact)

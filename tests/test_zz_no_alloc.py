@@ -4,10 +4,13 @@ own pool, a latency-critical loop that cannot risk an allocation's device
 synchronisation).  Its split-KV scratch is the library's fixed per-device
 array instead of a workspace argument.
 
-Checked through the C ABI against pa_decode (which takes a caller-allocated
-workspace) on two calls in a row -- two different batches, so the second
-call runs over the scratch the first one left behind -- within the tests'
-attention tolerance.  This file is collected last on purpose.
+Every case goes through the C ABI and is checked two ways: against the
+oracle within the tests' attention tolerance, and bit for bit against
+pa_decode (which takes a caller-allocated workspace) on the same inputs --
+both launch the same kernel with the same grid, so any difference would be
+a scratch-layout slip.  Calls follow one another on the shared array, so
+each runs over what the previous one left behind.  This file is collected
+last on purpose.
 """
 import numpy as np
 import pytest
@@ -15,7 +18,7 @@ import torch
 
 from paged_kv_cache_116_gb300 import workloads as W
 
-from helpers import device_caches, within_tol
+from helpers import device_caches, oracle_attention, within_tol
 
 pytestmark = pytest.mark.gpu
 
@@ -32,30 +35,110 @@ def pa():
     return pa
 
 
-def _reference_decode(pa, w, kc, vc, bt, lens, mc):
+def _inputs(w):
+    kc, vc, bt = device_caches(w, DEV)
+    lens = torch.from_numpy(w.seq_lens).to(DEV)
+    return kc, vc, bt, lens, int(w.seq_lens.max())
+
+
+def _workspace_decode(pa, w, kc, vc, bt, lens, mc):
     ws_bytes = pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size, mc,
                                            W.TORCH_DTYPES[w.dtype])
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=DEV)
-    out = torch.empty((w.num_seqs, w.num_heads, w.head_dim), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
+    out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
     pa.pa_decode(out, w.q.to(DEV), kc, vc, bt, lens, mc, w.scale, workspace=ws)
     return out
 
 
-def test_noalloc_matches_workspace_decode_twice(pa):
-    batches = [
-        W.decode_workload("na1", "bf16", 16, 32, 8, 128, W.gqa_batch_lengths(24), seed=11),
-        W.decode_workload("na2", "f16", 16, 8, 2, 128, [1, 900, 33, 2048, 16, 470, 5], seed=12),
-    ]
-    for w in batches:  # two calls in a row on the shared scratch
-        kc, vc, bt = device_caches(w, DEV)
-        lens = torch.from_numpy(w.seq_lens).to(DEV)
-        mc = int(w.seq_lens.max())
-        ref = _reference_decode(pa, w, kc, vc, bt, lens, mc)
-        got = torch.full_like(ref, float("nan"))
-        pa.pa_decode_noalloc(got, w.q.to(DEV), kc, vc, bt, lens, mc, w.scale)
+def _noalloc_decode(pa, w, kc, vc, bt, lens, mc):
+    out = torch.full((w.num_seqs, w.num_heads, w.head_dim), float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
+    pa.pa_decode_noalloc(out, w.q.to(DEV), kc, vc, bt, lens, mc, w.scale)
+    return out
+
+
+def _check(pa, w):
+    kc, vc, bt, lens, mc = _inputs(w)
+    got = _noalloc_decode(pa, w, kc, vc, bt, lens, mc)
+    ref = _workspace_decode(pa, w, kc, vc, bt, lens, mc)
+    torch.cuda.synchronize()
+    pa.pa_device_status(clear=True)  # raises if a bounded wait ran out
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), "pa_decode_noalloc differs from pa_decode (%s)" % w.name
+    ok, err = within_tol(got.double().cpu().numpy(), oracle_attention(w), w.dtype)
+    assert ok, "pa_decode_noalloc differs from the oracle by %.3g (%s)" % (err, w.name)
+
+
+# shapes chosen so that each fits the 8 MiB array yet splits units between
+# warps: the G <= 8 and G > 8 kernel instances, head_dim 64 / 128 / 256,
+# 8- and 32-token blocks
+SHAPES = [
+    ("g4_hd128_bf16", lambda: W.decode_workload("na_g4", "bf16", 16, 32, 8, 128, W.gqa_batch_lengths(24), seed=11)),
+    ("g1_hd128_f16", lambda: W.decode_workload("na_mha", "f16", 16, 8, 8, 128, [1, 900, 33, 2048, 16, 470, 5],
+                                               seed=12)),
+    ("g12_hd128_f16", lambda: W.decode_workload("na_g12", "f16", 16, 24, 2, 128, [1, 130, 257, 500], seed=13)),
+    ("g16_hd64_bf16", lambda: W.decode_workload("na_g16", "bf16", 16, 16, 1, 64, [700, 31, 1, 333], seed=14)),
+    ("g4_hd256_bf16", lambda: W.decode_workload("na_hd256", "bf16", 32, 8, 2, 256, [1000, 65, 2, 400], seed=15)),
+    ("g8_hd64_bs8_f16", lambda: W.decode_workload("na_bs8", "f16", 8, 16, 2, 64, [9, 800, 17, 1], seed=16)),
+]
+
+
+@pytest.mark.parametrize("name,make", SHAPES)
+def test_noalloc_equals_workspace_decode_and_oracle(pa, name, make):
+    _check(pa, make())
+
+
+def test_noalloc_two_calls_in_a_row_over_stale_scratch(pa):
+    """The first call splits two long sequences over every warp, so its
+    partial records fill the array well past the second call's count
+    prefix (1,000 sequences x 8 KV heads x 8 bytes); the second call must
+    ignore those leftovers."""
+    first = W.decode_workload("na_fill", "bf16", 16, 32, 8, 128, [3000, 2500], seed=21)
+    second = W.decode_workload("na_after", "bf16", 16, 32, 8, 128, np.random.default_rng(22).integers(1, 40, 1000)
+                               .tolist(), seed=22)
+    _check(pa, first)
+    _check(pa, second)
+
+
+def test_noalloc_more_sequences_than_one_launch_takes(pa):
+    """4,200 one-query sequences at G = 1 run as two launches (4,096 + 104)
+    on the same array, one after the other."""
+    lens = np.random.default_rng(31).integers(1, 40, 4200).tolist()
+    _check(pa, W.decode_workload("na_4200", "bf16", 16, 2, 2, 128, lens, seed=31))
+
+
+def test_noalloc_reset_then_decode(pa):
+    """pa_decode_noalloc_reset zeroes the array; the next call is unchanged."""
+    w = W.decode_workload("na_reset", "bf16", 16, 32, 8, 128, [1500, 700, 3], seed=41)
+    kc, vc, bt, lens, mc = _inputs(w)
+    before = _noalloc_decode(pa, w, kc, vc, bt, lens, mc)
+    pa.pa_decode_noalloc_reset()
+    after = _noalloc_decode(pa, w, kc, vc, bt, lens, mc)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # a reset ordered on another stream
+        pa.pa_decode_noalloc_reset(side)
+    torch.cuda.current_stream().wait_stream(side)
+    again = _noalloc_decode(pa, w, kc, vc, bt, lens, mc)
+    ref = _workspace_decode(pa, w, kc, vc, bt, lens, mc)
+    torch.cuda.synchronize()
+    for got in (before, after, again):
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
+def test_noalloc_check_mode_rejects_bad_tables(pa):
+    w = W.decode_workload("na_check", "bf16", 16, 8, 2, 128, [40, 17], seed=51)
+    kc, vc, bt, lens, mc = _inputs(w)
+    bad = bt.clone()
+    bad[1, 0] = w.num_blocks  # outside the pool
+    out = torch.zeros((w.num_seqs, w.num_heads, w.head_dim), dtype=torch.bfloat16, device=DEV)
+    pa.pa_set_check_mode(True)
+    try:
+        with pytest.raises(pa.PAError, match="PA_ERR_INDEX"):
+            pa.pa_decode_noalloc(out, w.q.to(DEV), kc, vc, bad, lens, mc, w.scale)
         torch.cuda.synchronize()
-        ok, err = within_tol(got.double().cpu().numpy(), ref.double().cpu().numpy(), w.dtype)
-        assert ok, "pa_decode_noalloc differs from pa_decode by %.3g (%s)" % (err, w.name)
+        assert torch.count_nonzero(out).item() == 0  # nothing ran
+        pa.pa_decode_noalloc(out, w.q.to(DEV), kc, vc, bt, lens, mc, w.scale)  # valid tables pass
+    finally:
+        pa.pa_set_check_mode(False)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(pa):
