@@ -589,7 +589,9 @@ def main():
     # no more (sequence, KV head) units than the grid's warps, 3 CTAs x 4 warps per SM)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     fused_in_kernel = tc_decode and (not fp8 or (hd == 128 and S * hkv <= sms * 3 * 4))
-    launches_per_step = (1 if fused_in_kernel else 2) if fused else 3 + (1 if pairs.shape[0] else 0)
+    # the tensor-core decode is two launches: the decode and its split merge
+    launches_per_step = ((1 if fused_in_kernel else 2) if fused else 3 + (1 if pairs.shape[0] else 0)) + \
+        (1 if tc_decode else 0)
 
     for i in range(max(args.warmup, 3)):
         step(i)

@@ -359,11 +359,10 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
  * kernels overlap on the GPU race and must be ordered by the caller.
  * Check mode (PA_OPT_CHECK_MODE) applies as for pa_decode: lengths and
  * tables are copied to the host and validated (PA_ERR_INDEX) before launch.
- * The array need not start at zero: per-unit counts carry a tag that each
- * call makes afresh.  After a bounded wait ran out (pa_device_status ->
- * PA_ERR_TIMEOUT), counts may be left part-way: before launching that same
- * work again with the same tag (a re-run of an already-recorded launch),
- * call pa_decode_noalloc_reset.
+ * The array need not start at zero, and no call reads what an earlier one
+ * left in it (each launch writes every split record and unit descriptor its
+ * merge reads), so it never needs clearing -- not even after a bounded wait
+ * ran out (PA_ERR_TIMEOUT).
  */
 PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* block_tables, int32_t max_blocks,
@@ -371,16 +370,6 @@ PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache
                                    int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
                                    int32_t block_size, int32_t max_context, float scale, int dtype,
                                    void* stream);
-
-/*
- * pa_decode_noalloc_reset -- zeroes the current device's pa_decode_noalloc
- * scratch array (8 MiB) on `stream` with cudaMemsetAsync; allocates nothing.
- * The pages have no counterpart.  Needed only after PA_ERR_TIMEOUT (see
- * pa_decode_noalloc); ordered like any other work on the stream, so it must
- * not overlap a pa_decode_noalloc kernel on another stream.  Returns
- * PA_ERR_CUDA if the array's address cannot be had or the memset fails.
- */
-PA_API pa_status pa_decode_noalloc_reset(void* stream);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ POOL_DTYPE_CODE = {**DTYPE_CODE, torch.uint8: PA_FP8_E4M3, torch.float8_e4m3fn: 
 
 EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option", "pa_set_check_mode",
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
-           "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc", "pa_decode_noalloc_reset",
+           "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
            "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8",
            "pa_decode_append_fp8", "pa_selftest_wait_timeout")
 
@@ -69,7 +69,6 @@ def lib():
                               vp], ci),
         "pa_varlen_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32, ci], sz),
         "pa_decode_noalloc": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp], ci),
-        "pa_decode_noalloc_reset": ([vp], ci),
         "pa_varlen": ([vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, cf, ci, ci, vp,
                        sz, vp], ci),
     }
@@ -296,12 +295,6 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, max_
                                  float(scale), _dtype(q), _stream(stream))
     _check(st, "pa_decode_noalloc")
     return out
-
-
-def pa_decode_noalloc_reset(stream=None):
-    """Zero the current device's pa_decode_noalloc scratch array (needed only
-    after a PA_ERR_TIMEOUT, before re-running the same launch)."""
-    _check(lib().pa_decode_noalloc_reset(_stream(stream)), "pa_decode_noalloc_reset")
 
 
 def pa_varlen_workspace_size(num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, block_size, max_context,

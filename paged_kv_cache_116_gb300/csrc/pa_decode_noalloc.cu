@@ -1,7 +1,6 @@
 // pa_decode_noalloc.cu -- pa_decode_noalloc: the tensor-core decode with its
 // scratch in a fixed device array owned by the library instead of a
-// caller-supplied workspace; and pa_decode_noalloc_reset, which clears that
-// array.
+// caller-supplied workspace.
 //
 // Who needs it: callers that must not allocate device memory at the time
 // they run the decode -- an inference runtime or plugin host that owns all
@@ -19,12 +18,9 @@
 // old address is gone); make that first call before any stream capture.
 // Every call on a device shares the array, so two calls whose kernels
 // overlap on the GPU (different streams without ordering) race on it.
-// Nothing in it has to start at zero for an ordinary call: the per-unit
-// counts carry a per-launch tag, and counts left by an earlier launch are
-// ignored.  A launch that gave up on a bounded wait (PA_ERR_TIMEOUT) can
-// leave a count part-way; that is harmless for later calls (new tags) but
-// not for a re-run of that same launch, which carries the same tag --
-// pa_decode_noalloc_reset zeroes the array first.
+// Nothing in it has to start at zero, and nothing a call leaves behind is
+// read by a later one: each launch writes every split record and unit
+// descriptor its merge reads before the merge runs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -189,17 +185,6 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
         if (e != cudaSuccess)
             return noalloc_fail(PA_ERR_CUDA, "pa_decode_noalloc: " + (err.empty() ? std::string(cudaGetErrorString(e)) : err));
     }
-    return PA_OK;
-}
-
-pa_status pa_decode_noalloc_reset(void* stream) {
-    void* scratch = nullptr;
-    pa_status st = scratch_for_current_device(&scratch);
-    if (st != PA_OK) return st;
-    // a memset node on the caller's stream: no allocation
-    cudaError_t e = cudaMemsetAsync(scratch, 0, kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess)
-        return noalloc_fail(PA_ERR_CUDA, std::string("pa_decode_noalloc_reset: ") + cudaGetErrorString(e));
     return PA_OK;
 }
 

@@ -12,14 +12,14 @@
 //    flat list of Hkv * sum(ceil(L/16)) tiles, cut into equal contiguous ranges, one per
 //    warp of a persistent grid, so every warp streams the same number of
 //    bytes whatever the length mix.  A unit cut between warps leaves partial
-//    softmax states (m, l, unnormalised o) in the workspace; the last of the
-//    unit's warps to finish (an epoch-tagged atomic count per unit, so the
-//    workspace never needs clearing; the last one zeroes the count, so a
-//    CUDA-graph replay of the same launch counts afresh) merges them by their
-//    log-sum-exp, in
-//    a fixed order ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
-//    apart and merged by the online-softmax rule).  The cut depends only on
-//    the lengths, never on physical block ids.
+//    softmax states (m, l, unnormalised o) in the workspace -- written with
+//    no fence, count or wait, so a cut costs the streaming warp almost
+//    nothing -- and decode_merge_kernel, launched as this kernel's
+//    programmatic dependent, merges them by their log-sum-exp in a fixed
+//    order once the grid has completed ("aiqz.cc PagedAttention", §工程实现
+//    要点: blocks computed apart and merged by the online-softmax rule).  The
+//    workspace never needs clearing.  The cut depends only on the lengths,
+//    never on physical block ids.
 //  * Each warp runs its own R-deep ring of shared-memory stages (one or two
 //    16-token tiles each).  Several lanes issue, in one instruction, the TMA
 //    loads (cp.async.bulk.tensor, 128-byte swizzle) of a stage's K and V
@@ -65,7 +65,7 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <atomic>
+#include <algorithm>
 #include <mutex>
 #include <string>
 
@@ -90,9 +90,13 @@ struct TcParams {
     int32_t num_kv_heads;
     int32_t group;
     float scale_log2;
-    unsigned long long* ws_cnt;  // [num_seqs * num_kv_heads] (epoch << 16) | partials done
-    float* ws_part;              // [total_warps][2] records of group * (HD + 4) floats
-    unsigned long long epoch;    // this launch's tag, < 2^48, never reused by the process
+    // split merge: the number of tiles W (written by block 0), one
+    // descriptor per unit {first warp, last warp, the first warp's record
+    // slot or -1 when the unit needs no merge, 0}, and two records of
+    // group * (HD + 4) floats per warp
+    long long* ws_tiles;
+    int4* ws_desc;  // [num_seqs * num_kv_heads]
+    float* ws_part; // [total_warps][2]
     // append mode (k_new != nullptr): each sequence's token at position L-1
     // arrives in k_new / v_new [num_seqs, Hkv, HD]; it is written to the pool
     // and attended from these rows, not from the pool
@@ -159,37 +163,14 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
                  : "memory");
 }
 
-// T: element type of q and out.  FP8: the cache holds E4M3 codes plus
-// scales (the mma then runs in f16 whatever T is).
-template <typename T, int HD, int NT, bool FP8, bool PAIR>
-__global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
-    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                     const TcParams p) {
-    using Gm = Geo<HD, FP8>;
-    constexpr int NW = Pipe<HD, FP8>::NW, R = Pipe<HD, FP8>::R, KS = Gm::KS;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float* scl = reinterpret_cast<float*>(base + (size_t)NW * R * Gm::STAGE);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * (Gm::STAGE + Gm::SCL));
-    int32_t* prefix = reinterpret_cast<int32_t*>(bars + NW * R);
-    int32_t* lens = prefix + p.num_seqs + 1;  // context lengths, read once per CTA
-
+// 16-token tiles per sequence and their exclusive prefix over the batch,
+// into shared memory (prefix[S + 1]; lens[S] gets the lengths unless null).
+// Every thread of the block calls it; it ends with a block barrier.
+__device__ __forceinline__ void tile_prefix(const int32_t* context_lens, int S, int32_t* prefix, int32_t* lens) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
-
-    // With programmatic dependent launch this grid may start while the
-    // previous kernel on the stream (e.g. the K/V write) is still running;
-    // every input is read after this wait.
-    pdl_wait_primary();
-    if (threadIdx.x == 0) {
-        prefetch_tmap(&tmK);
-        prefetch_tmap(&tmV);
-    }
-
-    // ---- blocks per sequence and their exclusive prefix
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
-        const int L = p.context_lens[s];
-        lens[s] = L;
+        const int L = context_lens[s];
+        if (lens) lens[s] = L;
         prefix[s + 1] = L > 0 ? (L + BS - 1) / BS : 0;
     }
     if (threadIdx.x == 0) prefix[0] = 0;
@@ -212,13 +193,48 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
         }
     }
     __syncthreads();
+}
+
+// T: element type of q and out.  FP8: the cache holds E4M3 codes plus
+// scales (the mma then runs in f16 whatever T is).
+template <typename T, int HD, int NT, bool FP8, bool PAIR>
+__global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                     const TcParams p) {
+    using Gm = Geo<HD, FP8>;
+    constexpr int NW = Pipe<HD, FP8>::NW, R = Pipe<HD, FP8>::R, KS = Gm::KS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* scl = reinterpret_cast<float*>(base + (size_t)NW * R * Gm::STAGE);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + (size_t)NW * R * (Gm::STAGE + Gm::SCL));
+    int32_t* prefix = reinterpret_cast<int32_t*>(bars + NW * R);
+    int32_t* lens = prefix + p.num_seqs + 1;  // context lengths, read once per CTA
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+
+    // With programmatic dependent launch this grid may start while the
+    // previous kernel on the stream (e.g. the K/V write) is still running;
+    // every input is read after this wait.
+    if (threadIdx.x == 0) {  // kernel parameters: no need to wait for them
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    pdl_wait_primary();
+    // the split merge (the next launch) may be scheduled now; it waits for
+    // this grid to complete before it reads anything
+    pdl_launch_dependents();
+
+    tile_prefix(p.context_lens, S, prefix, lens);
 
     const int64_t W = (int64_t)prefix[S] * Hkv;
-    // sequences with no context get a zero row
+    if (blockIdx.x == 0 && threadIdx.x == 0) *p.ws_tiles = W;
+    // sequences with no context get a zero row (and nothing to merge)
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
         if (prefix[s + 1] == prefix[s]) {
             T* o = static_cast<T*>(p.out) + (int64_t)s * p.num_heads * HD;
             for (int e = threadIdx.x; e < p.num_heads * HD; e += blockDim.x) o[e] = Elt<T>::from_f(0.f);
+            for (int h = threadIdx.x; h < Hkv; h += blockDim.x) p.ws_desc[(int64_t)s * Hkv + h] = make_int4(0, 0, -1, 0);
         }
     }
 
@@ -426,42 +442,6 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
         if (p.k_new != nullptr) load_new_rows();
     };
 
-    // Combine the partial records of unit (cs, ch) held by warps w0..w1, in
-    // warp order; lanes split the group's G * HD outputs into runs of 16.
-    auto merge_unit = [&](int64_t w0, int64_t w1, int64_t U0) {
-        const int64_t st0 = w0 * W / TW;
-        T* out = static_cast<T*>(p.out) + ((int64_t)cs * p.num_heads + (int64_t)ch * G) * HD;
-        for (int base_e = lane * 16; base_e < G * HD; base_e += 32 * 16) {
-            const int j = base_e / HD, d0 = base_e - j * HD;
-            float M = -INFINITY, L = 0.f, o[16];
-#pragma unroll
-            for (int t = 0; t < 16; ++t) o[t] = 0.f;
-            for (int64_t w = w0; w <= w1; ++w) {
-                if (w * W / TW == (w + 1) * W / TW) continue;  // empty range
-                const int slot = (w == w0 && U0 > st0) ? 1 : 0;
-                const float* r = p.ws_part + (w * 2 + slot) * (int64_t)G * (HD + 4) + j * (HD + 4);
-                const float m = __ldcg(r + HD), l = __ldcg(r + HD + 1);
-                float4 a[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) a[t] = __ldcg(reinterpret_cast<const float4*>(r + d0) + t);
-                const float Mn = fmaxf(M, m);
-                const float c = exp2f(M - Mn), e = exp2f(m - Mn);
-                L = L * c + e * l;
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    o[4 * t + 0] = o[4 * t + 0] * c + e * a[t].x;
-                    o[4 * t + 1] = o[4 * t + 1] * c + e * a[t].y;
-                    o[4 * t + 2] = o[4 * t + 2] * c + e * a[t].z;
-                    o[4 * t + 3] = o[4 * t + 3] * c + e * a[t].w;
-                }
-                M = Mn;
-            }
-            const float inv = 1.f / L;
-#pragma unroll
-            for (int t = 0; t < 16; ++t) out[j * HD + d0 + t] = Elt<T>::from_f(o[t] * inv);
-        }
-    };
-
     // head dim of accumulator row g + 8 hi of m-tile mt
     auto odim = [&](int mt, int hi) -> int { return FP8 ? vb0 + 2 * mt + hi : mt * 16 + g + 8 * hi; };
 
@@ -478,7 +458,9 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 lt[nt][e] = l;
             }
         const bool complete = (seg_b0 == 0 && bend == nb);
+        int* desc = reinterpret_cast<int*>(p.ws_desc + (int64_t)cs * Hkv + ch);
         if (complete) {
+            if (lane == 0) *reinterpret_cast<int4*>(desc) = make_int4((int)gw, (int)gw, -1, 0);
             T* out = static_cast<T*>(p.out) + ((int64_t)cs * p.num_heads + (int64_t)ch * G) * HD;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -495,7 +477,17 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                     }
                 }
         } else {
+            // a piece of a unit cut between warps: its partial state goes to
+            // this warp's record (slot 0: the warp's first piece, 1: its
+            // last); decode_merge_kernel combines the pieces after this grid
             const int slot = first_seg ? 0 : 1;
+            if (lane == 0) {
+                if (seg_b0 == 0) {  // the unit's first piece: this warp is its first
+                    desc[0] = (int)gw;
+                    desc[2] = slot;
+                }
+                if (bend == nb) desc[1] = (int)gw;  // its last piece
+            }
             float* rec = p.ws_part + (gw * 2 + slot) * (int64_t)G * (HD + 4);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -515,34 +507,6 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                         }
                     }
                 }
-            __threadfence();
-            __syncwarp();
-            // the warps that hold this unit: [w0, w1], empty ranges excluded
-            const int64_t U0 = (int64_t)prefix[cs] * Hkv + (int64_t)ch * nb, U1 = U0 + nb;
-            const int64_t w0 = ((U0 + 1) * TW - 1) / W, w1 = (U1 * TW - 1) / W;
-            int last = 0;
-            if (lane == 0) {
-                int expected = 0;
-                for (int64_t w = w0; w <= w1; ++w) expected += (w * W / TW < (w + 1) * W / TW) ? 1 : 0;
-                unsigned long long* cnt = p.ws_cnt + (int64_t)cs * Hkv + ch;
-                unsigned long long cur = *reinterpret_cast<volatile unsigned long long*>(cnt), want;
-                while (true) {  // ends: each failed swap means another writer's succeeded
-                    want = ((cur >> 16) == p.epoch) ? cur + 1 : ((p.epoch << 16) | 1ull);
-                    const unsigned long long prev = atomicCAS(cnt, cur, want);
-                    if (prev == cur) break;
-                    cur = prev;
-                }
-                last = ((int)(want & 0xffffull) == expected) ? 1 : 0;
-                // The unit's count is complete: leave it at zero, so that a
-                // replay of this very launch (a CUDA graph keeps its epoch)
-                // starts the count afresh instead of continuing it.
-                if (last) atomicExch(cnt, 0ull);
-            }
-            last = __shfl_sync(0xffffffffu, last, 0);
-            if (last) {
-                __threadfence();
-                merge_unit(w0, w1, U0);
-            }
         }
     };
 
@@ -940,13 +904,97 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     }
 }
 
-// ---------------------------------------------------------------- host side
-
-// Tags of successive launches (48 bits, never 0, never reused in a process).
-unsigned long long next_epoch() {
-    static std::atomic<unsigned long long> counter{0};
-    return ((counter.fetch_add(1) + 1) & ((1ull << 48) - 1)) | (1ull << 47);
+// The split merge ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
+// apart, merged by the online-softmax rule).  Launched right after
+// decode_tc_kernel as its programmatic dependent: it waits for that grid
+// to complete, then half a warp per (sequence, KV head, query head of the
+// group) whose unit was cut between warps combines the unit's partial
+// records (m, l, unnormalised o) by their log-sum-exp, in warp order.  The
+// records are read in batches of up to four whose loads all go out
+// together (one memory round trip per batch, not one per record), each
+// batch folded into the running state by the same rule.  The unit's
+// descriptor names its first and last warp and the first warp's record
+// slot; every later warp holds the unit as its first piece (slot 0).  Warps
+// with empty ranges (only when the batch has fewer tiles than the decode
+// grid has warps) hold no record.
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const TcParams p, const int64_t TW) {
+    constexpr int E = HD / 16;  // output elements per lane
+    constexpr int B = 4;        // records per batch
+    pdl_wait_primary();
+    const int G = p.group;
+    const int64_t item = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
+    if (item >= (int64_t)p.num_seqs * p.num_kv_heads * G) return;
+    const int hl = threadIdx.x & 15;  // lane within the half warp
+    const int j = (int)(item % G);
+    const int64_t u = item / G;
+    const int4 d = __ldcg(p.ws_desc + u);
+    const int64_t W = __ldcg(p.ws_tiles);
+    if (d.z < 0) return;  // one warp held the unit whole and wrote the output
+    // every descriptor of a unit with context is rewritten by each launch;
+    // one outside this grid can only be a leftover after a warp gave up on
+    // a bounded wait (reported as PA_ERR_TIMEOUT), so it is not followed
+    if (d.x < 0 || d.x > d.y || (int64_t)d.y >= TW || d.z > 1) return;
+    const float* rec0 = p.ws_part + (int64_t)j * (HD + 4) + hl * E;
+    const int64_t rstride = (int64_t)G * (HD + 4);
+    float M = -INFINITY, L = 0.f, o[E];
+#pragma unroll
+    for (int t = 0; t < E; ++t) o[t] = 0.f;
+    for (int64_t w0 = d.x; w0 <= d.y; w0 += B) {
+        float m[B], l[B];
+        float4 a[B][E / 4];
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const int64_t w = w0 + b;
+            // an absent record (past the unit, or an empty range) weighs nothing
+            const bool ok = w <= d.y && !(W < TW && w * W / TW == (w + 1) * W / TW);
+            m[b] = -INFINITY;
+            l[b] = 0.f;
+            if (ok) {
+                const float* r = rec0 + (w * 2 + (w == d.x ? d.z : 0)) * rstride;
+                m[b] = __ldcg(r - hl * E + HD);
+                l[b] = __ldcg(r - hl * E + HD + 1);
+#pragma unroll
+                for (int t = 0; t < E / 4; ++t) a[b][t] = __ldcg(reinterpret_cast<const float4*>(r) + t);
+            } else {
+#pragma unroll
+                for (int t = 0; t < E / 4; ++t) a[b][t] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        float Mn = M;
+#pragma unroll
+        for (int b = 0; b < B; ++b) Mn = fmaxf(Mn, m[b]);
+        const float c = exp2f(M - Mn);
+        L *= c;
+#pragma unroll
+        for (int t = 0; t < E; ++t) o[t] *= c;
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+            const float e = exp2f(m[b] - Mn);  // 0 for an absent record
+            L = fmaf(e, l[b], L);
+#pragma unroll
+            for (int t = 0; t < E / 4; ++t) {
+                o[4 * t + 0] = fmaf(e, a[b][t].x, o[4 * t + 0]);
+                o[4 * t + 1] = fmaf(e, a[b][t].y, o[4 * t + 1]);
+                o[4 * t + 2] = fmaf(e, a[b][t].z, o[4 * t + 2]);
+                o[4 * t + 3] = fmaf(e, a[b][t].w, o[4 * t + 3]);
+            }
+        }
+        M = Mn;
+    }
+    const float inv = 1.f / L;
+    const int s = (int)(u / p.num_kv_heads), h = (int)(u - (int64_t)s * p.num_kv_heads);
+    T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + (int64_t)h * G + j) * HD + hl * E;
+#pragma unroll
+    for (int t = 0; t < E; t += 4) {  // 4 outputs (8 bytes) per store
+        uint2 v;
+        v.x = pack2<T>(o[t] * inv, o[t + 1] * inv);
+        v.y = pack2<T>(o[t + 2] * inv, o[t + 3] * inv);
+        *reinterpret_cast<uint2*>(out + t) = v;
+    }
 }
+
+// ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -994,6 +1042,13 @@ bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, bool fp8, int num
     return true;
 }
 
+// Bytes of the workspace's unit descriptors (after a 256-byte header, ahead
+// of the split records).
+size_t desc_ws_bytes(int32_t num_seqs, int32_t num_kv_heads) {
+    const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
+    return ((size_t)s * num_kv_heads * sizeof(int4) + 255) & ~(size_t)255;
+}
+
 template <typename T, int HD, int NT, bool FP8, bool PAIR = false>
 const void* kernel_ptr() {
     return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8, PAIR>);
@@ -1001,7 +1056,7 @@ const void* kernel_ptr() {
 
 template <int HD, bool FP8>
 int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t max_context, int64_t override_ctas) {
-    // the per-unit count holds up to 65535 partials: keep the grid's warps below that
+    // an explicit grid (PA_OPT_DECODE_CTAS) is capped; each warp owns two split records
     if (override_ctas > 0) return (int)(override_ctas < 16000 ? override_ctas : 16000);
     int dev = 0, sms = 0, occ = 0;
     cudaGetDevice(&dev);
@@ -1036,10 +1091,10 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.num_kv_heads = a.num_kv_heads;
     p.group = a.num_heads / a.num_kv_heads;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    const size_t cnt_bytes = ((size_t)a.num_seqs * a.num_kv_heads * 8 + 255) & ~(size_t)255;
-    p.ws_cnt = static_cast<unsigned long long*>(workspace);
-    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + cnt_bytes);
-    p.epoch = next_epoch();
+    p.ws_tiles = static_cast<long long*>(workspace);
+    p.ws_desc = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + 256);
+    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256 +
+                                         desc_ws_bytes(a.num_seqs, a.num_kv_heads));
     p.k_new = a.k_new;
     p.v_new = a.v_new;
     p.k_pool = const_cast<void*>(a.k_cache);
@@ -1064,7 +1119,17 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8, PAIR>, tmK, tmV, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8, PAIR>, tmK, tmV, p);
+    if (e != cudaSuccess) return e;
+    // the split merge, one warp per (unit, query head), as a programmatic
+    // dependent
+    const int64_t items = (int64_t)a.num_seqs * a.num_kv_heads * p.group;
+    const int64_t tw = (int64_t)grid * Pipe<HD, FP8>::NW;
+    cudaLaunchConfig_t mcfg = cfg;
+    mcfg.gridDim = dim3((unsigned)((items + 15) / 16));
+    mcfg.blockDim = dim3(256);
+    mcfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<T, HD>, p, tw);
 }
 
 template <typename T>
@@ -1127,10 +1192,9 @@ int decode_tc_warps_per_cta(int32_t head_dim, bool kv_fp8) {
 
 size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
                            bool kv_fp8) {
-    const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
     const int nw = decode_tc_warps_per_cta(head_dim, kv_fp8);
-    const size_t cnt_bytes = ((size_t)s * num_kv_heads * 8 + 255) & ~(size_t)255;
-    return cnt_bytes + (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
+    return 256 + desc_ws_bytes(num_seqs, num_kv_heads) +
+           (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
