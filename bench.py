@@ -30,9 +30,11 @@ overlap its neighbours' kernels); `cpu_baseline` is the
 CPU oracle on a bounded sample.  `--impl reference` times that oracle alone
 as the reference arm.
 
-Multi-GPU (torchrun): every rank runs its own replica of the batch (the
-sequences are independent, no data-path collective); `value` sums all ranks'
-bytes over the slowest rank's time.
+Multi-GPU (torchrun, N ranks): the batch is N times the configuration,
+drawn by the same generators, and each rank takes its shard -- a
+length-balanced cut by sequence, the rank holding only its requests' blocks
+(weak scaling, no data-path collective); `value` sums all ranks' bytes over
+the slowest rank's time.
 """
 import argparse
 import hashlib
@@ -112,11 +114,23 @@ def max_over_ranks(x, device=None):
     return float(t.item())
 
 
-def whole_job_rate(units_per_step_per_rank, world, steps, ms):
-    """Units per second over the whole job: every rank processes its own
-    replica of the batch (weak scaling), so the job handles world x the
-    units of one rank in the slowest rank's time."""
-    return units_per_step_per_rank * world * steps / (ms / 1e3)
+def sum_over_ranks(x, device=None):
+    """The sum of every rank's x; x itself without a process group.
+    Collective: every rank must call it."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_step_all_ranks, steps, ms):
+    """Units per second over the whole job: every rank's units of a step
+    (each rank holds its shard of the batch) over the slowest rank's time."""
+    return units_per_step_all_ranks * steps / (ms / 1e3)
 
 
 class Clocks:
@@ -172,14 +186,27 @@ class Clocks:
 # ---------------------------------------------------------------- workloads
 
 
-def make_workload(name, device, block_size=16):
+def make_workload(name, device, block_size=16, rank=0, world=1):
+    """The named configuration (one GPU), or -- on `world` ranks -- rank's
+    shard of a batch `world` times as large drawn by the same generators
+    (weak scaling): requests split by a length-balanced cut, each rank
+    holding only its requests' blocks (paged_kv_cache_116_gb300.shard)."""
+    from paged_kv_cache_116_gb300 import shard as SH
     from paged_kv_cache_116_gb300 import workloads as W
 
+    n = world
     if name == "tiny_decode":
-        return W.tiny_decode()
-    if name == "gqa_decode_batch":
-        return W.gqa_decode_batch(device=device, block_size=block_size)
-    return getattr(W, name)(device=device)
+        w = W.tiny_decode() if n == 1 else W.decode_workload(
+            "tiny_decode_fp32_bs4", "f32", 4, 4, 2, 32, [6, 13, 1, 20] * n, num_blocks=32 * n, scale=32 ** -0.5)
+    elif name == "gqa_decode_batch":
+        w = W.gqa_decode_batch(num_seqs=64 * n, device=device, block_size=block_size)
+    elif name == "long_context_decode":
+        w = W.long_context_decode(num_seqs=8 * n, device=device)
+    elif name == "mha_decode":
+        w = W.mha_decode(num_seqs=128 * n, device=device)
+    else:
+        w = W.mixed_varlen(num_chunks=16 * n, num_groups=60 * n, device=device)
+    return w if n == 1 else SH.shard(w, rank, n, by="sequence")
 
 
 def varlen_flops(w, select=None):
@@ -486,7 +513,7 @@ def main():
     import paged_kv_cache_116_gb300 as pa
     from paged_kv_cache_116_gb300 import workloads as W
 
-    w = make_workload(args.workload, dev, args.block_size)
+    w = make_workload(args.workload, dev, args.block_size, rank, world)
     tdt = W.TORCH_DTYPES[w.dtype]
     S, hq, hkv, hd, bs = w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     decode = w.is_decode and w.cow_pairs.shape[0] == 0
@@ -689,8 +716,9 @@ def main():
     eager_ms = timed(step, eager_steps) / eager_steps
     ms = max_over_ranks(ms, dev)
     ms_step = ms / args.steps
-    value = whole_job_rate(kv_bytes, world, args.steps, ms) / 1e9
-    seq_per_s = whole_job_rate(S, world, args.steps, ms)
+    job_kv_bytes, job_seqs = sum_over_ranks(kv_bytes, dev), sum_over_ranks(S, dev)
+    value = whole_job_rate(job_kv_bytes, args.steps, ms) / 1e9
+    seq_per_s = whole_job_rate(job_seqs, args.steps, ms)
 
     # e2e: each step's inputs from pinned host memory -> H2D, the step, the
     # output D2H to pinned memory
@@ -774,7 +802,7 @@ def main():
         reps = max(1, min(args.steps, 5000) // GS)
         e_steps = reps * GS
         e_ms = max_over_ranks(timed(lambda i: pg.replay(), reps), dev)
-        e2e = {"value": whole_job_rate(kv_bytes, world, e_steps, e_ms) / 1e9, "unit": "GB/s",
+        e2e = {"value": whole_job_rate(job_kv_bytes, e_steps, e_ms) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / e_steps,
                "how": "pinned-host inputs (one packed buffer per step) -> one H2D copy on a copy stream -> "
                       "the step's C-ABI calls -> D2H output on a second copy stream; two buffer sets, so "
@@ -821,7 +849,12 @@ def main():
                                 ("pa_write_kv_fp8 + pa_decode_fp8" if fp8 else
                                  "pa_write_kv + " + ("pa_decode" if decode else "pa_varlen"))) +
                                ", replayed as a CUDA graph",
-                       "seed": 0},
+                       "seed": 0,
+                       "parallelism": ("one GPU" if world == 1 else
+                                       "%d ranks, each with its shard (length-balanced cut by sequence, own block "
+                                       "pool) of a batch %d times the configuration; no data-path collective"
+                                       % (world, world)),
+                       "global_num_seqs": int(job_seqs)},
             "seq_per_s": seq_per_s,
             "eager_ms_per_step": eager_ms,
             "unfused_ms_per_step": unfused_ms,
