@@ -35,6 +35,21 @@
 // P V_X(k) has read it.  V rows past the context are zeroed in shared memory
 // before P V.  Every wait is bounded in time; on expiry the CTA sets
 // a status bit, abandons the tile and still frees its tensor memory.
+//
+// Decode rows (requests with one new token, at most 16 query heads per KV
+// head) take another route: 128 MMA rows of which G are used, and three
+// serial softmax / MMA hand-offs for a 300-token context, would hold an SM
+// for ~14 us per row.  Instead one CTA takes eight such requests of a KV
+// head, one warp each, and each warp streams its request's keys through its
+// own two-stage TMA ring in 16-token tiles and works them on the CUDA-core
+// tensor path: S^T = K Q^T with mma.m16n8k16 (the tile's 16 keys as M, the
+// G query heads as N, so each K/V byte is read once for the group), an
+// exp2-domain online softmax over the tile, P^T moved into B-fragment
+// layout with movmatrix, O^T += V^T P^T in fp32 registers.
+//
+// The grid is [prefill tile pairs | decode groups | spare]: every CTA first
+// scans the requests' pair counts and decode flags (one packed exclusive
+// prefix in shared memory) and finds its work by binary search.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -66,9 +81,14 @@ constexpr uint32_t S_COL = 0, P_COL = 0, O_COL = 128;  // within a tile's 256 co
 constexpr uint64_t WAIT_NS = 2000000000ull;  // 2 s
 constexpr int kMaxSeqsSmem = 4096;
 constexpr int kTableWindow = 512;  // block-table entries a producer stages at a time
+constexpr int DG = 8;              // decode requests per decode CTA (one per warp)
+constexpr int DR = 2;              // stages of a decode warp's ring
+constexpr int kPairBits = 20;      // packed prefix: pairs in the low 20 bits, decode rank above
+constexpr int kMaxDecodeGroupG = 16;
 
 struct UmParams {
     void* out;
+    const void* q;
     const int32_t* block_tables;
     int32_t max_blocks;
     const int32_t* seq_lens;
@@ -102,9 +122,193 @@ struct UGeo {
     static constexpr int CU_OFF = TBL_OFF + 2 * TBL_INTS * 4;
 };
 
+static_assert(DG * DR <= UGeo<64>::NBAR, "a decode CTA's warps use the kernel's barriers");
+static_assert(DG * DR * 2 * BS * 64 * 2 <= UGeo<64>::BAR_OFF && DG * DR * 2 * BS * 128 * 2 <= UGeo<128>::BAR_OFF,
+              "decode warps' stages fit below the barriers");
+
 template <int HD>
 size_t um_smem_bytes(int num_seqs) {
     return 1024 + (size_t)UGeo<HD>::CU_OFF + (size_t)((num_seqs < kMaxSeqsSmem ? num_seqs : kMaxSeqsSmem) + 1) * 4;
+}
+
+// One decode request (a single query at position L-1, which sees all L
+// keys) for KV head kvh, worked by one warp: its G query heads' outputs.
+// wst: the warp's DR stages of a 16-token K tile then V tile (1024-byte
+// aligned, 128-byte swizzle as the tensor maps write them); wbar: DR
+// mbarriers.  Returns false if a bounded wait ran out.
+template <typename T, int HD, int NT>
+__device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtensorMap* tmV, const UmParams& p,
+                                            int req, int kvh, uint8_t* wst, uint64_t* wbar, int lane) {
+    constexpr int CH = HD / 64, KS = HD / 16;
+    constexpr int TILE = BS * HD * 2;  // bytes of a 16-token K (or V) tile
+    constexpr int STAGE = 2 * TILE;
+    const int G = p.group;
+    const int L = p.seq_lens[req], qrow0 = p.cu[req];
+    T* out = static_cast<T*>(p.out) + ((int64_t)qrow0 * p.num_heads + (int64_t)kvh * G) * HD;
+    const int ntl = (L + BS - 1) / BS;
+    if (ntl <= 0) {  // no context: a zero row
+        for (int e = lane; e < G * HD; e += 32) out[e] = Elt<T>::from_f(0.f);
+        return true;
+    }
+    const int32_t* table = p.block_tables + (int64_t)req * p.max_blocks;
+    const int bsz = p.block_size;
+    const uint64_t pol = l2_policy_evict_last();  // forked prompts are read by several requests
+    // pool row of tile t's first token (and of its second 8-row half)
+    auto entry = [&](int t, int32_t& row2) -> int32_t {
+        row2 = 0;
+        if (t >= ntl) return 0;
+        const int tok = t * BS;
+        if (bsz == 8) {
+            const int32_t r1 = table[tok >> 3] * 8;
+            row2 = tok + 8 < L ? table[(tok >> 3) + 1] * 8 : r1;
+            return r1;
+        }
+        return table[tok / bsz] * bsz + tok % bsz;
+    };
+    int32_t trow2, trow = entry(lane, trow2);  // lane i: tile 32 win + i
+    int win = 0;
+    const int halves = bsz == 8 ? 2 : 1;
+    const int nbox = CH * 2 * halves;
+    auto issue = [&](int t) {
+        if ((t >> 5) != win) {
+            win = t >> 5;
+            trow = entry(32 * win + lane, trow2);
+        }
+        const int slot = t % DR;
+        const int32_t row = __shfl_sync(0xffffffffu, trow, t & 31), row2 = __shfl_sync(0xffffffffu, trow2, t & 31);
+        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], (uint32_t)(2 * TILE));
+        fence_proxy_async_smem();  // this slot's previous tile was read by ldmatrix
+        if (lane < nbox) {
+            const int hf = lane % halves, c = (lane / halves) % CH, is_v = lane / (halves * CH);
+            uint8_t* dst = wst + slot * STAGE + is_v * TILE + c * BS * 128 + hf * 1024;
+            tma_load_3d(dst, is_v ? tmV : tmK, &wbar[slot], 0, kvh * CH + c, hf ? row2 : row, pol);
+        }
+    };
+    int ip = 0;
+    for (; ip < DR && ip < ntl; ++ip) issue(ip);
+
+    const int g = lane >> 2, c4 = lane & 3;
+    const int mi = lane >> 3, ri = lane & 7;
+    const int k_tok = (mi & 1) * 8 + ri, k_dof = (mi >> 1) * 8;  // ldmatrix roles (K, non-transposed)
+    const int v_tok = (mi >> 1) * 8 + ri, v_dof = (mi & 1) * 8;  // (V^T, transposed)
+    auto swz = [](int tok, int dstart) -> uint32_t {
+        const int c = dstart >> 6, j = (dstart & 63) >> 3;
+        return (uint32_t)(c * BS * 128 + tok * 128 + ((j ^ (tok & 7)) << 4));
+    };
+    uint32_t qb[KS][NT][2];
+    const T* qbase = static_cast<const T*>(p.q) + ((int64_t)qrow0 * p.num_heads + (int64_t)kvh * G) * HD;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hh = nt * 8 + g;
+            if (hh < G) {
+                const T* qp = qbase + (int64_t)hh * HD + kk * 16 + 2 * c4;
+                qb[kk][nt][0] = *reinterpret_cast<const uint32_t*>(qp);
+                qb[kk][nt][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+            } else {
+                qb[kk][nt][0] = qb[kk][nt][1] = 0u;
+            }
+        }
+    float acc[KS][NT][4], mrow[NT][2], lrow[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        mrow[nt][0] = mrow[nt][1] = -INFINITY;
+        lrow[nt][0] = lrow[nt][1] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) acc[kk][nt][0] = acc[kk][nt][1] = acc[kk][nt][2] = acc[kk][nt][3] = 0.f;
+    }
+    const float sl = p.scale_log2;
+    const uint32_t st0 = smem_u32(wst);
+    for (int t = 0; t < ntl; ++t) {
+        const int slot = t % DR;
+        if (!mbar_wait_ns(&wbar[slot], (uint32_t)(t / DR) & 1u, WAIT_NS)) {
+            for (int u = t + 1; u < ip; ++u) mbar_wait_ns(&wbar[u % DR], (uint32_t)(u / DR) & 1u, WAIT_NS);
+            return false;
+        }
+        const uint32_t kt = st0 + (uint32_t)slot * STAGE, vt = kt + TILE;
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kt + swz(k_tok, kk * 16 + k_dof), a0, a1, a2, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+        }
+        const int valid = min(BS, L - t * BS);
+        const bool ok0 = g < valid, ok1 = g + 8 < valid;
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float x0 = ok0 ? sc[nt][0] * sl : -INFINITY, x1 = ok0 ? sc[nt][1] * sl : -INFINITY;
+            const float x2 = ok1 ? sc[nt][2] * sl : -INFINITY, x3 = ok1 ? sc[nt][3] * sl : -INFINITY;
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(mrow[nt][0], mx0), mn1 = fmaxf(mrow[nt][1], mx1);
+            const float al0 = fast_exp2(mrow[nt][0] - mn0), al1 = fast_exp2(mrow[nt][1] - mn1);
+            mrow[nt][0] = mn0;
+            mrow[nt][1] = mn1;
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            lrow[nt][0] = fmaf(lrow[nt][0], al0, p0 + p2);
+            lrow[nt][1] = fmaf(lrow[nt][1], al1, p1 + p3);
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    acc[mt][nt][0] *= al0;
+                    acc[mt][nt][1] *= al1;
+                    acc[mt][nt][2] *= al0;
+                    acc[mt][nt][3] *= al1;
+                }
+            }
+            pb[nt][0] = movm_t(pack2<T>(p0, p1));
+            pb[nt][1] = movm_t(pack2<T>(p2, p3));
+        }
+        // V rows past the context may hold anything: their operand lanes are zeroed
+        uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
+        if (valid < BS) {
+            m01 = (2 * c4 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 1 < valid ? 0xffff0000u : 0u);
+            m23 = (2 * c4 + 8 < valid ? 0x0000ffffu : 0u) | (2 * c4 + 9 < valid ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vt + swz(v_tok, mt * 16 + v_dof), a0, a1, a2, a3);
+            a0 &= m01;
+            a1 &= m01;
+            a2 &= m23;
+            a3 &= m23;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+        }
+        __syncwarp();
+        if (ip < ntl) issue(ip++);
+    }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = lrow[nt][e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int hh = nt * 8 + 2 * c4 + e;
+            if (hh < G) {
+                const float inv = 1.f / l;
+#pragma unroll
+                for (int mt = 0; mt < KS; ++mt) {
+                    out[hh * HD + mt * 16 + g] = Elt<T>::from_f(acc[mt][nt][e] * inv);
+                    out[hh * HD + mt * 16 + g + 8] = Elt<T>::from_f(acc[mt][nt][2 + e] * inv);
+                }
+            }
+        }
+    return true;
 }
 
 template <typename T, int HD>
@@ -125,35 +329,81 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* v_zeroed = tb + 6;
     volatile uint32_t* taddr_slot = reinterpret_cast<volatile uint32_t*>(base + Gm::TADDR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Gm::TADDR_OFF + 4);
-    int32_t* cu_s = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, G = p.group, TT = p.tokens_per_tile;
     const int kvh = blockIdx.y;
     pdl_wait_primary();
 
-    // ---- request and tile pair: request i owns pairs
-    // [floor(cu[i] / 2T) + i, floor(cu[i+1] / 2T) + i + 1); a request's
-    // ceil(n / 2T) pairs fit, the rest are spare CTAs that return at once
-    const bool cu_in_smem = S <= kMaxSeqsSmem;
-    if (cu_in_smem)
-        for (int i = threadIdx.x; i <= S; i += blockDim.x) cu_s[i] = p.cu[i];
+    // ---- work of this CTA.  Per request: its tile pairs (ceil(n / 2T); none
+    // for a decode row taken by a decode CTA) and whether it is such a
+    // decode row; one packed exclusive prefix of both over the requests.
+    int32_t* pref = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);  // [S + 1]
+    const bool dec_route = G <= kMaxDecodeGroupG;
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        const int n = p.cu[i + 1] - p.cu[i];
+        const bool dec = dec_route && n == 1;
+        pref[i + 1] = dec ? (1 << kPairBits) : (n + 2 * TT - 1) / (2 * TT);
+    }
+    if (threadIdx.x == 0) pref[0] = 0;
     __syncthreads();
-    auto cu_at = [&](int i) -> int { return cu_in_smem ? cu_s[i] : p.cu[i]; };
-    auto pair0 = [&](int i) -> int64_t { return (int64_t)cu_at(i) / (2 * TT) + i; };
+    if (warp == 0) {
+        const int per = (S + 31) / 32;
+        const int lo = 1 + lane * per, hi = min(S + 1, lo + per);
+        int sum = 0;
+        for (int i = lo; i < hi; ++i) sum += pref[i];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - sum;
+        for (int i = lo; i < hi; ++i) {
+            run += pref[i];
+            pref[i] = run;
+        }
+    }
+    __syncthreads();
+    constexpr int kPairMask = (1 << kPairBits) - 1;
     const int64_t bid = blockIdx.x;
+    const int n_pairs = pref[S] & kPairMask, n_dec = pref[S] >> kPairBits;
+    if (bid >= n_pairs) {
+        // ---- a decode CTA (or a spare one): decode rows of ranks DG d .. DG d + 7
+        const int64_t d = bid - n_pairs;
+        if (d * DG >= n_dec) return;  // spare (uniform for the CTA)
+        if (threadIdx.x == 0) {
+            for (int w = 0; w < DG * DR; ++w) mbar_init(&bars[w], 1u);
+            mbar_fence_init();
+        }
+        __syncthreads();
+        const int rank = (int)(d * DG) + warp;
+        if (warp >= DG || rank >= n_dec) return;
+        // the request with exactly `rank` decode rows before it and one more after it
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if ((pref[mid + 1] >> kPairBits) > rank) hi = mid;
+            else lo = mid + 1;
+        }
+        constexpr int kStage = 2 * BS * HD * 2;
+        uint8_t* wst = base + (size_t)warp * DR * kStage;
+        const bool ok = G <= 8 ? warp_decode<T, HD, 1>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, lane)
+                               : warp_decode<T, HD, 2>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, lane);
+        if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
+        return;
+    }
+    // ---- a prefill CTA: tile pair bid - pref[req] of request req
     int lo = 0, hi = S - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (pair0(mid) <= bid) lo = mid;
+        if ((pref[mid] & kPairMask) <= bid) lo = mid;
         else hi = mid - 1;
     }
     const int req = lo;
-    const int q0 = cu_at(req), n_new = cu_at(req + 1) - q0;
+    const int q0 = p.cu[req], n_new = p.cu[req + 1] - q0;
     const int ntile = (n_new + TT - 1) / TT;
-    const int npair = (ntile + 1) / 2;
-    const int64_t p_rel = bid - pair0(req);
-    if (p_rel >= npair) return;  // spare CTA (uniform for the CTA)
+    const int64_t p_rel = bid - (pref[req] & kPairMask);
     const int L = p.seq_lens[req];
     const int first_pos = L - n_new;
     const int nb_seq = (L + BS - 1) / BS;
@@ -584,6 +834,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     }
     UmParams p;
     p.out = a.out;
+    p.q = a.q;
     p.block_tables = a.block_tables;
     p.max_blocks = a.max_blocks;
     p.seq_lens = a.seq_lens;
@@ -595,13 +846,20 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     p.block_size = a.block_size;
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    // prefill tile pairs (at most total_q / 2T + one per request), then
+    // decode CTAs of DG requests; CTAs past the work the kernel finds return
     const int64_t pairs = (int64_t)a.total_q / (2 * TT) + a.num_seqs;
+    if (pairs >= (1 << kPairBits)) {
+        *err = "too many query rows for one varlen launch";
+        return cudaErrorInvalidValue;
+    }
+    const int64_t dgroups = G <= kMaxDecodeGroupG ? (a.num_seqs + DG - 1) / DG : 0;
     const size_t smem = um_smem_bytes<HD>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)pairs, (unsigned)a.num_kv_heads);
+    cfg.gridDim = dim3((unsigned)(pairs + dgroups), (unsigned)a.num_kv_heads);
     cfg.blockDim = dim3(NTHREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -623,11 +881,25 @@ bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group) {
 
 cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream) {
     if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
-    if (a.dtype == 1)
-        return a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(a, num_blocks, err, stream)
-                                : um_launch<__nv_bfloat16, 128>(a, num_blocks, err, stream);
-    return a.head_dim == 64 ? um_launch<__half, 64>(a, num_blocks, err, stream)
-                            : um_launch<__half, 128>(a, num_blocks, err, stream);
+    // a launch scans at most kMaxSeqsSmem requests in shared memory; query
+    // rows keep their global indices (cu_seqlens_q values), so a larger batch
+    // runs as several launches over slices of the per-request arrays
+    for (int32_t s0 = 0; s0 < a.num_seqs; s0 += kMaxSeqsSmem) {
+        AttnArgs c = a;
+        c.num_seqs = a.num_seqs - s0 < kMaxSeqsSmem ? a.num_seqs - s0 : kMaxSeqsSmem;
+        c.seq_lens = a.seq_lens + s0;
+        c.cu_seqlens_q = a.cu_seqlens_q + s0;
+        c.block_tables = a.block_tables + (int64_t)s0 * a.max_blocks;
+        cudaError_t e;
+        if (a.dtype == 1)
+            e = a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(c, num_blocks, err, stream)
+                                 : um_launch<__nv_bfloat16, 128>(c, num_blocks, err, stream);
+        else
+            e = a.head_dim == 64 ? um_launch<__half, 64>(c, num_blocks, err, stream)
+                                 : um_launch<__half, 128>(c, num_blocks, err, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 uint32_t varlen_umma_status(bool clear) {
