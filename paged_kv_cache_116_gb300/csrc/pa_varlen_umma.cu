@@ -626,79 +626,92 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // their warp instead of splitting it.
             const int vis = valid ? min(prow - kbase, BK - 1) : BK - 1;
             const bool full = vis == BK - 1;  // no masked column (most tiles)
-            // pass 1: the row maximum over the 128 raw scores
-            float mx = -INFINITY;
+            // Exponentials are taken against the row's running maximum
+            // m_used (exp2 domain), which a row keeps until a tile's maximum
+            // exceeds it by more than 8 (P then stays below 2^8, far inside
+            // its type's range).  So once every row of the warp has a
+            // maximum, one pass over the scores gives the exponentials and
+            // the tile's maximum together; only the first tile, a tile that
+            // outgrows some row's maximum, or a non-positive scale takes the
+            // maximum first and then the exponentials.  Whether to redo is
+            // decided per warp (tensor-memory loads are warp-wide); a row
+            // whose maximum did not grow recomputes the same values.
+            // 64 scores per tensor-memory wait; P (two per column) is kept in
+            // registers until it is final, then written over the low half of
+            // the S columns; masked keys get exactly 0.
+            float sum = 0.f, mraw = -INFINITY;  // mraw: the tile's maximum raw score
+            float pk[BK / 2];  // the tile's P, two per 32-bit column, stored once it is final
+            auto exp_pass = [&](float neg_m, bool track) {
+                sum = 0.f;
 #pragma unroll
-            for (int q32 = 0; q32 < BK / 32; ++q32) {
-                float a[32];
-                tmem_ld32(t_lane + S_COL + 32 * q32, a);
-                tmem_wait_ld();
-                if (full) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, a[j]);
-                } else {
-                    const int nv = vis - 32 * q32;  // columns j <= nv are visible
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) mx = fmaxf(mx, j <= nv ? a[j] : -INFINITY);
-                }
-            }
-            // exp2 domain: x = s * scale * log2(e); a positive scale keeps the
-            // order, so the maximum is taken on raw scores and the scaling is
-            // fused into the exponent's argument
-            float m_tile;
-            if (sl > 0.f) {
-                m_tile = mx * sl;
-            } else {
-                m_tile = -INFINITY;
-#pragma unroll
-                for (int q32 = 0; q32 < BK / 32; ++q32) {
-                    float a[32];
-                    tmem_ld32(t_lane + S_COL + 32 * q32, a);
+                for (int q64 = 0; q64 < BK / 64; ++q64) {
+                    float a[64];
+                    tmem_ld32(t_lane + S_COL + 64 * q64, *reinterpret_cast<float(*)[32]>(a));
+                    tmem_ld32(t_lane + S_COL + 64 * q64 + 32, *reinterpret_cast<float(*)[32]>(a + 32));
                     tmem_wait_ld();
-                    const int nv = vis - 32 * q32;
+                    if (full) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j)
-                        if (j <= nv) m_tile = fmaxf(m_tile, a[j] * sl);
+                        for (int j = 0; j < 32; ++j) {
+                            if (track) mraw = fmaxf(mraw, fmaxf(a[2 * j], a[2 * j + 1]));
+                            const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
+                            const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
+                            sum += e0 + e1;
+                            pk[32 * q64 + j] = __uint_as_float(pack2<T>(e0, e1));
+                        }
+                    } else {
+                        const int nv = vis - 64 * q64;  // columns j <= nv are visible
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const bool v0 = 2 * j <= nv, v1 = 2 * j + 1 <= nv;
+                            if (track) mraw = fmaxf(mraw, fmaxf(v0 ? a[2 * j] : -INFINITY, v1 ? a[2 * j + 1] : -INFINITY));
+                            const float e0 = v0 ? fast_exp2(fmaf(a[2 * j], sl, neg_m)) : 0.f;
+                            const float e1 = v1 ? fast_exp2(fmaf(a[2 * j + 1], sl, neg_m)) : 0.f;
+                            sum += e0 + e1;
+                            pk[32 * q64 + j] = __uint_as_float(pack2<T>(e0, e1));
+                        }
+                    }
                 }
+            };
+            // the maximum alone (first tile; non-positive scale)
+            auto max_pass = [&]() -> float {
+                float m_t = -INFINITY;
+#pragma unroll
+                for (int q64 = 0; q64 < BK / 64; ++q64) {
+                    float a[64];
+                    tmem_ld32(t_lane + S_COL + 64 * q64, *reinterpret_cast<float(*)[32]>(a));
+                    tmem_ld32(t_lane + S_COL + 64 * q64 + 32, *reinterpret_cast<float(*)[32]>(a + 32));
+                    tmem_wait_ld();
+                    const int nv = full ? BK : vis - 64 * q64;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j)
+                        if (j <= nv) m_t = fmaxf(m_t, sl > 0.f ? a[j] : a[j] * sl);
+                }
+                return sl > 0.f ? m_t * sl : m_t;
+            };
+            // a positive scale keeps the order, so the maximum is taken on raw scores
+            bool one_pass = sl > 0.f && __all_sync(0xffffffffu, m_used != -INFINITY);
+            float m_tile = -INFINITY;
+            if (one_pass) {
+                exp_pass(-m_used, true);
+                m_tile = mraw * sl;
+                one_pass = __all_sync(0xffffffffu, !(m_tile > m_used + 8.f));
+            } else {
+                m_tile = max_pass();
             }
-            const float m_new = fmaxf(m_used, m_tile);
-            const bool grow = (m_used == -INFINITY) || (m_new > m_used + 8.f);
+            bool grow = false;
             float alpha = 1.f;
-            if (grow) {
-                alpha = fast_exp2(m_used - m_new);
-                m_used = m_new;
-            }
-            const float neg_m = -m_used;
-            // pass 2: 32 keys at a time, exponentials packed two per column
-            // into the low half of the S columns (already read back); masked
-            // keys get exactly 0
-            float sum = 0.f;
-#pragma unroll
-            for (int q32 = 0; q32 < BK / 32; ++q32) {
-                float a[32];
-                tmem_ld32(t_lane + S_COL + 32 * q32, a);
-                tmem_wait_ld();
-                uint32_t pk[16];
-                if (full) {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
-                        const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
-                        sum += e0 + e1;
-                        pk[j] = pack2<T>(e0, e1);
-                    }
-                } else {
-                    const int nv = vis - 32 * q32;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float e0 = 2 * j <= nv ? fast_exp2(fmaf(a[2 * j], sl, neg_m)) : 0.f;
-                        const float e1 = 2 * j + 1 <= nv ? fast_exp2(fmaf(a[2 * j + 1], sl, neg_m)) : 0.f;
-                        sum += e0 + e1;
-                        pk[j] = pack2<T>(e0, e1);
-                    }
+            if (!one_pass) {
+                const float m_new = fmaxf(m_used, m_tile);
+                grow = (m_used == -INFINITY) || (m_new > m_used + 8.f);
+                if (grow) {
+                    alpha = fast_exp2(m_used - m_new);
+                    m_used = m_new;
                 }
-                tmem_st16(t_lane + P_COL + 16 * q32, pk);
+                exp_pass(-m_used, false);
             }
+            // P over the first 64 S columns, all of which have been read
+            tmem_st32(t_lane + P_COL, *reinterpret_cast<float(*)[32]>(pk));
+            tmem_st32(t_lane + P_COL + 32, *reinterpret_cast<float(*)[32]>(pk + 32));
             l = l * alpha + sum;
             const bool rescale = __any_sync(0xffffffffu, grow && kt > 0);
             if (rescale) {
