@@ -326,7 +326,15 @@ PA_API pa_status pa_decode_append_fp8(void* out, const void* q, const void* k_ne
  *                 non-decreasing, cu_seqlens_q[num_seqs] = total_q
  *   seq_lens:     device int32 [num_seqs], n_i <= seq_lens[i] <= max_context
  *   max_q:        upper bound of n_i over the batch
- *   workspace:    pa_varlen_workspace_size(...) bytes (may be NULL when 0)
+ *   workspace:    optional device scratch of pa_varlen_workspace_size(...)
+ *                 bytes (16-byte aligned; caller-owned, contents need no
+ *                 initialisation).  Given, the tensor-core kernel first lists
+ *                 its work longest first (a one-CTA plan kernel) and runs it
+ *                 in that order; NULL (or 0 bytes) runs it in request order.
+ *                 The outputs are the same either way.  A non-NULL workspace
+ *                 smaller than the size returns PA_ERR_WORKSPACE.  The size
+ *                 is 0 where the CUDA-core kernel runs (fp32, other head
+ *                 dims, PA_OPT_VARLEN_KERNEL = 1).
  */
 PA_API size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size,

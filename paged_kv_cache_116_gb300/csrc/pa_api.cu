@@ -571,9 +571,12 @@ pa_status pa_decode_append_fp8(void* out, const void* q, const void* k_new, cons
 size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
                                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t max_context,
                                 int dtype) {
-    (void)num_seqs, (void)total_q, (void)max_q, (void)num_heads, (void)num_kv_heads, (void)head_dim,
-        (void)block_size, (void)max_context, (void)dtype;
-    return 0;
+    (void)max_q, (void)max_context;
+    if (num_seqs <= 0 || total_q <= 0 || num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads) return 0;
+    const int G = num_heads / num_kv_heads;
+    const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
+    if (want == 1 || !pa::varlen_umma_supported(dtype, head_dim, block_size, G)) return 0;
+    return pa::varlen_umma_workspace(num_seqs, total_q, G);
 }
 
 pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
@@ -581,7 +584,6 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
                     int32_t total_q, int32_t max_q, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
                     int32_t num_blocks, int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
                     void* workspace, size_t workspace_bytes, void* stream) {
-    (void)workspace, (void)workspace_bytes;
     pa_status g = check_geometry(num_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
     if (g != PA_OK) return g;
     if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_blocks < 0 || max_context < 0)
@@ -634,9 +636,21 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     a.scale = scale;
     a.causal = causal ? 1 : 0;
     a.dtype = dtype;
+    a.max_context = max_context;
     if (use_um) {
+        // optional workspace: the tensor-core kernel then runs its work
+        // longest first (a plan kernel sorts it); without one, in request order
+        void* ws = nullptr;
+        if (workspace && workspace_bytes > 0) {
+            const size_t need = pa::varlen_umma_workspace(num_seqs, total_q, num_heads / num_kv_heads);
+            if (workspace_bytes < need)
+                return fail(PA_ERR_WORKSPACE, "workspace holds " + std::to_string(workspace_bytes) + " bytes, " +
+                                                  std::to_string(need) + " needed");
+            if (!aligned16(workspace)) return fail(PA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+            ws = workspace;
+        }
         std::string err;
-        cudaError_t e = pa::launch_varlen_umma(a, num_blocks, &err, st);
+        cudaError_t e = pa::launch_varlen_umma(a, num_blocks, ws, &err, st);
         if (e != cudaSuccess)
             return err.empty() ? cuda_fail(e, "pa_varlen launch") : fail(PA_ERR_CUDA, "pa_varlen: " + err);
         return PA_OK;

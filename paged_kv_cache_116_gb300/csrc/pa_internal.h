@@ -88,6 +88,8 @@ struct AttnArgs {
     float scale;
     int causal;
     int dtype;
+    // upper bound of seq_lens (varlen: sizes the work plan's buckets)
+    int32_t max_context = 0;
     // decode only: the new token of each sequence (position L-1), written to
     // the pool and attended from these rows (nullptr: plain decode)
     const void* k_new = nullptr;
@@ -125,7 +127,11 @@ uint32_t selftest_status(bool clear);
 
 // ---- tcgen05 varlen (pa_varlen_umma.cu)
 bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group);
-cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream);
+// Bytes of the optional workspace that lets the kernel run its work longest first.
+size_t varlen_umma_workspace(int32_t num_seqs, int64_t total_q, int32_t group);
+// workspace: nullptr (request order), or varlen_umma_workspace(...) bytes.
+cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, void* workspace, std::string* err,
+                               cudaStream_t stream);
 uint32_t varlen_umma_status(bool clear);
 
 }  // namespace pa

@@ -47,15 +47,24 @@
 // exp2-domain online softmax over the tile, P^T moved into B-fragment
 // layout with movmatrix, O^T += V^T P^T in fp32 registers.
 //
-// The grid is [prefill tile pairs | decode groups | spare]: every CTA first
-// scans the requests' pair counts and decode flags (one packed exclusive
-// prefix in shared memory) and finds its work by binary search.
+// The grid is [prefill tile pairs | decode groups | spare].  With a
+// workspace, a one-CTA plan kernel runs first and lists the prefill tile
+// pairs longest first (bucketed by the number of 128-key tiles tile A
+// reads) and the decode rows; the varlen kernel, its programmatic
+// dependent, takes item blockIdx.x / Hkv for KV head blockIdx.x % Hkv, so
+// the long pairs of every request and both heads start in the first waves
+// and the short ones fill the tail.  Each CTA's output is independent of
+// the others', so the order changes no result.  Without a workspace every
+// CTA scans the requests' pair counts and decode flags (one packed
+// exclusive prefix in shared memory) and finds its work, in request order,
+// by binary search.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <type_traits>
@@ -85,6 +94,8 @@ constexpr int DG = 8;              // decode requests per decode CTA (one per wa
 constexpr int DR = 2;              // stages of a decode warp's ring
 constexpr int kPairBits = 20;      // packed prefix: pairs in the low 20 bits, decode rank above
 constexpr int kMaxDecodeGroupG = 16;
+constexpr int kPairMask = (1 << kPairBits) - 1;
+constexpr int kMaxPlanBuckets = 4096;  // 128-key tile counts the plan sorts apart (longer ones share the last)
 
 struct UmParams {
     void* out;
@@ -100,6 +111,12 @@ struct UmParams {
     int32_t block_size;       // tokens per pool block: 8, or a multiple of 16 up to 256
     int32_t causal;
     float scale_log2;
+    // planned order (workspace given): plan[0] = prefill pairs, plan[1] =
+    // decode rows; items[k] = (request, pair) of the k-th prefill CTA,
+    // longest first; dec_req[r] = the request of decode rank r
+    const int32_t* plan;
+    const int2* items;
+    const int32_t* dec_req;
 };
 
 template <int HD>
@@ -332,7 +349,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.num_seqs, G = p.group, TT = p.tokens_per_tile;
-    const int kvh = blockIdx.y;
+    const bool planned = p.plan != nullptr;
+    const int Hkv = p.num_heads / G;
+    const int kvh = planned ? (int)(blockIdx.x % Hkv) : (int)blockIdx.y;
     pdl_wait_primary();
 
     // ---- work of this CTA.  Per request: its tile pairs (ceil(n / 2T); none
@@ -340,6 +359,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // decode row; one packed exclusive prefix of both over the requests.
     int32_t* pref = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);  // [S + 1]
     const bool dec_route = G <= kMaxDecodeGroupG;
+    int64_t bid = blockIdx.x;
+    int n_pairs, n_dec;
+    if (planned) {
+        bid = blockIdx.x / Hkv;
+        n_pairs = __ldcg(p.plan);
+        n_dec = __ldcg(p.plan + 1);
+    } else {
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         const int n = p.cu[i + 1] - p.cu[i];
         const bool dec = dec_route && n == 1;
@@ -365,9 +391,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
     }
     __syncthreads();
-    constexpr int kPairMask = (1 << kPairBits) - 1;
-    const int64_t bid = blockIdx.x;
-    const int n_pairs = pref[S] & kPairMask, n_dec = pref[S] >> kPairBits;
+    n_pairs = pref[S] & kPairMask;
+    n_dec = pref[S] >> kPairBits;
+    }
     if (bid >= n_pairs) {
         // ---- a decode CTA (or a spare one): decode rows of ranks DG d .. DG d + 7
         const int64_t d = bid - n_pairs;
@@ -379,12 +405,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncthreads();
         const int rank = (int)(d * DG) + warp;
         if (warp >= DG || rank >= n_dec) return;
-        // the request with exactly `rank` decode rows before it and one more after it
-        int lo = 0, hi = S - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if ((pref[mid + 1] >> kPairBits) > rank) hi = mid;
-            else lo = mid + 1;
+        int lo = 0;
+        if (planned) {
+            lo = __ldcg(p.dec_req + rank);
+        } else {
+            // the request with exactly `rank` decode rows before it and one more after it
+            int hi = S - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if ((pref[mid + 1] >> kPairBits) > rank) hi = mid;
+                else lo = mid + 1;
+            }
         }
         constexpr int kStage = 2 * BS * HD * 2;
         uint8_t* wst = base + (size_t)warp * DR * kStage;
@@ -393,17 +424,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
         return;
     }
-    // ---- a prefill CTA: tile pair bid - pref[req] of request req
-    int lo = 0, hi = S - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if ((pref[mid] & kPairMask) <= bid) lo = mid;
-        else hi = mid - 1;
+    // ---- a prefill CTA: tile pair p_rel of request req
+    int req;
+    int64_t p_rel;
+    if (planned) {
+        const int2 it = __ldcg(p.items + bid);
+        req = it.x;
+        p_rel = it.y;
+    } else {
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((pref[mid] & kPairMask) <= bid) lo = mid;
+            else hi = mid - 1;
+        }
+        req = lo;
+        p_rel = bid - (pref[req] & kPairMask);
     }
-    const int req = lo;
     const int q0 = p.cu[req], n_new = p.cu[req + 1] - q0;
     const int ntile = (n_new + TT - 1) / TT;
-    const int64_t p_rel = bid - (pref[req] & kPairMask);
     const int L = p.seq_lens[req];
     const int first_pos = L - n_new;
     const int nb_seq = (L + BS - 1) / BS;
@@ -789,6 +828,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == W_MMA) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// The work plan (one CTA): every prefill tile pair of the batch, sorted by
+// the number of 128-key tiles its tile A reads, most first (a counting sort
+// over kMaxPlanBuckets buckets; the order inside a bucket is whatever the
+// atomics give, which changes no output), then the decode rows.  plan[0] =
+// pairs, plan[1] = decode rows.
+__global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __restrict__ cu,
+                                                           const int32_t* __restrict__ seq_lens, int S, int TT,
+                                                           int causal, int dec_route, int nbuckets, int32_t* plan,
+                                                           int2* items, int32_t* dec_req) {
+    extern __shared__ int32_t hist[];  // [nbuckets] counts, then [nbuckets] cursors
+    __shared__ int32_t n_dec_s;
+    int32_t* cursor = hist + nbuckets;
+    pdl_wait_primary();
+    pdl_launch_dependents();  // the varlen kernel may be scheduled; it waits for this grid
+    for (int b = threadIdx.x; b < nbuckets; b += blockDim.x) hist[b] = 0;
+    if (threadIdx.x == 0) n_dec_s = 0;
+    __syncthreads();
+    // 128-key tiles tile A of pair pr of a request reads
+    auto tiles_of = [&](int n, int L, int pr) -> int {
+        const int ntile = (n + TT - 1) / TT, ta = ntile - 1 - 2 * pr, t0 = ta * TT;
+        const int kv_end = causal ? L - n + t0 + min(TT, n - t0) : L;
+        return min((kv_end + BK - 1) / BK, nbuckets - 1);
+    };
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        const int n = cu[i + 1] - cu[i], L = seq_lens[i];
+        if (dec_route && n == 1) {
+            dec_req[atomicAdd(&n_dec_s, 1)] = i;
+            continue;
+        }
+        const int npair = (n + 2 * TT - 1) / (2 * TT);
+        for (int pr = 0; pr < npair; ++pr) atomicAdd(&hist[tiles_of(n, L, pr)], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {  // exclusive prefix over the buckets, longest first
+        const int lane = threadIdx.x, per = (nbuckets + 31) / 32;
+        const int lo = lane * per, hi = min(nbuckets, lo + per);
+        int sum = 0;
+        for (int k = lo; k < hi; ++k) sum += hist[nbuckets - 1 - k];
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - sum;
+        for (int k = lo; k < hi; ++k) {
+            cursor[nbuckets - 1 - k] = run;
+            run += hist[nbuckets - 1 - k];
+        }
+        if (lane == 31) plan[0] = run;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < S; i += blockDim.x) {
+        const int n = cu[i + 1] - cu[i], L = seq_lens[i];
+        if (dec_route && n == 1) continue;
+        const int npair = (n + 2 * TT - 1) / (2 * TT);
+        for (int pr = 0; pr < npair; ++pr) items[atomicAdd(&cursor[tiles_of(n, L, pr)], 1)] = make_int2(i, pr);
+    }
+    if (threadIdx.x == 0) plan[1] = n_dec_s;
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 um_encode_fn() {
@@ -823,8 +923,18 @@ bool um_encode(CUtensorMap* m, const void* base, int dtype, const cuuint64_t dim
     return true;
 }
 
+// Workspace layout of a planned launch: plan header, prefill items (one per
+// possible tile pair), decode-row requests.
+int64_t um_pairs_bound(int64_t total_q, int32_t num_seqs, int TT) { return total_q / (2 * TT) + num_seqs; }
+size_t um_round(size_t b) { return (b + 255) & ~(size_t)255; }
+size_t um_plan_bytes(int64_t total_q, int32_t num_seqs, int TT) {
+    return 256 + um_round((size_t)um_pairs_bound(total_q, num_seqs, TT) * sizeof(int2)) +
+           um_round((size_t)num_seqs * sizeof(int32_t));
+}
+
 template <typename T, int HD>
-cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream) {
+cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, std::string* err,
+                      cudaStream_t stream) {
     const int G = a.num_heads / a.num_kv_heads;
     const int TT = TM / G;
     CUtensorMap tmQ, tmK, tmV;
@@ -859,6 +969,9 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
     p.block_size = a.block_size;
     p.causal = a.causal;
     p.scale_log2 = a.scale * 1.4426950408889634f;
+    p.plan = nullptr;
+    p.items = nullptr;
+    p.dec_req = nullptr;
     // prefill tile pairs (at most total_q / 2T + one per request), then
     // decode CTAs of DG requests; CTAs past the work the kernel finds return
     const int64_t pairs = (int64_t)a.total_q / (2 * TT) + a.num_seqs;
@@ -867,18 +980,37 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, std::string* err, c
         return cudaErrorInvalidValue;
     }
     const int64_t dgroups = G <= kMaxDecodeGroupG ? (a.num_seqs + DG - 1) / DG : 0;
-    const size_t smem = um_smem_bytes<HD>(a.num_seqs);
+    const size_t smem = um_smem_bytes<HD>(workspace ? 0 : a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(pairs + dgroups), (unsigned)a.num_kv_heads);
-    cfg.blockDim = dim3(NTHREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    if (workspace) {
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        p.plan = reinterpret_cast<const int32_t*>(ws);
+        p.items = reinterpret_cast<const int2*>(ws + 256);
+        p.dec_req = reinterpret_cast<const int32_t*>(ws + 256 + um_round((size_t)pairs * sizeof(int2)));
+        const int nbuckets = (int)std::min<int64_t>(kMaxPlanBuckets, (int64_t)(a.max_context + BK - 1) / BK + 2);
+        cudaLaunchConfig_t pc = {};
+        pc.gridDim = dim3(1);
+        pc.blockDim = dim3(1024);
+        pc.dynamicSmemBytes = (size_t)2 * nbuckets * sizeof(int32_t);
+        pc.stream = stream;
+        pc.attrs = attr;
+        pc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&pc, varlen_plan_kernel, a.cu_seqlens_q, a.seq_lens, a.num_seqs, TT, a.causal,
+                               G <= kMaxDecodeGroupG ? 1 : 0, nbuckets, const_cast<int32_t*>(p.plan),
+                               const_cast<int2*>(p.items), const_cast<int32_t*>(p.dec_req));
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = workspace ? dim3((unsigned)((pairs + dgroups) * a.num_kv_heads), 1u)
+                            : dim3((unsigned)(pairs + dgroups), (unsigned)a.num_kv_heads);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, varlen_umma_kernel<T, HD>, tmQ, tmK, tmV, p);
@@ -892,24 +1024,33 @@ bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group) {
            group <= TM;
 }
 
-cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, std::string* err, cudaStream_t stream) {
+size_t varlen_umma_workspace(int32_t num_seqs, int64_t total_q, int32_t group) {
+    if (num_seqs <= 0 || total_q <= 0 || group < 1 || group > TM) return 0;
+    return um_plan_bytes(total_q, num_seqs, TM / group);
+}
+
+cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, void* workspace, std::string* err,
+                               cudaStream_t stream) {
     if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
-    // a launch scans at most kMaxSeqsSmem requests in shared memory; query
-    // rows keep their global indices (cu_seqlens_q values), so a larger batch
-    // runs as several launches over slices of the per-request arrays
+    auto one = [&](const AttnArgs& c, void* ws) -> cudaError_t {
+        if (a.dtype == 1)
+            return a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(c, num_blocks, ws, err, stream)
+                                    : um_launch<__nv_bfloat16, 128>(c, num_blocks, ws, err, stream);
+        return a.head_dim == 64 ? um_launch<__half, 64>(c, num_blocks, ws, err, stream)
+                                : um_launch<__half, 128>(c, num_blocks, ws, err, stream);
+    };
+    if (workspace) return one(a, workspace);  // planned: any number of requests in one launch
+    // unplanned: a launch scans at most kMaxSeqsSmem requests in shared
+    // memory; query rows keep their global indices (cu_seqlens_q values), so
+    // a larger batch runs as several launches over slices of the
+    // per-request arrays
     for (int32_t s0 = 0; s0 < a.num_seqs; s0 += kMaxSeqsSmem) {
         AttnArgs c = a;
         c.num_seqs = a.num_seqs - s0 < kMaxSeqsSmem ? a.num_seqs - s0 : kMaxSeqsSmem;
         c.seq_lens = a.seq_lens + s0;
         c.cu_seqlens_q = a.cu_seqlens_q + s0;
         c.block_tables = a.block_tables + (int64_t)s0 * a.max_blocks;
-        cudaError_t e;
-        if (a.dtype == 1)
-            e = a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(c, num_blocks, err, stream)
-                                 : um_launch<__nv_bfloat16, 128>(c, num_blocks, err, stream);
-        else
-            e = a.head_dim == 64 ? um_launch<__half, 64>(c, num_blocks, err, stream)
-                                 : um_launch<__half, 128>(c, num_blocks, err, stream);
+        cudaError_t e = one(c, nullptr);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
