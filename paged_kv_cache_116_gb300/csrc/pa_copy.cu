@@ -12,11 +12,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
 namespace pa {
 namespace {
+
+// Launch as a programmatic dependent of the previous kernel on the stream:
+// its launch overlaps that kernel's tail; the kernel waits for it
+// (griddepcontrol.wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 
 __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
     uint4 r;
@@ -31,6 +52,8 @@ __device__ __forceinline__ uint4 ld_nc_v4(const uint4* p) {
 __global__ void slot_mapping_kernel(const int32_t* __restrict__ block_tables, int32_t max_blocks,
                                     const int32_t* __restrict__ seq_idx, const int64_t* __restrict__ positions,
                                     int64_t n, int32_t block_size, int64_t* __restrict__ slot_out) {
+    pdl_wait_primary();  // launched as a programmatic dependent: inputs may come from the kernel before
+    pdl_launch_dependents();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t pos = positions[i];
         if (pos < 0) {
@@ -50,6 +73,7 @@ constexpr int kWriteWarps = 8;
 __global__ void __launch_bounds__(kWriteWarps * 32)
     write_kv_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, const int64_t* __restrict__ slots,
                     int64_t n, uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t row_vecs) {
+    pdl_wait_primary();  // the slots (or the pool) may come from the kernel before
     // a dependent kernel (the decode reading these rows) may be scheduled
     // now; it waits for this grid to finish before it reads anything
     pdl_launch_dependents();
@@ -72,6 +96,7 @@ __global__ void __launch_bounds__(kWriteWarps * 32)
                      const int32_t* __restrict__ block_tables, int32_t max_blocks,
                      const int32_t* __restrict__ context_lens, int32_t num_seqs, int32_t block_size,
                      uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, int64_t row_vecs) {
+    pdl_wait_primary();
     pdl_launch_dependents();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t s = blockIdx.x * (int64_t)(kWriteWarps / 2) + (warp >> 1);
@@ -165,6 +190,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_rows8_kernel(const T* __restrict__ k, const T* __restrict__ v, Rows rows, int64_t n_items, int32_t hkv,
                        int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
                        float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_wait_primary();
     pdl_launch_dependents();
     constexpr int HD = 8 * EPL;
     const int lane = threadIdx.x & 31, sub = lane >> 3, l8 = lane & 7;
@@ -208,6 +234,7 @@ __global__ void __launch_bounds__(kQuantWarps * 32)
     quant_rows_kernel(const T* __restrict__ k, const T* __restrict__ v, Rows rows, int64_t n_items, int32_t hkv,
                       int32_t hd, int32_t bs, uint8_t* __restrict__ k_codes, uint8_t* __restrict__ v_codes,
                       float* __restrict__ k_scales, float* __restrict__ v_scales) {
+    pdl_wait_primary();
     pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * kQuantWarps;
@@ -245,11 +272,11 @@ cudaError_t launch_quant(const void* k, const void* v, const Rows& rows, int64_t
     const unsigned grid = (unsigned)std::min<int64_t>((n_items + per_cta - 1) / per_cta, kQuantMaxCtas);
     const dim3 block(kQuantWarps * 32);
     switch (hd % 8 == 0 ? hd / 8 : 0) {
-        case 4: quant_rows8_kernel<T, 4><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
-        case 8: quant_rows8_kernel<T, 8><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
-        case 16: quant_rows8_kernel<T, 16><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
-        case 32: quant_rows8_kernel<T, 32><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales); break;
-        default: quant_rows_kernel<T><<<grid, block, 0, stream>>>(kt, vt, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales); break;
+        case 4: return launch_pdl(quant_rows8_kernel<T, 4, Rows>, grid, block, stream, kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales);
+        case 8: return launch_pdl(quant_rows8_kernel<T, 8, Rows>, grid, block, stream, kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales);
+        case 16: return launch_pdl(quant_rows8_kernel<T, 16, Rows>, grid, block, stream, kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales);
+        case 32: return launch_pdl(quant_rows8_kernel<T, 32, Rows>, grid, block, stream, kt, vt, rows, n_items, hkv, bs, k_codes, v_codes, k_scales, v_scales);
+        default: return launch_pdl(quant_rows_kernel<T, Rows>, grid, block, stream, kt, vt, rows, n_items, hkv, hd, bs, k_codes, v_codes, k_scales, v_scales);
     }
     return cudaGetLastError();
 }
@@ -273,6 +300,8 @@ struct CopyPtrs {
 
 __global__ void __launch_bounds__(256)
     copy_blocks_kernel(const CopyPtrs ptrs, const int64_t* __restrict__ pairs, int64_t block_vecs) {
+    pdl_wait_primary();  // the pool may still be read or written by the kernel before
+    pdl_launch_dependents();
     const int64_t pair = blockIdx.x;
     const int layer = blockIdx.y;
     const int64_t src = pairs[2 * pair], dst = pairs[2 * pair + 1];
@@ -355,9 +384,8 @@ cudaError_t launch_slot_mapping(const int32_t* block_tables, int32_t max_blocks,
     if (n == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = (n + threads - 1) / threads;
-    slot_mapping_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), threads, 0, stream>>>(
-        block_tables, max_blocks, seq_idx, positions, n, block_size, slot_out);
-    return cudaGetLastError();
+    return launch_pdl(slot_mapping_kernel, dim3((unsigned)(blocks < 65535 ? blocks : 65535)), dim3(threads), stream,
+                      block_tables, max_blocks, seq_idx, positions, n, block_size, slot_out);
 }
 
 cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_mapping, int64_t n, void* k_cache,
@@ -365,10 +393,9 @@ cudaError_t launch_write_kv(const void* k, const void* v, const int64_t* slot_ma
     if (n == 0) return cudaSuccess;
     const int64_t per_cta = kWriteWarps / 2;
     const int64_t blocks = (n + per_cta - 1) / per_cta;
-    write_kv_kernel<<<(unsigned)blocks, kWriteWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n, static_cast<uint4*>(k_cache),
-        static_cast<uint4*>(v_cache), row_bytes / 16);
-    return cudaGetLastError();
+    return launch_pdl(write_kv_kernel, dim3((unsigned)blocks), dim3(kWriteWarps * 32), stream,
+                      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, n,
+                      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), row_bytes / 16);
 }
 
 cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t* block_tables, int32_t max_blocks,
@@ -376,10 +403,10 @@ cudaError_t launch_append_kv(const void* k_new, const void* v_new, const int32_t
                              void* v_cache, int64_t row_bytes, cudaStream_t stream) {
     if (num_seqs == 0) return cudaSuccess;
     const int64_t per_cta = kWriteWarps / 2;
-    append_kv_kernel<<<(unsigned)((num_seqs + per_cta - 1) / per_cta), kWriteWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables, max_blocks, context_lens,
-        num_seqs, block_size, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), row_bytes / 16);
-    return cudaGetLastError();
+    return launch_pdl(append_kv_kernel, dim3((unsigned)((num_seqs + per_cta - 1) / per_cta)), dim3(kWriteWarps * 32),
+                      stream, static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables,
+                      max_blocks, context_lens, num_seqs, block_size, static_cast<uint4*>(k_cache),
+                      static_cast<uint4*>(v_cache), row_bytes / 16);
 }
 
 cudaError_t launch_write_kv_fp8(const void* k, const void* v, int dtype, const int64_t* slot_mapping, int64_t n,
@@ -408,8 +435,7 @@ cudaError_t launch_copy_blocks(void* const* k_caches, void* const* v_caches, int
         ptrs.v[l] = static_cast<uint4*>(v_caches[l]);
     }
     dim3 grid((unsigned)num_pairs, (unsigned)num_layers);
-    copy_blocks_kernel<<<grid, 256, 0, stream>>>(ptrs, block_pairs, block_bytes / 16);
-    return cudaGetLastError();
+    return launch_pdl(copy_blocks_kernel, grid, dim3(256), stream, ptrs, block_pairs, block_bytes / 16);
 }
 
 }  // namespace pa
