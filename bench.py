@@ -611,7 +611,7 @@ def main():
         attend(pools[i % copies], q, bt, lens, cu, torch.cuda.current_stream())
 
     tc_decode = (decode and w.dtype in ("bf16", "f16") and hd in ((128, 256) if fp8 else (64, 128, 256)) and
-                 hq // hkv <= 16 and (bs == 8 or (bs % 16 == 0 and bs <= 256)))
+                 hq // hkv <= 16 and (not fp8 or bs == 8 or (bs % 16 == 0 and bs <= 256)))
     # the append happens inside the decode kernel (a code cache: head_dim 128 and
     # no more (sequence, KV head) units than the grid's warps, 3 CTAs x 4 warps per SM)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count

@@ -237,7 +237,11 @@ PA_API pa_status pa_swap_blocks(void* const* src_k, void* const* src_v, void* co
  *   workspace:    device scratch of at least pa_decode_workspace_size(...) bytes
  *                 (may be NULL when that size is 0), 16-byte aligned; its
  *                 content on entry does not matter.
- * Accumulation is fp32 for every dtype.
+ * Accumulation is fp32 for every dtype.  bf16/f16 with head_dim 64/128/256
+ * and at most 16 query heads per KV head run on the tensor cores at any
+ * block size (TMA boxes for 8 and multiples of 16 up to 256, a row-by-row
+ * gather otherwise); the rest on the CUDA-core kernel, which reads each K/V
+ * row once for up to 8 query heads of a KV head.
  */
 PA_API size_t pa_decode_workspace_size(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads,
                                 int32_t head_dim, int32_t block_size, int32_t max_context, int dtype);
@@ -354,8 +358,8 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
  * synchronisation, or code with no allocator at hand.  The pages have no
  * counterpart; it exists for those callers only.
  * Same arguments and result as pa_decode (tensor-core cases: bf16/f16,
- * head_dim 64/128/256, block_size 8 or a multiple of 16 up to 256, at most
- * 16 query heads per KV head; others return PA_ERR_UNSUPPORTED), but no
+ * head_dim 64/128/256, any block_size, at most 16 query heads per KV head;
+ * others return PA_ERR_UNSUPPORTED), but no
  * workspace: the split-KV scratch
  * is one library-owned device array of 8 MiB per device, held from load
  * until process exit.  A problem whose scratch (pa_decode_workspace_size

@@ -359,9 +359,8 @@ static bool use_decode_tc(int dtype, int head_dim, int block_size, int group, bo
         *st = fail(PA_ERR_UNSUPPORTED, kv_fp8 ? "the tensor-core decode kernel over an FP8 cache takes bf16/f16 "
                                                 "queries, head_dim 128/256, block_size 8 or a multiple of 16 up "
                                                 "to 256, and at most 16 query heads per KV head"
-                                              : "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256, "
-                                                "block_size 8 or a multiple of 16 up to 256, and at most 16 query "
-                                                "heads per KV head");
+                                              : "the tensor-core decode kernel takes bf16/f16, head_dim 64/128/256 "
+                                                "and at most 16 query heads per KV head");
         return false;
     }
     return ok;

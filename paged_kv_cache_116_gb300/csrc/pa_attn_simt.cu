@@ -1,15 +1,19 @@
 // pa_attn_simt.cu -- CUDA-core paged attention for any element type and any
-// head_dim up to 256: one CTA per (query row, query head).
+// head_dim up to 256: one CTA per (query row, KV head, group of up to 8 of
+// that KV head's query heads).
 //
 // This is the path for fp32 (where the 1e-5 bound rules out 16-bit tensor
 // operands) and for shapes the tensor-core kernels do not take.  It follows
 // the handbook's paged_attention row by row: the row's request comes from
 // cu_seqlens_q, its position from seq_len - num_new + j, and its keys are
-// read through the block table in logical order.  Each of the CTA's warps
-// keeps an online-softmax state over an interleaved share of the keys
-// (lanes split head_dim), and the warps' states are merged by their
-// log-sum-exp at the end ("aiqz.cc PagedAttention", §工程实现要点: per-block
-// softmax merged online).
+// read through the block table in logical order.  The query heads that
+// share a KV head are worked together (query-group packing: each K/V row is
+// read once for the CTA's heads, not once per head).  Lanes split head_dim
+// and hold every head's query slice and output accumulator; each of the
+// CTA's warps keeps one online-softmax state per head over an interleaved
+// share of the keys, and the warps' states are merged by their log-sum-exp
+// at the end ("aiqz.cc PagedAttention", §工程实现要点: per-block softmax
+// merged online).
 //
 // With a quantized cache (FP8 E4M3 codes, one fp32 scale per token and KV
 // head, scales [num_blocks, num_kv_heads, block_size]) a key or value element
@@ -41,11 +45,16 @@ template <typename T> struct CacheElt<T, true> {
     }
 };
 
-template <typename T, bool FP8>
+// DPL: head dims per lane (head_dim <= 32 DPL); GH: query heads per CTA.
+template <typename T, bool FP8, int DPL, int GH>
 __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
     using C = CacheElt<T, FP8>;
-    const int row = blockIdx.x;   // query row
-    const int head = blockIdx.y;  // query head
+    const int row = blockIdx.x;  // query row
+    const int G = a.num_heads / a.num_kv_heads;
+    const int hchunks = (G + GH - 1) / GH;
+    const int kvh = blockIdx.y / hchunks;
+    const int h0 = kvh * G + (blockIdx.y - kvh * hchunks) * GH;  // first query head of the CTA
+    const int nh = min(GH, kvh * G + G - h0);                    // heads of the CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     // request of this row: the last i with cu_seqlens_q[i] <= row
@@ -67,24 +76,26 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
     const int pos = seq_len - num_new + j;
     const int visible = a.causal ? pos + 1 : seq_len;
 
-    const int G = a.num_heads / a.num_kv_heads;
-    const int kvh = head / G;
     const int hd = a.head_dim;
     const int64_t row_elts = (int64_t)a.num_kv_heads * hd;
-    const T* q = static_cast<const T*>(a.q) + ((int64_t)row * a.num_heads + head) * hd;
+    const T* q = static_cast<const T*>(a.q) + ((int64_t)row * a.num_heads + h0) * hd;
     const typename C::S* kc = static_cast<const typename C::S*>(a.k_cache) + (int64_t)kvh * hd;
     const typename C::S* vc = static_cast<const typename C::S*>(a.v_cache) + (int64_t)kvh * hd;
     const int32_t* table = a.block_tables + (int64_t)req * a.max_blocks;
     const float scale_log2 = a.scale * 1.4426950408889634f;
 
-    float qv[kMaxDimsPerLane], acc[kMaxDimsPerLane];
+    float qv[GH][DPL], acc[GH][DPL], m[GH], l[GH];
 #pragma unroll
-    for (int k = 0; k < kMaxDimsPerLane; ++k) {
-        const int d = lane + 32 * k;
-        qv[k] = d < hd ? Elt<T>::to_f(q[d]) : 0.f;
-        acc[k] = 0.f;
+    for (int h = 0; h < GH; ++h) {
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) {
+            const int d = lane + 32 * k;
+            qv[h][k] = (h < nh && d < hd) ? Elt<T>::to_f(q[(int64_t)h * hd + d]) : 0.f;
+            acc[h][k] = 0.f;
+        }
     }
-    float m = -INFINITY, l = 0.f;
     for (int t = warp; t < visible; t += kWarps) {
         const int64_t blk = table[t / a.block_size], off_in = t % a.block_size;
         const int64_t slot = blk * a.block_size + off_in;
@@ -95,55 +106,93 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
             vs = a.v_scales[si];
         }
         const typename C::S* kr = kc + slot * row_elts;
-        float dot = 0.f;
-#pragma unroll
-        for (int k = 0; k < kMaxDimsPerLane; ++k) {
-            const int d = lane + 32 * k;
-            if (d < hd) dot = fmaf(qv[k], C::to_f(kr[d]), dot);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, off);
-        const float x = dot * ks * scale_log2;
-        const float m_new = fmaxf(m, x);
-        const float corr = exp2f(m - m_new);
-        const float p = exp2f(x - m_new);
-        l = l * corr + p;
-        const float pv = p * vs;
         const typename C::S* vr = vc + slot * row_elts;
+        float kx[DPL], vx[DPL];
 #pragma unroll
-        for (int k = 0; k < kMaxDimsPerLane; ++k) {
+        for (int k = 0; k < DPL; ++k) {
             const int d = lane + 32 * k;
-            if (d < hd) acc[k] = fmaf(pv, C::to_f(vr[d]), acc[k] * corr);
+            kx[k] = d < hd ? C::to_f(kr[d]) : 0.f;
+            vx[k] = d < hd ? C::to_f(vr[d]) : 0.f;
         }
-        m = m_new;
+        float dot[GH];
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            dot[h] = 0.f;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) dot[h] = fmaf(qv[h][k], kx[k], dot[h]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int h = 0; h < GH; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            const float x = dot[h] * ks * scale_log2;
+            const float m_new = fmaxf(m[h], x);
+            const float corr = exp2f(m[h] - m_new);
+            const float p = exp2f(x - m_new);
+            l[h] = l[h] * corr + p;
+            const float pv = p * vs;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(pv, vx[k], acc[h][k] * corr);
+            m[h] = m_new;
+        }
     }
 
-    // merge the warps' (m, l, acc) by their log-sum-exp
-    __shared__ float sm_m[kWarps], sm_l[kWarps];
-    __shared__ float sm_acc[kWarps][kMaxDimsPerLane * 32];
+    // merge the warps' (m, l, acc) per head by their log-sum-exp
+    __shared__ float sm_m[kWarps][GH], sm_l[kWarps][GH];
+    __shared__ float sm_acc[kWarps][GH][DPL * 32];
     if (lane == 0) {
-        sm_m[warp] = m;
-        sm_l[warp] = l;
+#pragma unroll
+        for (int h = 0; h < GH; ++h) {
+            sm_m[warp][h] = m[h];
+            sm_l[warp][h] = l[h];
+        }
     }
 #pragma unroll
-    for (int k = 0; k < kMaxDimsPerLane; ++k) sm_acc[warp][lane + 32 * k] = acc[k];
+    for (int h = 0; h < GH; ++h)
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) sm_acc[warp][h][lane + 32 * k] = acc[h][k];
     __syncthreads();
-    float M = -INFINITY;
+    for (int e = threadIdx.x; e < nh * hd; e += blockDim.x) {
+        const int h = e / hd, d = e - h * hd;
+        float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float wgt[kWarps], L = 0.f;
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sm_m[w][h]);
+        float L = 0.f, o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        wgt[w] = sm_m[w] == -INFINITY ? 0.f : exp2f(sm_m[w] - M);
-        L += wgt[w] * sm_l[w];
+        for (int w = 0; w < kWarps; ++w) {
+            const float wgt = sm_m[w][h] == -INFINITY ? 0.f : exp2f(sm_m[w][h] - M);
+            L += wgt * sm_l[w][h];
+            o += wgt * sm_acc[w][h][d];
+        }
+        static_cast<T*>(a.out)[((int64_t)row * a.num_heads + h0 + h) * hd + d] = Elt<T>::from_f(L > 0.f ? o / L : 0.f);
     }
-    T* out = static_cast<T*>(a.out) + ((int64_t)row * a.num_heads + head) * hd;
-    for (int d = threadIdx.x; d < hd; d += blockDim.x) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) o += wgt[w] * sm_acc[w][d];
-        out[d] = Elt<T>::from_f(L > 0.f ? o / L : 0.f);
+}
+
+template <typename T, bool FP8>
+cudaError_t launch_typed(const AttnArgs& a, cudaStream_t stream) {
+    const int G = a.num_heads / a.num_kv_heads;
+    const int dpl = a.head_dim <= 64 ? 2 : (a.head_dim <= 128 ? 4 : 8);
+    // query heads per CTA: the whole group up to 8 (4 with 8 dims per lane)
+    const int gh = G == 1 ? 1 : (G <= 4 || dpl == 8 ? 4 : 8);
+    dim3 grid((unsigned)a.total_q, (unsigned)(a.num_kv_heads * ((G + gh - 1) / gh)));
+    const dim3 block(kWarps * 32);
+#define PA_SIMT(D, H) attn_simt_kernel<T, FP8, D, H><<<grid, block, 0, stream>>>(a)
+    if (dpl == 2) {
+        if (gh == 1) PA_SIMT(2, 1);
+        else if (gh == 4) PA_SIMT(2, 4);
+        else PA_SIMT(2, 8);
+    } else if (dpl == 4) {
+        if (gh == 1) PA_SIMT(4, 1);
+        else if (gh == 4) PA_SIMT(4, 4);
+        else PA_SIMT(4, 8);
+    } else {
+        if (gh == 1) PA_SIMT(8, 1);
+        else PA_SIMT(8, 4);
     }
+#undef PA_SIMT
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -154,21 +203,18 @@ bool attn_simt_supported(int dtype, int head_dim) {
 
 cudaError_t launch_attn_simt(const AttnArgs& a, cudaStream_t stream) {
     if (a.total_q == 0) return cudaSuccess;
-    dim3 grid((unsigned)a.total_q, (unsigned)a.num_heads);
     if (a.kv_fp8) {
         switch (a.dtype) {
-            case 0: attn_simt_kernel<float, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
-            case 1: attn_simt_kernel<__nv_bfloat16, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
-            default: attn_simt_kernel<__half, true><<<grid, kWarps * 32, 0, stream>>>(a); break;
+            case 0: return launch_typed<float, true>(a, stream);
+            case 1: return launch_typed<__nv_bfloat16, true>(a, stream);
+            default: return launch_typed<__half, true>(a, stream);
         }
-        return cudaGetLastError();
     }
     switch (a.dtype) {
-        case 0: attn_simt_kernel<float, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
-        case 1: attn_simt_kernel<__nv_bfloat16, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
-        default: attn_simt_kernel<__half, false><<<grid, kWarps * 32, 0, stream>>>(a); break;
+        case 0: return launch_typed<float, false>(a, stream);
+        case 1: return launch_typed<__nv_bfloat16, false>(a, stream);
+        default: return launch_typed<__half, false>(a, stream);
     }
-    return cudaGetLastError();
 }
 
 }  // namespace pa

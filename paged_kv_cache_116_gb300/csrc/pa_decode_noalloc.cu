@@ -125,9 +125,8 @@ pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const
         return noalloc_fail(PA_ERR_UNSUPPORTED, "num_blocks * block_size must fit in int32");
     const int G = num_heads / num_kv_heads;
     if (!pa::decode_tc_supported(dtype, head_dim, block_size, G))
-        return noalloc_fail(PA_ERR_UNSUPPORTED, "pa_decode_noalloc takes bf16/f16, head_dim 64/128/256, "
-                                                "block_size 8 or a multiple of 16 up to 256, and at most 16 "
-                                                "query heads per KV head");
+        return noalloc_fail(PA_ERR_UNSUPPORTED, "pa_decode_noalloc takes bf16/f16, head_dim 64/128/256 and at "
+                                                "most 16 query heads per KV head");
     if (num_seqs == 0) return PA_OK;
     if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
         return noalloc_fail(PA_ERR_INVALID_ARG, "null pointer");

@@ -66,6 +66,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -195,12 +196,31 @@ __device__ __forceinline__ void tile_prefix(const int32_t* context_lens, int S, 
     __syncthreads();
 }
 
+// 16 bytes global -> shared, asynchronously (L2 only).
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+// Arrive on bar once this thread's earlier cp.async copies have landed (the
+// barrier counts the arrival among those it expects).
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Block sizes a 16-row (or two 8-row) TMA box per 128-byte chunk can load;
+// the others are gathered row by row.
+__host__ __device__ constexpr bool tma_block_size(int bs) { return bs == 8 || (bs % 16 == 0 && bs <= 256); }
+
 // T: element type of q and out.  FP8: the cache holds E4M3 codes plus
-// scales (the mma then runs in f16 whatever T is).
-template <typename T, int HD, int NT, bool FP8, bool PAIR>
+// scales (the mma then runs in f16 whatever T is).  GATHER (16-bit caches
+// whose block size no TMA box fits, e.g. 1, 2, 4 or 24): each stage's tile
+// is gathered with 16-byte cp.async copies, one token row at a time
+// through the block table, into the same swizzled layout the TMA boxes
+// give; the stage's barrier then counts one arrival per lane.
+template <typename T, int HD, int NT, bool FP8, bool PAIR, bool GATHER = false>
 __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                      const TcParams p) {
+    static_assert(!(GATHER && FP8), "code caches are loaded by TMA only");
     using Gm = Geo<HD, FP8>;
     constexpr int NW = Pipe<HD, FP8>::NW, R = Pipe<HD, FP8>::R, KS = Gm::KS;
     extern __shared__ uint8_t smem_raw[];
@@ -216,7 +236,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     // With programmatic dependent launch this grid may start while the
     // previous kernel on the stream (e.g. the K/V write) is still running;
     // every input is read after this wait.
-    if (threadIdx.x == 0) {  // kernel parameters: no need to wait for them
+    if (!GATHER && threadIdx.x == 0) {  // kernel parameters: no need to wait for them
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
     }
@@ -248,7 +268,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     uint8_t* wst = base + (size_t)warp * R * Gm::STAGE;
     float* wscl = scl + (size_t)warp * R * (Gm::SCL / 4);
     if (lane == 0) {
-        for (int r = 0; r < R; ++r) mbar_init(&wbar[r], 1);
+        for (int r = 0; r < R; ++r) mbar_init(&wbar[r], GATHER ? 32 : 1);
         mbar_fence_init();
     }
     __syncwarp();
@@ -288,8 +308,11 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 
     // ---- producer side: issue cursor, table window, TMA
     const uint64_t pol = l2_policy_evict_first();
-    int32_t tbl_cur2, tbl_next2;
-    int32_t tbl_cur = table_entry(lane, tbl_cur2), tbl_next = table_entry(32 + lane, tbl_next2);
+    int32_t tbl_cur2 = 0, tbl_next2 = 0, tbl_cur = 0, tbl_next = 0;
+    if constexpr (!GATHER) {
+        tbl_cur = table_entry(lane, tbl_cur2);
+        tbl_next = table_entry(32 + lane, tbl_next2);
+    }
     int win = 0, ip = 0;
     int is_, ih, ib;
     locate(f0, is_, ih, ib);
@@ -310,6 +333,33 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     // Issue one stage: tiles ip .. ip+TPS-1 that exist (ip is a multiple of
     // TPS, so they share one 32-tile table window).
     auto issue_next = [&]() {
+        if constexpr (GATHER) {
+            // one 16-token tile: lane pieces of 16 bytes, K and V rows of
+            // token r of the tile from its block (tokens past the context
+            // re-read the last one: masked later, and no table entry past
+            // ceil(L / bs) is touched)
+            const int us = is_, uh = ih, ub = ib;
+            advance();
+            const int slot = ip % R;
+            const int L_u = lens[us];
+            const int32_t* tb = p.block_tables + (int64_t)us * p.max_blocks;
+            constexpr int PPR = HD * 2 / 16;  // 16-byte pieces of one head's row
+            uint8_t* stage = wst + (size_t)slot * Gm::STAGE;
+#pragma unroll
+            for (int i = 0; i < BS * PPR / 32; ++i) {
+                const int pidx = lane + 32 * i, r = pidx / PPR, col16 = pidx - r * PPR;
+                const int tok = min(ub * BS + r, L_u - 1);
+                const int64_t prow = (int64_t)__ldg(tb + tok / bsz) * bsz + tok % bsz;
+                const int64_t off = ((prow * Hkv + uh) * HD) * 2 + col16 * 16;
+                const uint32_t dst =
+                    smem_u32(stage + (col16 >> 3) * BS * 128 + r * 128 + (((col16 & 7) ^ (r & 7)) << 4));
+                cp_async16(dst, static_cast<const uint8_t*>(p.k_pool) + off);
+                cp_async16(dst + Gm::TILE, static_cast<const uint8_t*>(p.v_pool) + off);
+            }
+            cp_async_arrive(&wbar[slot]);
+            ++ip;
+            return;
+        }
         const int w = ip >> 5;
         if (w != win) {
             tbl_cur = tbl_next;
@@ -1049,9 +1099,9 @@ size_t desc_ws_bytes(int32_t num_seqs, int32_t num_kv_heads) {
     return ((size_t)s * num_kv_heads * sizeof(int4) + 255) & ~(size_t)255;
 }
 
-template <typename T, int HD, int NT, bool FP8, bool PAIR = false>
+template <typename T, int HD, int NT, bool FP8, bool PAIR = false, bool GATHER = false>
 const void* kernel_ptr() {
-    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8, PAIR>);
+    return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8, PAIR, GATHER>);
 }
 
 template <int HD, bool FP8>
@@ -1073,13 +1123,17 @@ int grid_for(const void* kfn, int32_t num_seqs, int32_t num_kv_heads, int32_t ma
     return (int)(grid < 1 ? 1 : grid);
 }
 
-template <typename T, int HD, int NT, bool FP8, bool PAIR = false>
+template <typename T, int HD, int NT, bool FP8, bool PAIR = false, bool GATHER = false>
 cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* workspace, std::string* err,
                          cudaStream_t stream) {
     CUtensorMap tmK, tmV;
-    if (!make_kv_map(&tmK, a.k_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err) ||
-        !make_kv_map(&tmV, a.v_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err))
+    if (GATHER) {  // no boxes: the maps are not read
+        memset(&tmK, 0, sizeof(tmK));
+        memset(&tmV, 0, sizeof(tmV));
+    } else if (!make_kv_map(&tmK, a.k_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err) ||
+               !make_kv_map(&tmV, a.v_cache, a.dtype, FP8, num_blocks, a.block_size, a.num_kv_heads, HD, err)) {
         return cudaErrorInvalidValue;
+    }
     TcParams p;
     p.out = a.out;
     p.q = a.q;
@@ -1103,7 +1157,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.k_scales = a.k_scales;
     p.v_scales = a.v_scales;
 
-    const void* kfn = kernel_ptr<T, HD, NT, FP8, PAIR>();
+    const void* kfn = kernel_ptr<T, HD, NT, FP8, PAIR, GATHER>();
     const size_t smem = smem_bytes<HD, FP8>(a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -1119,7 +1173,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8, PAIR>, tmK, tmV, p);
+    e = cudaLaunchKernelEx(&cfg, decode_tc_kernel<T, HD, NT, FP8, PAIR, GATHER>, tmK, tmV, p);
     if (e != cudaSuccess) return e;
     // the split merge, one warp per (unit, query head), as a programmatic
     // dependent
@@ -1145,6 +1199,16 @@ cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* 
         return two ? launch_typed<T, 256, 2, true>(a, num_blocks, grid, ws, err, st)
                    : launch_typed<T, 256, 1, true>(a, num_blocks, grid, ws, err, st);
     }
+    if (!tma_block_size(a.block_size)) {
+        switch (a.head_dim) {
+            case 64: return two ? launch_typed<T, 64, 2, false, false, true>(a, num_blocks, grid, ws, err, st)
+                                : launch_typed<T, 64, 1, false, false, true>(a, num_blocks, grid, ws, err, st);
+            case 128: return two ? launch_typed<T, 128, 2, false, false, true>(a, num_blocks, grid, ws, err, st)
+                                 : launch_typed<T, 128, 1, false, false, true>(a, num_blocks, grid, ws, err, st);
+            default: return two ? launch_typed<T, 256, 2, false, false, true>(a, num_blocks, grid, ws, err, st)
+                                : launch_typed<T, 256, 1, false, false, true>(a, num_blocks, grid, ws, err, st);
+        }
+    }
     switch (a.head_dim) {
         case 64: return two ? launch_typed<T, 64, 2, false>(a, num_blocks, grid, ws, err, st)
                             : launch_typed<T, 64, 1, false>(a, num_blocks, grid, ws, err, st);
@@ -1160,16 +1224,28 @@ cudaError_t launch_dtype(const AttnArgs& a, int32_t num_blocks, int grid, void* 
 bool decode_tc_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8) {
     const bool hd_ok = kv_fp8 ? (head_dim == 128 || head_dim == 256)
                               : (head_dim == 64 || head_dim == 128 || head_dim == 256);
-    return (dtype == 1 || dtype == 2) && hd_ok && (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) &&
-           group >= 1 && group <= 16;
+    // 16-bit caches of any block size (boxes or a row gather); code caches by boxes only
+    const bool bs_ok = kv_fp8 ? tma_block_size(block_size) : block_size >= 1;
+    return (dtype == 1 || dtype == 2) && hd_ok && bs_ok && group >= 1 && group <= 16;
 }
 
 int decode_tc_grid(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                    int32_t max_context, int dtype, int32_t group, int64_t ctas_override, bool kv_fp8) {
-    (void)block_size;
     const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
     const bool two = group > 8;
     const bool bf = dtype == 1;
+    if (!kv_fp8 && !tma_block_size(block_size)) {  // the row-gather instances
+#define PA_GFN(HD)                                                                                           \
+    (bf ? (two ? kernel_ptr<__nv_bfloat16, HD, 2, false, false, true>()                                      \
+               : kernel_ptr<__nv_bfloat16, HD, 1, false, false, true>())                                     \
+        : (two ? kernel_ptr<__half, HD, 2, false, false, true>() : kernel_ptr<__half, HD, 1, false, false, true>()))
+        switch (head_dim) {
+            case 64: return grid_for<64, false>(PA_GFN(64), s, num_kv_heads, max_context, ctas_override);
+            case 128: return grid_for<128, false>(PA_GFN(128), s, num_kv_heads, max_context, ctas_override);
+            default: return grid_for<256, false>(PA_GFN(256), s, num_kv_heads, max_context, ctas_override);
+        }
+#undef PA_GFN
+    }
 #define PA_KFN(HD, F8)                                                                                      \
     (bf ? (two ? kernel_ptr<__nv_bfloat16, HD, 2, F8>() : kernel_ptr<__nv_bfloat16, HD, 1, F8>())          \
         : (two ? kernel_ptr<__half, HD, 2, F8>() : kernel_ptr<__half, HD, 1, F8>()))

@@ -214,7 +214,8 @@ def test_decode_append_equals_write_then_decode(pa, name, make, kernel):
 
 BS_CASES = []
 _r3 = np.random.default_rng(321)
-for _bs in (8, 32, 64, 128, 256):
+# 8 and multiples of 16: TMA boxes; 1, 2, 4, 12, 24: the row gather
+for _bs in (1, 2, 4, 8, 12, 24, 32, 64, 128, 256):
     for _i in range(2):
         _hd = int(_r3.choice([64, 128]))
         _g = int(_r3.choice([1, 4, 6]))
@@ -229,12 +230,29 @@ def test_decode_block_sizes_both_kernels(pa, bs, hd, g, lens, seed):
     kc, vc, bt = device_caches(w, DEV)
     exact = oracle_attention(w)
     for kernel in (1, 2):
-        compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel), exact)
+        for ctas in ((0, 3) if kernel == 2 else (0,)):
+            compare(w, run_decode(pa, w, kc, vc, bt, kernel=kernel, ctas=ctas), exact)
 
 
-@pytest.mark.parametrize("bs", [8, 32, 128])
+@pytest.mark.parametrize("bs", [1, 4, 12])
+def test_gathered_block_sizes_are_bit_identical_under_relabelling(pa, bs):
+    """The row-gather tiles (block sizes no TMA box fits) read blocks only
+    through the table: relabelling physical blocks changes no bit."""
+    w = W.decode_workload("gperm", "bf16", bs, 16, 4, 128, [1, 3 * bs + 1, 700, 33], seed=60 + bs)
+    kc, vc, bt = device_caches(w, DEV)
+    base = run_decode(pa, w, kc, vc, bt, kernel=2)
+    perm = torch.from_numpy(np.random.default_rng(bs).permutation(w.num_blocks)).to(DEV)
+    kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_decode(pa, w, kc2, vc2, bt2, kernel=2)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("bs", [1, 4, 8, 24, 32, 128])
 def test_decode_append_block_sizes(pa, bs):
-    w = W.decode_workload("ap_bs", "bf16", bs, 8, 2, 128, [1, bs - 1, bs, bs + 1, 3 * bs + 5], seed=bs)
+    w = W.decode_workload("ap_bs", "bf16", bs, 8, 2, 128, [1, max(bs - 1, 2), bs, bs + 1, 3 * bs + 5], seed=bs)
     kc, vc, bt = device_caches(w, DEV, after_step=False)
     lens = torch.from_numpy(w.seq_lens).to(DEV)
     mc = int(w.seq_lens.max())
