@@ -8,11 +8,13 @@ A step is one pass of the path over one batch, through the C ABI:
   mixed_varlen:     pa_copy_blocks (copy-on-write of the shared tails) ->
                     pa_slot_mapping -> pa_write_kv (every new token) ->
                     pa_varlen (prefill chunks + decode rows)
-  --kv-dtype fp8:   a decode workload over the quantized cache (E4M3 codes,
-                    one fp32 scale per token and KV head): pa_decode_append_fp8
+  --kv-dtype fp8:   a workload over the quantized cache (E4M3 codes, one
+                    fp32 scale per token and KV head); decode: pa_decode_append_fp8
                     (the new rows quantized into their slots, then the decode;
                     --unfused: pa_slot_mapping -> pa_write_kv_fp8 ->
-                    pa_decode_fp8); its K/V bytes are the codes plus the scales
+                    pa_decode_fp8); mixed_varlen: the block copies move code
+                    and scale blocks, pa_write_kv_fp8, pa_varlen_fp8; its
+                    K/V bytes are the codes plus the scales
 Inputs are resident in HBM.  Enough copies of the K/V pool to exceed twice
 the 129 MB L2 alternate between steps, so no step reads a pool the previous
 one left in L2.  The step is captured once per pool copy as a CUDA graph and
@@ -71,7 +73,7 @@ def parse():
     ap.add_argument("--unfused", action="store_true",
                     help="decode step as pa_slot_mapping + pa_write_kv + pa_decode instead of pa_decode_append")
     ap.add_argument("--kv-dtype", choices=["native", "fp8"], default="native",
-                    help="fp8: decode workloads over an FP8 E4M3 cache (queries keep the workload's type)")
+                    help="fp8: the workload over an FP8 E4M3 cache (queries keep the workload's type)")
     return ap.parse_args()
 
 
@@ -263,7 +265,7 @@ def oracle_step(w, kc, vc, q, num_threads=0):
 
 
 def oracle_setup_fp8(w):
-    """Oracle-side quantized pool (codes and scales) of a host decode workload."""
+    """Oracle-side quantized pool (codes and scales) of a host workload after its step's writes and copies."""
     import numpy as np
 
     import oracle
@@ -275,6 +277,9 @@ def oracle_setup_fp8(w):
     vs = ks.copy()
     s = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
     oracle.write_kv_fp8(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), w.dtype, s, kc, vc, ks, vs)
+    if w.cow_pairs.shape[0]:
+        oracle.copy_blocks([kc], [vc], w.cow_pairs)
+        oracle.copy_blocks([ks], [vs], w.cow_pairs)
     s = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
     oracle.write_kv_fp8(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), w.dtype, s, kc, vc, ks, vs)
     return (kc, vc, ks, vs), W.raw_numpy(w.q)
@@ -518,8 +523,6 @@ def main():
     S, hq, hkv, hd, bs = w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.block_size
     decode = w.is_decode and w.cow_pairs.shape[0] == 0
     fp8 = args.kv_dtype == "fp8"
-    if fp8 and not decode:
-        raise SystemExit("--kv-dtype fp8 applies to the decode workloads")
     max_ctx, max_q = int(w.seq_lens.max()), int(w.query_lens.max())
     kv_bytes = fp8_kv_bytes(w) if fp8 else w.kv_bytes_read()
     N = int(w.query_lens.sum())
@@ -562,16 +565,20 @@ def main():
     q, new_k, new_v = w.q.to(dev).contiguous(), w.new_k.to(dev).contiguous(), w.new_v.to(dev).contiguous()
     out = torch.empty_like(q)
     slot_buf = torch.empty(N, dtype=torch.int64, device=dev)
-    if decode:
+    if not decode:
+        ws_bytes = (pa.pa_varlen_fp8_workspace_size if fp8 else pa.pa_varlen_workspace_size)(
+            S, N, max_q, hq, hkv, hd, bs, max_ctx, tdt)
+    elif decode:
         ws_bytes = (pa.pa_decode_fp8_workspace_size if fp8 else pa.pa_decode_workspace_size)(S, hq, hkv, hd, bs,
                                                                                               max_ctx, tdt)
-    else:
-        ws_bytes = pa.pa_varlen_workspace_size(S, N, max_q, hq, hkv, hd, bs, max_ctx, tdt)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def attend(pool, qq, tables, ll, cuq, st, o=None):
         o = out if o is None else o
-        if fp8:
+        if fp8 and not decode:
+            pa.pa_varlen_fp8(o, qq, *pool, tables, ll, cuq, max_q, max_ctx, w.scale, causal=w.causal,
+                             workspace=ws, stream=st)
+        elif fp8:
             pa.pa_decode_fp8(o, qq, *pool, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
         elif decode:
             pa.pa_decode(o, qq, *pool, tables, ll, max_ctx, w.scale, workspace=ws, stream=st)
@@ -587,6 +594,8 @@ def main():
         d_q, d_k, d_v, d_bt, d_lens, d_cu, d_seq, d_pos, d_pairs = t_in
         if d_pairs.shape[0]:
             pa.pa_copy_blocks(pool[0], pool[1], d_pairs, stream=st)
+            if fp8:  # the scale pools' blocks move with the codes
+                pa.pa_copy_blocks(pool[2], pool[3], d_pairs, stream=st)
         pa.pa_slot_mapping(d_bt, d_seq, d_pos, bs, slot_out=slot_buf, stream=st)
         (pa.pa_write_kv_fp8 if fp8 else pa.pa_write_kv)(d_k, d_v, slot_buf, *pool, stream=st)
         attend(pool, d_q, d_bt, d_lens, d_cu, st, o)
@@ -618,7 +627,7 @@ def main():
     fused_in_kernel = tc_decode and (not fp8 or (hd == 128 and S * hkv <= sms * 3 * 4))
     # the tensor-core decode is two launches: the decode and its split merge
     launches_per_step = ((1 if fused_in_kernel else 2) if fused else 3 + (1 if pairs.shape[0] else 0)) + \
-        (1 if tc_decode else 0)
+        (1 if tc_decode else 0) + (1 if fp8 and pairs.shape[0] else 0)
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -677,7 +686,7 @@ def main():
     # same pools (prefill chunks: tensor-bound; decode rows: HBM-bound); in the
     # mixed call they share one launch, so these times do not add up to it
     parts = None
-    if not decode and not args.no_extras:
+    if not decode and not fp8 and not args.no_extras:
         parts = {}
         peaks_p, _ = measured_peaks()
         for name, sel in (("prefill_chunks", np.where(w.query_lens > 1)[0]),
@@ -820,6 +829,15 @@ def main():
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
                 "traffic": traffic_record(args.workload + ("_fp8" if fp8 else ""), "pa_decode_tc.cu"),
                 "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
+    elif fp8:
+        # the mixed step over a code cache runs on the CUDA-core kernel: its
+        # bound is issue, reported here against the copy peak in K/V bytes
+        achieved = kv_bytes / (kern_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": "attn_simt_kernel<FP8> (pa_varlen_fp8, CUDA-core path)",
+                "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": kv_bytes,
+                "algorithmic_flops": varlen_flops(w), "traffic": None, "kernel_us": kern_ms * 1e3,
+                "kernel_us_median_of_51": kern_med_us}
     else:
         fl = varlen_flops(w)
         achieved = fl / (kern_ms / 1e3) / 1e12
@@ -846,7 +864,7 @@ def main():
                                     "pa_decode_append_fp8" if fp8 else "pa_decode_append",
                                     "quantizing write" if fp8 else "write") if fused else
                                 ("pa_copy_blocks + " if pairs.shape[0] else "") + "pa_slot_mapping + " +
-                                ("pa_write_kv_fp8 + pa_decode_fp8" if fp8 else
+                                (("pa_write_kv_fp8 + " + ("pa_decode_fp8" if decode else "pa_varlen_fp8")) if fp8 else
                                  "pa_write_kv + " + ("pa_decode" if decode else "pa_varlen"))) +
                                ", replayed as a CUDA graph",
                        "seed": 0,

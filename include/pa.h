@@ -351,6 +351,32 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * pa_varlen_fp8 -- pa_varlen over a quantized cache (see pa_write_kv_fp8):
+ * the handbook's paged_attention ("分页 KV Cache", §分页注意力) with each key
+ * and value element its code's value times its (token, KV head) row's scale
+ * (the quantized cache of "KV cache：容量推导、分页与回收", §输入放得下，输出
+ * 还要留空间).  Prefill chunks and decode rows mix as in pa_varlen; causal
+ * as there.  Runs on the CUDA-core kernel (fp32 arithmetic, any head_dim up
+ * to 256 and any block size), which reads each code row once for up to 8
+ * query heads of its KV head.
+ *   out, q:             device [total_q, num_heads, head_dim] of dtype (PA_F32/BF16/F16)
+ *   k_codes, v_codes:   device uint8 [num_blocks, block_size, num_kv_heads, head_dim]
+ *   k_scales, v_scales: device fp32 [num_blocks, num_kv_heads, block_size], 16-byte aligned
+ *   workspace:          pa_varlen_fp8_workspace_size(...) bytes (0 today: may be NULL)
+ * The other arguments and the error behaviour are pa_varlen's.
+ */
+PA_API size_t pa_varlen_fp8_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                           int32_t max_context, int dtype);
+PA_API pa_status pa_varlen_fp8(void* out, const void* q, const void* k_codes, const void* v_codes,
+                               const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                               int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                               int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                               int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                               int32_t max_context, float scale, int causal, int dtype, void* workspace,
+                               size_t workspace_bytes, void* stream);
+
+/*
  * pa_decode_noalloc -- pa_decode for callers that cannot allocate device
  * memory when they run it: a runtime or plugin host that hands out all
  * device memory from its own pool and forbids cudaMalloc in its callbacks, a

@@ -10,4 +10,4 @@ from ._binding import (  # noqa: F401
     PA_OPT_FP8_PAIR_STEP, PA_OPT_VARLEN_KERNEL, PAError, lib, pa_copy_blocks, pa_decode, pa_decode_append, pa_decode_append_fp8,
     pa_decode_fp8, pa_decode_fp8_workspace_size, pa_decode_noalloc, pa_decode_workspace_size, pa_device_status,
     pa_get_option, pa_selftest_wait_timeout, pa_set_check_mode, pa_set_option, pa_slot_mapping, pa_swap_blocks,
-    pa_varlen, pa_varlen_workspace_size, pa_write_kv, pa_write_kv_fp8)
+    pa_varlen, pa_varlen_fp8, pa_varlen_fp8_workspace_size, pa_varlen_workspace_size, pa_write_kv, pa_write_kv_fp8)

@@ -23,7 +23,7 @@ EXPORTS = ("pa_status_string", "pa_last_error", "pa_set_option", "pa_get_option"
            "pa_device_status", "pa_slot_mapping", "pa_write_kv", "pa_copy_blocks", "pa_decode_workspace_size",
            "pa_decode", "pa_decode_append", "pa_varlen_workspace_size", "pa_varlen", "pa_decode_noalloc",
            "pa_swap_blocks", "pa_write_kv_fp8", "pa_decode_fp8_workspace_size", "pa_decode_fp8",
-           "pa_decode_append_fp8", "pa_selftest_wait_timeout")
+           "pa_decode_append_fp8", "pa_selftest_wait_timeout", "pa_varlen_fp8_workspace_size", "pa_varlen_fp8")
 
 
 class PAError(RuntimeError):
@@ -71,6 +71,9 @@ def lib():
         "pa_decode_noalloc": ([vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i32, i32, cf, ci, vp], ci),
         "pa_varlen": ([vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, cf, ci, ci, vp,
                        sz, vp], ci),
+        "pa_varlen_fp8_workspace_size": ([i32, i32, i32, i32, i32, i32, i32, i32, ci], sz),
+        "pa_varlen_fp8": ([vp, vp, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, i32, cf,
+                           ci, ci, vp, sz, vp], ci),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -317,4 +320,28 @@ def pa_varlen(out, q, k_cache, v_cache, block_tables, seq_lens, cu_seqlens_q, ma
                          bs, max_context, float(scale), 1 if causal else 0, _dtype(q), _ptr(workspace), ws_bytes,
                          _stream(stream))
     _check(st, "pa_varlen")
+    return out
+
+
+def pa_varlen_fp8_workspace_size(num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, block_size,
+                                 max_context, dtype):
+    code = DTYPE_CODE[dtype] if isinstance(dtype, torch.dtype) else dtype
+    return lib().pa_varlen_fp8_workspace_size(num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim,
+                                              block_size, max_context, code)
+
+
+def pa_varlen_fp8(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, seq_lens, cu_seqlens_q, max_q,
+                  max_context, scale, causal=True, workspace=None, stream=None):
+    """Mixed prefill/decode over a quantized cache: codes [NB, bs, Hkv, hd] uint8, scales [NB, Hkv, bs] fp32;
+    q, out [T, Hq, hd] of the query type; cu_seqlens_q [S+1]; seq_lens [S]."""
+    _dev(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, seq_lens, cu_seqlens_q, workspace)
+    nb, bs, hkv, hd = k_codes.shape
+    T, hq, _ = q.shape
+    S = seq_lens.shape[0]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().pa_varlen_fp8(_ptr(out), _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scales), _ptr(v_scales),
+                             _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), _ptr(cu_seqlens_q), S, T, max_q,
+                             hq, hkv, hd, nb, bs, max_context, float(scale), 1 if causal else 0, _dtype(q),
+                             _ptr(workspace), ws_bytes, _stream(stream))
+    _check(st, "pa_varlen_fp8")
     return out

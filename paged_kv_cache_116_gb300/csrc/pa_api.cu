@@ -578,11 +578,17 @@ size_t pa_varlen_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q
     return pa::varlen_umma_workspace(num_seqs, total_q, G);
 }
 
-pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
-                    int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_seqlens_q, int32_t num_seqs,
-                    int32_t total_q, int32_t max_q, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
-                    int32_t num_blocks, int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// k_scales != nullptr: the caches hold E4M3 codes with these scales.
+static pa_status varlen_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                             int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_seqlens_q,
+                             int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks, int32_t block_size,
+                             int32_t max_context, float scale, int causal, int dtype, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    const bool fp8 = k_scales != nullptr;
     pa_status g = check_geometry(num_heads, num_kv_heads, head_dim, num_blocks, block_size, dtype);
     if (g != PA_OK) return g;
     if (num_seqs < 0 || total_q < 0 || max_q < 0 || max_blocks < 0 || max_context < 0)
@@ -592,12 +598,15 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
         return fail(PA_ERR_INVALID_ARG, "null pointer");
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
         return fail(PA_ERR_INVALID_ARG, "out, q and the caches must be 16-byte aligned");
+    if (fp8 && (!v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+        return fail(PA_ERR_INVALID_ARG, "k_scales and v_scales must be non-null and 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
-    const bool um_ok = pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
+    const bool um_ok = !fp8 && pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
     const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
     if (want == 2 && !um_ok)
-        return fail(PA_ERR_UNSUPPORTED, "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128 and "
-                                        "block_size 8 or a multiple of 16");
+        return fail(PA_ERR_UNSUPPORTED, fp8 ? "the tcgen05 varlen kernel does not read a code cache"
+                                            : "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128 and "
+                                              "block_size 8 or a multiple of 16");
     const bool use_um = um_ok && (want == 2 || want == 0);
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {
@@ -636,6 +645,9 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     a.causal = causal ? 1 : 0;
     a.dtype = dtype;
     a.max_context = max_context;
+    a.kv_fp8 = fp8 ? 1 : 0;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
     if (use_um) {
         // optional workspace: the tensor-core kernel then runs its work
         // longest first (a plan kernel sorts it); without one, in request order
@@ -656,6 +668,38 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
     }
     cudaError_t e = pa::launch_attn_simt(a, st);
     return e == cudaSuccess ? PA_OK : cuda_fail(e, "pa_varlen launch");
+}
+
+extern "C" {
+
+pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                    int32_t max_blocks, const int32_t* seq_lens, const int32_t* cu_seqlens_q, int32_t num_seqs,
+                    int32_t total_q, int32_t max_q, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t num_blocks, int32_t block_size, int32_t max_context, float scale, int causal, int dtype,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    return varlen_impl(out, q, k_cache, v_cache, nullptr, nullptr, block_tables, max_blocks, seq_lens, cu_seqlens_q,
+                       num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                       max_context, scale, causal, dtype, workspace, workspace_bytes, stream);
+}
+
+size_t pa_varlen_fp8_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                    int32_t max_context, int dtype) {
+    (void)num_seqs, (void)total_q, (void)max_q, (void)num_heads, (void)num_kv_heads, (void)head_dim,
+        (void)block_size, (void)max_context, (void)dtype;
+    return 0;
+}
+
+pa_status pa_varlen_fp8(void* out, const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                        const float* v_scales, const int32_t* block_tables, int32_t max_blocks,
+                        const int32_t* seq_lens, const int32_t* cu_seqlens_q, int32_t num_seqs, int32_t total_q,
+                        int32_t max_q, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim, int32_t num_blocks,
+                        int32_t block_size, int32_t max_context, float scale, int causal, int dtype, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    if (num_seqs > 0 && total_q > 0 && (!k_scales || !v_scales)) return fail(PA_ERR_INVALID_ARG, "null pointer");
+    return varlen_impl(out, q, k_codes, v_codes, k_scales, v_scales, block_tables, max_blocks, seq_lens,
+                       cu_seqlens_q, num_seqs, total_q, max_q, num_heads, num_kv_heads, head_dim, num_blocks,
+                       block_size, max_context, scale, causal, dtype, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -104,7 +104,7 @@ FP8_NAN_CODE = 0x7F
 def oracle_fp8_caches(w):
     """Oracle code pools [NB, bs, Hkv, hd] (NaN code everywhere) and scale
     pools [NB, Hkv, bs] (NaN everywhere) after the quantizing write of the
-    workload's cached rows and then its new rows."""
+    workload's cached rows, the step's block copies, and its new rows."""
     shape = (w.num_blocks, w.block_size, w.num_kv_heads, w.head_dim)
     sshape = (w.num_blocks, w.num_kv_heads, w.block_size)
     kc = np.full(shape, FP8_NAN_CODE, np.uint8)
@@ -113,6 +113,9 @@ def oracle_fp8_caches(w):
     vs = ks.copy()
     slots = oracle.slot_mapping(w.pre_block_tables, w.pre_seq_idx, w.pre_pos, w.block_size)
     oracle.write_kv_fp8(W.raw_numpy(w.pre_k), W.raw_numpy(w.pre_v), w.dtype, slots, kc, vc, ks, vs)
+    if w.cow_pairs.shape[0]:
+        oracle.copy_blocks([kc], [vc], w.cow_pairs)
+        oracle.copy_blocks([ks], [vs], w.cow_pairs)
     slots = oracle.slot_mapping(w.block_tables, w.new_seq_idx, w.new_pos, w.block_size)
     oracle.write_kv_fp8(W.raw_numpy(w.new_k), W.raw_numpy(w.new_v), w.dtype, slots, kc, vc, ks, vs)
     return kc, vc, ks, vs
@@ -137,6 +140,10 @@ def device_fp8_caches(w, dev, after_step=True):
                                    w.block_size)
         pa.pa_write_kv_fp8(w.pre_k.to(dev), w.pre_v.to(dev), slots, kc, vc, ks, vs)
     if after_step:
+        if w.cow_pairs.shape[0]:
+            pairs = torch.from_numpy(w.cow_pairs).to(dev)
+            pa.pa_copy_blocks(kc, vc, pairs)
+            pa.pa_copy_blocks(ks, vs, pairs)
         slots = pa.pa_slot_mapping(bt, torch.from_numpy(w.new_seq_idx).to(dev), torch.from_numpy(w.new_pos).to(dev),
                                    w.block_size)
         pa.pa_write_kv_fp8(w.new_k.to(dev), w.new_v.to(dev), slots, kc, vc, ks, vs)

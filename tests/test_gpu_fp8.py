@@ -456,3 +456,75 @@ def test_fp8_decode_more_sequences_than_one_launch_takes(pa):
     kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
     exact = oracle_fp8_attention(w, *oracle_fp8_caches(w))
     compare(w, run_decode_fp8(pa, w, kc, vc, ks, vs, bt), exact)
+
+
+# ---------------------------------------------------------------- varlen over the quantized cache
+
+def run_varlen_fp8(pa, w, pools, causal=None):
+    kc, vc, ks, vs, bt = pools
+    out = torch.full(tuple(w.q.shape), float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
+    mq, mc = int(w.query_lens.max()), int(w.seq_lens.max())
+    pa.pa_varlen_fp8(out, w.q.to(DEV), kc, vc, ks, vs, bt, torch.from_numpy(w.seq_lens).to(DEV),
+                     torch.from_numpy(w.query_start_loc).to(DEV), mq, mc, w.scale,
+                     causal=w.causal if causal is None else causal)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_varlen_fp8(w, opools, causal):
+    kc, vc, ks, vs = opools
+    return oracle.paged_attention_fp8(W.raw_numpy(w.q), w.dtype, kc, vc, ks, vs, w.block_tables, w.seq_lens,
+                                      w.query_start_loc, w.scale, causal)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_varlen_fp8_handbook_layout(pa, dtype):
+    """The handbook's three requests (a decode, a full prefill, a chunk after
+    cached context) over an FP8 cache, causal and not."""
+    w = W.handbook_check(dtype=dtype)
+    pools = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal(pools[:4], opools)
+    for causal in (True, False):
+        err = compare(w, run_varlen_fp8(pa, w, pools, causal=causal), oracle_varlen_fp8(w, opools, causal))
+        if dtype == "f32":
+            assert err < 1e-5
+
+
+def test_varlen_fp8_mixed_step_with_cow_full(pa):
+    """The mixed varlen step (16 prefill chunks after cached context, 240
+    decode rows of 60 sampling groups sharing a prompt, the copy-on-write of
+    the shared tails) over an FP8 cache: codes and scales bit-exact after
+    the step's quantizing writes and block copies, attention against the
+    oracle with num_new > 1."""
+    w = W.mixed_varlen(device=DEV)
+    pools = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal(pools[:4], opools)
+    compare(w, run_varlen_fp8(pa, w, pools), oracle_varlen_fp8(w, opools, True))
+
+
+VARLEN_FP8_CASES = []
+_r4 = np.random.default_rng(909)
+for _i in range(8):
+    _bs = int(_r4.choice([1, 4, 16, 32]))
+    _hd = int(_r4.choice([64, 96, 128]))
+    _g = int(_r4.choice([1, 3, 6, 12]))
+    _hkv = int(_r4.choice([1, 2]))
+    _dt = str(_r4.choice(["f32", "bf16", "f16"]))
+    _S = int(_r4.integers(1, 6))
+    _lens = _r4.integers(1, 3 * _bs + 60, _S)
+    _q = np.minimum(_lens, _r4.integers(1, 50, _S))
+    _q[_r4.random(_S) < 0.3] = 1
+    VARLEN_FP8_CASES.append((_dt, _bs, _hd, _g, _hkv, _lens.tolist(), _q.tolist(), 950 + _i))
+
+
+@pytest.mark.parametrize("dt,bs,hd,g,hkv,lens,qlens,seed", VARLEN_FP8_CASES)
+def test_random_varlen_fp8(pa, dt, bs, hd, g, hkv, lens, qlens, seed):
+    w = W.varlen_workload("vfp8", dt, bs, g * hkv, hkv, hd, lens, qlens, seed=seed)
+    pools = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal(pools[:4], opools)
+    for causal in (True, False):
+        compare(w, run_varlen_fp8(pa, w, pools, causal=causal), oracle_varlen_fp8(w, opools, causal))
+
