@@ -829,8 +829,19 @@ def main():
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
                 "traffic": traffic_record(args.workload + ("_fp8" if fp8 else ""), "pa_decode_tc.cu"),
                 "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
+    elif fp8 and w.dtype in ("bf16", "f16") and hd == 128 and (bs == 8 or (bs % 16 == 0 and bs <= 256)):
+        # the mixed step over a code cache on the tensor cores (codes turned
+        # into f16 in shared memory by the producer warps)
+        fl = varlen_flops(w)
+        achieved = fl / (kern_ms / 1e3) / 1e12
+        peak = peaks["bf16_tflops"]  # the f16 rate equals the bf16 rate
+        roof = {"bound": "tensor", "kernel": "varlen_umma_kernel<FP8> (pa_varlen_fp8, tcgen05)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_kind": kind + " bf16_tflops (burst; f16 runs at the same rate)", "algorithmic_flops": fl,
+                "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9, "traffic": None,
+                "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
     elif fp8:
-        # the mixed step over a code cache runs on the CUDA-core kernel: its
+        # the mixed step over a code cache on the CUDA-core kernel: its
         # bound is issue, reported here against the copy peak in K/V bytes
         achieved = kv_bytes / (kern_ms / 1e3) / 1e9
         roof = {"bound": "hbm", "kernel": "attn_simt_kernel<FP8> (pa_varlen_fp8, CUDA-core path)",

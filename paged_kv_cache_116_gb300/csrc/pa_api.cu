@@ -601,10 +601,11 @@ static pa_status varlen_impl(void* out, const void* q, const void* k_cache, cons
     if (fp8 && (!v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
         return fail(PA_ERR_INVALID_ARG, "k_scales and v_scales must be non-null and 16-byte aligned");
     if (!pa::attn_simt_supported(dtype, head_dim)) return fail(PA_ERR_UNSUPPORTED, "head_dim must be in [1, 256]");
-    const bool um_ok = !fp8 && pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads);
+    const bool um_ok = pa::varlen_umma_supported(dtype, head_dim, block_size, num_heads / num_kv_heads, fp8);
     const int64_t want = g_options[PA_OPT_VARLEN_KERNEL];
     if (want == 2 && !um_ok)
-        return fail(PA_ERR_UNSUPPORTED, fp8 ? "the tcgen05 varlen kernel does not read a code cache"
+        return fail(PA_ERR_UNSUPPORTED, fp8 ? "the tcgen05 varlen kernel over a code cache takes bf16/f16 "
+                                              "queries, head_dim 128 and block_size 8 or a multiple of 16"
                                             : "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128 and "
                                               "block_size 8 or a multiple of 16");
     const bool use_um = um_ok && (want == 2 || want == 0);
@@ -685,9 +686,12 @@ pa_status pa_varlen(void* out, const void* q, const void* k_cache, const void* v
 size_t pa_varlen_fp8_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                                     int32_t max_context, int dtype) {
-    (void)num_seqs, (void)total_q, (void)max_q, (void)num_heads, (void)num_kv_heads, (void)head_dim,
-        (void)block_size, (void)max_context, (void)dtype;
-    return 0;
+    (void)max_q, (void)max_context;
+    if (num_seqs <= 0 || total_q <= 0 || num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads) return 0;
+    const int G = num_heads / num_kv_heads;
+    if (g_options[PA_OPT_VARLEN_KERNEL] == 1 || !pa::varlen_umma_supported(dtype, head_dim, block_size, G, true))
+        return 0;
+    return pa::varlen_umma_workspace(num_seqs, total_q, G);
 }
 
 pa_status pa_varlen_fp8(void* out, const void* q, const void* k_codes, const void* v_codes, const float* k_scales,

@@ -157,12 +157,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
-__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                     smem_u32(smem_dst)),
-                 "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 // 16-token tiles per sequence and their exclusive prefix over the batch,
 // into shared memory (prefix[S + 1]; lens[S] gets the lengths unless null).
@@ -402,7 +396,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 const int32_t r = hf ? row2 : row;
                 const int64_t si = (int64_t)(r / bsz) * Hkv * bsz + (int64_t)ihj * bsz + r % bsz;
                 float* sd = wscl + slot * (Gm::SCL / 4) + j * Gm::TSCL + is_v * BS + hf * 8;
-                bulk_load(sd, (is_v ? p.v_scales : p.k_scales) + si, halves == 2 ? 32 : 64, &wbar[slot]);
+                bulk_g2s(sd, (is_v ? p.v_scales : p.k_scales) + si, halves == 2 ? 32 : 64, &wbar[slot]);
             }
         }
         ip += nt_stage;

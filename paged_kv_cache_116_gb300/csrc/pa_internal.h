@@ -126,7 +126,7 @@ cudaError_t launch_selftest_wait(uint32_t polls, cudaStream_t stream);
 uint32_t selftest_status(bool clear);
 
 // ---- tcgen05 varlen (pa_varlen_umma.cu)
-bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group);
+bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8 = false);
 // Bytes of the optional workspace that lets the kernel run its work longest first.
 size_t varlen_umma_workspace(int32_t num_seqs, int64_t total_q, int32_t group);
 // workspace: nullptr (request order), or varlen_umma_workspace(...) bytes.

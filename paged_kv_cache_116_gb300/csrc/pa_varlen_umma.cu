@@ -60,11 +60,13 @@
 // by binary search.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 #include <string>
 #include <type_traits>
@@ -117,6 +119,9 @@ struct UmParams {
     const int32_t* plan;
     const int2* items;
     const int32_t* dec_req;
+    // quantized cache (FP8 mode): fp32 scales [num_blocks, num_kv_heads, block_size]
+    const float* k_scales;
+    const float* v_scales;
 };
 
 template <int HD>
@@ -131,15 +136,20 @@ struct UGeo {
     static constexpr int V_OFF = K_OFF + R * TILE;
     static constexpr int BAR_OFF = V_OFF + R * TILE;
     // q_full, k_full[R], k_empty[R], v_full[R], v_empty[R],
-    // per tile: s_full, p_full, o_done; v_zeroed
-    static constexpr int NBAR = 1 + 4 * R + 6 + 1;
+    // per tile: s_full, p_full, o_done; v_zeroed;
+    // code cache only: k_conv[R], v_conv[R] (a slot's codes turned into
+    // f16), q_conv (the Q tiles in f16)
+    static constexpr int NBAR = 1 + 4 * R + 6 + 1 + 2 * R + 1;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TBL_OFF = TADDR_OFF + 16;                 // two producers' table windows
     static constexpr int TBL_INTS = 2 * kTableWindow;              // rows of each group's first and second box
-    static constexpr int CU_OFF = TBL_OFF + 2 * TBL_INTS * 4;
+    // code cache: K then V scales per slot (targets of 16-byte-aligned bulk copies)
+    static constexpr int SCL_OFF = (TBL_OFF + 2 * TBL_INTS * 4 + 127) / 128 * 128;
+    static constexpr int CU_OFF = SCL_OFF + 2 * R * BK * 4;
 };
 
 static_assert(DG * DR <= UGeo<64>::NBAR, "a decode CTA's warps use the kernel's barriers");
+static_assert(UGeo<128>::SCL_OFF % 128 == 0 && UGeo<64>::SCL_OFF % 128 == 0, "scale area aligned for bulk copies");
 static_assert(DG * DR * 2 * BS * 64 * 2 <= UGeo<64>::BAR_OFF && DG * DR * 2 * BS * 128 * 2 <= UGeo<128>::BAR_OFF,
               "decode warps' stages fit below the barriers");
 
@@ -153,13 +163,22 @@ size_t um_smem_bytes(int num_seqs) {
 // wst: the warp's DR stages of a 16-token K tile then V tile (1024-byte
 // aligned, 128-byte swizzle as the tensor maps write them); wbar: DR
 // mbarriers.  Returns false if a bounded wait ran out.
-template <typename T, int HD, int NT>
+// FP8 (head_dim 128): the cache holds E4M3 codes with scales; each tile's
+// codes land in the tile's second 128-byte chunk (where f16 row r of that
+// chunk goes) and its 16 K and 16 V scales in `wscl` [DR][2][16]; once the
+// tile has landed the warp turns it into f16 code x scale in place (V rows
+// past the context become zeros), then the mma runs in f16.
+template <typename T, int HD, int NT, bool FP8 = false>
 __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtensorMap* tmV, const UmParams& p,
-                                            int req, int kvh, uint8_t* wst, uint64_t* wbar, int lane) {
+                                            int req, int kvh, uint8_t* wst, uint64_t* wbar, float* wscl,
+                                            int lane) {
+    static_assert(!FP8 || HD == 128, "code tiles at head_dim 128");
+    using MT = typename std::conditional<FP8, __half, T>::type;  // the mma operand type
     constexpr int CH = HD / 64, KS = HD / 16;
     constexpr int TILE = BS * HD * 2;  // bytes of a 16-token K (or V) tile
     constexpr int STAGE = 2 * TILE;
     const int G = p.group;
+    const int Hkv = p.num_heads / G;
     const int L = p.seq_lens[req], qrow0 = p.cu[req];
     T* out = static_cast<T*>(p.out) + ((int64_t)qrow0 * p.num_heads + (int64_t)kvh * G) * HD;
     const int ntl = (L + BS - 1) / BS;
@@ -185,7 +204,7 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
     int32_t trow2, trow = entry(lane, trow2);  // lane i: tile 32 win + i
     int win = 0;
     const int halves = bsz == 8 ? 2 : 1;
-    const int nbox = CH * 2 * halves;
+    const int nbox = FP8 ? 4 * halves : CH * 2 * halves;  // FP8: K, V code boxes and K, V scale copies
     auto issue = [&](int t) {
         if ((t >> 5) != win) {
             win = t >> 5;
@@ -193,12 +212,26 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
         }
         const int slot = t % DR;
         const int32_t row = __shfl_sync(0xffffffffu, trow, t & 31), row2 = __shfl_sync(0xffffffffu, trow2, t & 31);
-        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], (uint32_t)(2 * TILE));
+        if (lane == 0) mbar_arrive_expect_tx(&wbar[slot], FP8 ? (uint32_t)(2 * BS * (128 + 4)) : (uint32_t)(2 * TILE));
         fence_proxy_async_smem();  // this slot's previous tile was read by ldmatrix
         if (lane < nbox) {
-            const int hf = lane % halves, c = (lane / halves) % CH, is_v = lane / (halves * CH);
-            uint8_t* dst = wst + slot * STAGE + is_v * TILE + c * BS * 128 + hf * 1024;
-            tma_load_3d(dst, is_v ? tmV : tmK, &wbar[slot], 0, kvh * CH + c, hf ? row2 : row, pol);
+            if constexpr (FP8) {
+                const int hf = lane % halves, kind = lane / halves;  // 0 K codes, 1 V codes, 2 K scales, 3 V scales
+                const int is_v = kind & 1;
+                const int32_t r = hf ? row2 : row;
+                if (kind < 2) {
+                    tma_load_3d(wst + slot * STAGE + is_v * TILE + BS * 128 + hf * 1024, is_v ? tmV : tmK,
+                                &wbar[slot], 0, kvh, r, pol);
+                } else {
+                    const int64_t si = (int64_t)(r / bsz) * Hkv * bsz + (int64_t)kvh * bsz + r % bsz;
+                    bulk_g2s(wscl + (slot * 2 + is_v) * BS + hf * 8, (is_v ? p.v_scales : p.k_scales) + si,
+                             (uint32_t)(BS * 4 / halves), &wbar[slot]);
+                }
+            } else {
+                const int hf = lane % halves, c = (lane / halves) % CH, is_v = lane / (halves * CH);
+                uint8_t* dst = wst + slot * STAGE + is_v * TILE + c * BS * 128 + hf * 1024;
+                tma_load_3d(dst, is_v ? tmV : tmK, &wbar[slot], 0, kvh * CH + c, hf ? row2 : row, pol);
+            }
         }
     };
     int ip = 0;
@@ -223,6 +256,13 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
                 const T* qp = qbase + (int64_t)hh * HD + kk * 16 + 2 * c4;
                 qb[kk][nt][0] = *reinterpret_cast<const uint32_t*>(qp);
                 qb[kk][nt][1] = *reinterpret_cast<const uint32_t*>(qp + 8);
+                if (FP8 && !std::is_same<T, __half>::value) {  // the mma runs in f16
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const T* x = reinterpret_cast<const T*>(&qb[kk][nt][e]);
+                        qb[kk][nt][e] = pack2<__half>(Elt<T>::to_f(x[0]), Elt<T>::to_f(x[1]));
+                    }
+                }
             } else {
                 qb[kk][nt][0] = qb[kk][nt][1] = 0u;
             }
@@ -244,6 +284,49 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
             return false;
         }
         const uint32_t kt = st0 + (uint32_t)slot * STAGE, vt = kt + TILE;
+        const int valid = min(BS, L - t * BS);
+        if constexpr (FP8) {
+            // codes -> f16 (x scale) in place: lane (row lane & 15, half
+            // lane >> 4) reads its row's 64 codes, then the warp writes
+            uint8_t* tk = wst + (size_t)slot * STAGE;
+            const int r = lane & 15, hh = lane >> 4;
+#pragma unroll
+            for (int kv = 0; kv < 2; ++kv) {  // K tile, then V tile
+                uint4 c[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    c[j] = *reinterpret_cast<const uint4*>(tk + kv * TILE + BS * 128 + r * 128 +
+                                                           (((4 * hh + j) ^ (r & 7)) << 4));
+                __syncwarp();  // every lane holds its codes before any row is rewritten
+                const bool zero = kv == 1 && r >= valid;
+                const __half2 hs = __float2half2_rn(zero ? 0.f : wscl[(slot * 2 + kv) * BS + r]);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {  // codes 64 hh + 16 j .. +15 -> f16 pieces 8 hh + 2 j, +1
+                    const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+                    uint32_t h[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const __half2_raw lo =
+                            __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[u] & 0xffffu), __NV_E4M3);
+                        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[u] >> 16), __NV_E4M3);
+                        __half2 a, b;
+                        memcpy(&a, &lo, 4);
+                        memcpy(&b, &hi, 4);
+                        a = zero ? __float2half2_rn(0.f) : __hmul2(a, hs);
+                        b = zero ? __float2half2_rn(0.f) : __hmul2(b, hs);
+                        memcpy(&h[2 * u], &a, 4);
+                        memcpy(&h[2 * u + 1], &b, 4);
+                    }
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const int pj = 2 * j + half;  // piece within chunk hh
+                        *reinterpret_cast<uint4*>(tk + kv * TILE + hh * BS * 128 + r * 128 + ((pj ^ (r & 7)) << 4)) =
+                            make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+                    }
+                }
+                __syncwarp();
+            }
+        }
         float sc[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
@@ -252,9 +335,8 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
             uint32_t a0, a1, a2, a3;
             ldsm_x4(kt + swz(k_tok, kk * 16 + k_dof), a0, a1, a2, a3);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<T>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+            for (int nt = 0; nt < NT; ++nt) mma16816<MT>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
         }
-        const int valid = min(BS, L - t * BS);
         const bool ok0 = g < valid, ok1 = g + 8 < valid;
         uint32_t pb[NT][2];
 #pragma unroll
@@ -284,8 +366,8 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
                     acc[mt][nt][3] *= al1;
                 }
             }
-            pb[nt][0] = movm_t(pack2<T>(p0, p1));
-            pb[nt][1] = movm_t(pack2<T>(p2, p3));
+            pb[nt][0] = movm_t(pack2<MT>(p0, p1));
+            pb[nt][1] = movm_t(pack2<MT>(p2, p3));
         }
         // V rows past the context may hold anything: their operand lanes are zeroed
         uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
@@ -302,7 +384,7 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
             a2 &= m23;
             a3 &= m23;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma16816<T>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
+            for (int nt = 0; nt < NT; ++nt) mma16816<MT>(acc[mt][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
         }
         __syncwarp();
         if (ip < ntl) issue(ip++);
@@ -328,12 +410,58 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
     return true;
 }
 
-template <typename T, int HD>
+// Code cache (FP8 mode, head_dim 128): a slot's 128 rows of 128 E4M3 codes,
+// landed by TMA in the slot's second 128-byte chunk (row r at the offset of
+// f16 row r of that chunk, same swizzle), become f16 values code x scale in
+// both chunks, in place: each lane reads a row's 128 codes before writing
+// that row.  Rows at or past `keep` (no context) are written as zeros when
+// `zero_tail` (V: P is 0 there but a code may be NaN).
+__device__ __forceinline__ void dequant_tile_in_place(uint8_t* slot, const float* scl, int keep, bool zero_tail,
+                                                      int lane) {
+    constexpr int KCH = BK * 128;
+#pragma unroll 1
+    for (int r = lane; r < BK; r += 32) {
+        uint8_t* row1 = slot + KCH + r * 128;
+        uint4 c[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c[j] = *reinterpret_cast<const uint4*>(row1 + ((j ^ (r & 7)) << 4));
+        const bool zero = zero_tail && r >= keep;
+        const __half2 hs = __float2half2_rn(zero ? 0.f : scl[r]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // codes 16j .. 16j+15 -> f16 pieces 2j, 2j+1
+            const uint32_t w[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+            uint32_t h[8];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[t] & 0xffffu), __NV_E4M3);
+                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[t] >> 16), __NV_E4M3);
+                __half2 a, b;
+                memcpy(&a, &lo, 4);
+                memcpy(&b, &hi, 4);
+                a = zero ? __float2half2_rn(0.f) : __hmul2(a, hs);
+                b = zero ? __float2half2_rn(0.f) : __hmul2(b, hs);
+                memcpy(&h[2 * t], &a, 4);
+                memcpy(&h[2 * t + 1], &b, 4);
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int pc = 2 * j + half, ch = pc >> 3, pj = pc & 7;
+                *reinterpret_cast<uint4*>(slot + ch * KCH + r * 128 + ((pj ^ (r & 7)) << 4)) =
+                    make_uint4(h[4 * half], h[4 * half + 1], h[4 * half + 2], h[4 * half + 3]);
+            }
+        }
+    }
+}
+
+template <typename T, int HD, bool FP8>
 __global__ void __launch_bounds__(NTHREADS, 1)
     varlen_umma_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const UmParams p) {
     using Gm = UGeo<HD>;
-    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value;
+    static_assert(!FP8 || HD == 128, "the code cache is read at head_dim 128");
+    // the MMA operand type: the query type, or f16 over a code cache
+    constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value && !FP8;
+    using PT = typename std::conditional<FP8, __half, T>::type;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + Gm::BAR_OFF);
@@ -344,6 +472,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     uint64_t* v_empty = bars + 1 + 3 * R;
     uint64_t* tb = bars + 1 + 4 * R;  // per tile X: tb[3X] s_full, +1 p_full, +2 o_done
     uint64_t* v_zeroed = tb + 6;
+    uint64_t* k_conv = v_zeroed + 1;
+    uint64_t* v_conv = k_conv + R;
+    uint64_t* q_conv = v_conv + R;
+    float* scl_s = reinterpret_cast<float*>(base + Gm::SCL_OFF);  // [2][R][BK]: K, then V scales
     volatile uint32_t* taddr_slot = reinterpret_cast<volatile uint32_t*>(base + Gm::TADDR_OFF);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(base + Gm::TADDR_OFF + 4);
 
@@ -419,8 +551,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         constexpr int kStage = 2 * BS * HD * 2;
         uint8_t* wst = base + (size_t)warp * DR * kStage;
-        const bool ok = G <= 8 ? warp_decode<T, HD, 1>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, lane)
-                               : warp_decode<T, HD, 2>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, lane);
+        float* wscl = scl_s + warp * DR * 2 * BS;  // FP8: this warp's [DR][2][16] scales
+        const bool ok = G <= 8 ? warp_decode<T, HD, 1, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane)
+                               : warp_decode<T, HD, 2, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane);
         if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
         return;
     }
@@ -464,6 +597,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < Gm::NBAR; ++i) mbar_init(&bars[i], 1u);
         for (int x = 0; x < 2; ++x) mbar_init(&tb[3 * x + 1], 4u);  // p_full: one arrival per softmax warp
         mbar_init(v_zeroed, 4u);
+        mbar_init(q_conv, 8u);  // one arrival per softmax warp
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -521,8 +655,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int ngrp = min(nb_seq, nkt * BPT);
         const int32_t* table = p.block_tables + (int64_t)req * p.max_blocks;
         const int bsz = p.block_size;
-        const int per_group = Gm::CH * (bsz == 8 ? 2 : 1);
+        const int halves = bsz == 8 ? 2 : 1;
+        // lanes per 16-token group: a box per chunk (16-bit) or a code box
+        // and a scale copy (code cache), each per 8-row half with 8-token blocks
+        const int per_group = (FP8 ? 2 : Gm::CH) * halves;
+        const float* scales = is_v ? p.v_scales : p.k_scales;
+        uint64_t* convs = is_v ? v_conv : k_conv;
         bool run = true;
+        // code cache: a tile is turned into f16 while the next one loads
+        int pending = -1;
+        auto convert = [&](int t) -> bool {
+            const int sl = t % R;
+            if (!mbar_wait_ns(&fulls[sl], (uint32_t)(t / R) & 1u, WAIT_NS) || *abort_flag) return false;
+            dequant_tile_in_place(base + (is_v ? Gm::V_OFF : Gm::K_OFF) + sl * Gm::TILE,
+                                  scl_s + (is_v * R + sl) * BK, L - t * BK, is_v != 0, lane);
+            fence_proxy_async_smem();  // the MMAs read these values through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&convs[sl]);
+            return true;
+        };
         for (int w0 = 0; w0 < ngrp && run; w0 += kTableWindow) {
             const int wn = min(kTableWindow, ngrp - w0);
             for (int i = lane; i < wn; i += 32) {
@@ -552,20 +703,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 uint8_t* st = base + (is_v ? Gm::V_OFF : Gm::K_OFF) + slot * Gm::TILE;
                 if (lane == 0) {
                     fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(&fulls[slot], (uint32_t)(nvalid * Gm::CH * BS * 128));
+                    mbar_arrive_expect_tx(&fulls[slot], FP8 ? (uint32_t)(nvalid * BS * (128 + 4))
+                                                            : (uint32_t)(nvalid * Gm::CH * BS * 128));
                 }
                 __syncwarp();
                 // lane = (group j, chunk c[, 8-row half]); groups past the context are never read
                 if (lane < nvalid * per_group) {
                     const int j = lane / per_group, r = lane - j * per_group;
-                    const int c = bsz == 8 ? (r >> 1) : r, h8 = bsz == 8 ? (r & 1) : 0;
-                    const int e = kt * BPT + j - w0;
-                    const int row = h8 ? tbl_s[kTableWindow + e] : tbl_s[e];
-                    tma_load_3d(st + c * Gm::KCH + j * BS * 128 + h8 * 1024, tm, &fulls[slot], 0,
-                                kvh * Gm::CH + c, row, pol);
+                    if constexpr (FP8) {
+                        // r < halves: the group's code rows (into the slot's second
+                        // chunk, where f16 row j*16+.. will be); else its scales
+                        const int h8 = r % halves;
+                        const int e = kt * BPT + j - w0;
+                        const int row = h8 ? tbl_s[kTableWindow + e] : tbl_s[e];
+                        if (r < halves) {
+                            tma_load_3d(st + Gm::KCH + j * BS * 128 + h8 * 1024, tm, &fulls[slot], 0, kvh, row, pol);
+                        } else {
+                            const int64_t si = (int64_t)(row / bsz) * Hkv * bsz + (int64_t)kvh * bsz + row % bsz;
+                            bulk_g2s(scl_s + (is_v * R + slot) * BK + j * BS + h8 * 8, scales + si,
+                                     (uint32_t)(BS * 4 / halves), &fulls[slot]);
+                        }
+                    } else {
+                        const int c = bsz == 8 ? (r >> 1) : r, h8 = bsz == 8 ? (r & 1) : 0;
+                        const int e = kt * BPT + j - w0;
+                        const int row = h8 ? tbl_s[kTableWindow + e] : tbl_s[e];
+                        tma_load_3d(st + c * Gm::KCH + j * BS * 128 + h8 * 1024, tm, &fulls[slot], 0,
+                                    kvh * Gm::CH + c, row, pol);
+                    }
+                }
+                if constexpr (FP8) {
+                    if (pending >= 0 && !convert(pending)) {
+                        if (lane == 0) fail();
+                        run = false;
+                        break;
+                    }
+                    pending = kt;
                 }
             }
             __syncwarp();
+        }
+        if constexpr (FP8) {
+            if (run && pending >= 0 && !convert(pending) && lane == 0) fail();
         }
     } else if (warp == W_MMA) {
         // ---------------- MMA issuer, in a fixed staggered order:
@@ -604,7 +782,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 if (j == nktx[x] - 1) umma_commit(&tb[3 * x + 2]);
                 if (x == 1 || j >= nkb) umma_commit(&v_empty[j % R]);  // last reader of V(j)
             };
-            bool ok = mbar_wait_ns(q_full, 0, WAIT_NS) && mbar_wait_ns(&k_full[0], 0, WAIT_NS);
+            // operands ready: landed (16-bit cache) or turned into f16 (code cache)
+            uint64_t* q_ready = FP8 ? q_conv : q_full;
+            uint64_t* k_ready = FP8 ? k_conv : k_full;
+            uint64_t* v_ready = FP8 ? v_conv : v_full;
+            bool ok = mbar_wait_ns(q_ready, 0, WAIT_NS) && mbar_wait_ns(&k_ready[0], 0, WAIT_NS);
             if (ok) {
                 tc_fence_after();
                 issue_s(0, 0);
@@ -612,13 +794,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             for (int k = 0; ok && k < nka; ++k) {
                 ok = !*abort_flag && mbar_wait_ns(&tb[1], (uint32_t)k & 1u, WAIT_NS) &&
-                     mbar_wait_ns(&v_full[k % R], (uint32_t)(k / R) & 1u, WAIT_NS);
+                     mbar_wait_ns(&v_ready[k % R], (uint32_t)(k / R) & 1u, WAIT_NS);
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(0, k);
                 const bool more = k + 1 < nka;
                 if (more) {
-                    ok = mbar_wait_ns(&k_full[(k + 1) % R], (uint32_t)((k + 1) / R) & 1u, WAIT_NS);
+                    ok = mbar_wait_ns(&k_ready[(k + 1) % R], (uint32_t)((k + 1) / R) & 1u, WAIT_NS);
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(0, k + 1);
@@ -649,6 +831,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float sl = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
+        if constexpr (FP8) {
+            // the MMAs run in f16 over a code cache: bf16 queries are turned
+            // into f16 in place (both Q tiles, 16-byte pieces over the 256
+            // softmax threads); f16 queries are used as they land
+            if (!mbar_wait_ns(q_full, 0, WAIT_NS)) {
+                ok = false;
+            } else if (std::is_same<T, __nv_bfloat16>::value) {
+                for (int e = threadIdx.x; e < 2 * Gm::QT / 16; e += 256) {
+                    uint4* pc = reinterpret_cast<uint4*>(base + Gm::Q_OFF) + e;
+                    uint4 v = *pc;
+                    uint32_t* w = &v.x;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const float lo = __uint_as_float(w[t] << 16), hi = __uint_as_float(w[t] & 0xffff0000u);
+                        w[t] = pack2<__half>(lo, hi);
+                    }
+                    *pc = v;
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_conv);
+        }
         for (int kt = 0; kt < my_nkt; ++kt) {
             // S_X(kt) complete; its commit also covers P V_X(kt-1), so O and
             // the P columns are free once this wait returns
@@ -695,7 +900,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
                             const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
                             sum += e0 + e1;
-                            pk[32 * q64 + j] = __uint_as_float(pack2<T>(e0, e1));
+                            pk[32 * q64 + j] = __uint_as_float(pack2<PT>(e0, e1));
                         }
                     } else {
                         const int nv = vis - 64 * q64;  // columns j <= nv are visible
@@ -706,7 +911,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                             const float e0 = v0 ? fast_exp2(fmaf(a[2 * j], sl, neg_m)) : 0.f;
                             const float e1 = v1 ? fast_exp2(fmaf(a[2 * j + 1], sl, neg_m)) : 0.f;
                             sum += e0 + e1;
-                            pk[32 * q64 + j] = __uint_as_float(pack2<T>(e0, e1));
+                            pk[32 * q64 + j] = __uint_as_float(pack2<PT>(e0, e1));
                         }
                     }
                 }
@@ -768,7 +973,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // Keys at or past L hold no context: their V rows of the tile that
             // holds the context end are zeroed once, by tile A's warps (tile A
             // reads every key tile tile B reads); tile B waits for that.
-            if (kt == klast && L - kbase < BK) {
+            if (!FP8 && kt == klast && L - kbase < BK) {  // (a code cache's converter zeroes them)
                 if (x == 0) {
                     if (!mbar_wait_ns(&v_full[kt % R], (uint32_t)(kt / R) & 1u, WAIT_NS)) {
                         ok = false;
@@ -905,6 +1110,7 @@ PFN_cuTensorMapEncodeTiled_v12000 um_encode_fn() {
     return fn;
 }
 
+// dtype: 1 bf16, 2 f16, 3 E4M3 codes (bytes)
 bool um_encode(CUtensorMap* m, const void* base, int dtype, const cuuint64_t dims[3], const cuuint64_t strides[2],
                const cuuint32_t box[3], std::string* err) {
     auto fn = um_encode_fn();
@@ -913,7 +1119,9 @@ bool um_encode(CUtensorMap* m, const void* base, int dtype, const cuuint64_t dim
         return false;
     }
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(m, dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+    const CUtensorMapDataType ty = dtype == 3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : (dtype == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16);
+    CUresult r = fn(m, ty, 3,
                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
@@ -932,7 +1140,7 @@ size_t um_plan_bytes(int64_t total_q, int32_t num_seqs, int TT) {
            um_round((size_t)num_seqs * sizeof(int32_t));
 }
 
-template <typename T, int HD>
+template <typename T, int HD, bool FP8 = false>
 cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, std::string* err,
                       cudaStream_t stream) {
     const int G = a.num_heads / a.num_kv_heads;
@@ -946,7 +1154,15 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TT};
         if (!um_encode(&tmQ, a.q, a.dtype, dims, strides, box, err)) return cudaErrorInvalidValue;
     }
-    {
+    if (FP8) {
+        // codes: one 128-byte row per (token, KV head); one box = 16 (or 8) rows
+        cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)a.num_kv_heads, (cuuint64_t)num_blocks * a.block_size};
+        cuuint64_t strides[2] = {(cuuint64_t)HD, (cuuint64_t)a.num_kv_heads * HD};
+        cuuint32_t box[3] = {(cuuint32_t)HD, 1, (cuuint32_t)(a.block_size == 8 ? 8 : BS)};
+        if (!um_encode(&tmK, a.k_cache, 3, dims, strides, box, err) ||
+            !um_encode(&tmV, a.v_cache, 3, dims, strides, box, err))
+            return cudaErrorInvalidValue;
+    } else {
         const int ch = HD / 64;
         cuuint64_t dims[3] = {64, (cuuint64_t)a.num_kv_heads * ch, (cuuint64_t)num_blocks * a.block_size};
         cuuint64_t strides[2] = {128, (cuuint64_t)a.num_kv_heads * HD * 2};
@@ -972,6 +1188,8 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
     p.plan = nullptr;
     p.items = nullptr;
     p.dec_req = nullptr;
+    p.k_scales = a.k_scales;
+    p.v_scales = a.v_scales;
     // prefill tile pairs (at most total_q / 2T + one per request), then
     // decode CTAs of DG requests; CTAs past the work the kernel finds return
     const int64_t pairs = (int64_t)a.total_q / (2 * TT) + a.num_seqs;
@@ -979,10 +1197,11 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         *err = "too many query rows for one varlen launch";
         return cudaErrorInvalidValue;
     }
-    const int64_t dgroups = G <= kMaxDecodeGroupG ? (a.num_seqs + DG - 1) / DG : 0;
+    const bool dec_route = G <= kMaxDecodeGroupG;
+    const int64_t dgroups = dec_route ? (a.num_seqs + DG - 1) / DG : 0;
     const size_t smem = um_smem_bytes<HD>(workspace ? 0 : a.num_seqs);
-    cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD, FP8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1001,7 +1220,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         pc.attrs = attr;
         pc.numAttrs = 1;
         e = cudaLaunchKernelEx(&pc, varlen_plan_kernel, a.cu_seqlens_q, a.seq_lens, a.num_seqs, TT, a.causal,
-                               G <= kMaxDecodeGroupG ? 1 : 0, nbuckets, const_cast<int32_t*>(p.plan),
+                               dec_route ? 1 : 0, nbuckets, const_cast<int32_t*>(p.plan),
                                const_cast<int2*>(p.items), const_cast<int32_t*>(p.dec_req));
         if (e != cudaSuccess) return e;
     }
@@ -1013,13 +1232,13 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, varlen_umma_kernel<T, HD>, tmQ, tmK, tmV, p);
+    return cudaLaunchKernelEx(&cfg, varlen_umma_kernel<T, HD, FP8>, tmQ, tmK, tmV, p);
 }
 
 }  // namespace
 
-bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group) {
-    return (dtype == 1 || dtype == 2) && (head_dim == 64 || head_dim == 128) &&
+bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8) {
+    return (dtype == 1 || dtype == 2) && (kv_fp8 ? head_dim == 128 : (head_dim == 64 || head_dim == 128)) &&
            (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) && group >= 1 &&
            group <= TM;
 }
@@ -1033,6 +1252,9 @@ cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, void* work
                                cudaStream_t stream) {
     if (a.total_q == 0 || a.num_seqs == 0) return cudaSuccess;
     auto one = [&](const AttnArgs& c, void* ws) -> cudaError_t {
+        if (a.kv_fp8)  // head_dim 128 only
+            return a.dtype == 1 ? um_launch<__nv_bfloat16, 128, true>(c, num_blocks, ws, err, stream)
+                                : um_launch<__half, 128, true>(c, num_blocks, ws, err, stream);
         if (a.dtype == 1)
             return a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(c, num_blocks, ws, err, stream)
                                     : um_launch<__nv_bfloat16, 128>(c, num_blocks, ws, err, stream);

@@ -460,15 +460,37 @@ def test_fp8_decode_more_sequences_than_one_launch_takes(pa):
 
 # ---------------------------------------------------------------- varlen over the quantized cache
 
-def run_varlen_fp8(pa, w, pools, causal=None):
+def run_varlen_fp8(pa, w, pools, causal=None, kernel=0, planned=False):
+    """kernel: 0 automatic, 1 CUDA-core, 2 tcgen05; planned: pass the workspace
+    that lets the tcgen05 kernel run its work longest first."""
     kc, vc, ks, vs, bt = pools
     out = torch.full(tuple(w.q.shape), float("nan"), dtype=W.TORCH_DTYPES[w.dtype], device=DEV)
     mq, mc = int(w.query_lens.max()), int(w.seq_lens.max())
-    pa.pa_varlen_fp8(out, w.q.to(DEV), kc, vc, ks, vs, bt, torch.from_numpy(w.seq_lens).to(DEV),
-                     torch.from_numpy(w.query_start_loc).to(DEV), mq, mc, w.scale,
-                     causal=w.causal if causal is None else causal)
-    torch.cuda.synchronize()
+    pa.pa_set_option(pa.PA_OPT_VARLEN_KERNEL, kernel)
+    try:
+        ws = None
+        if planned:
+            n = pa.pa_varlen_fp8_workspace_size(w.num_seqs, int(w.query_lens.sum()), mq, w.num_heads, w.num_kv_heads,
+                                                w.head_dim, w.block_size, mc, W.TORCH_DTYPES[w.dtype])
+            ws = torch.empty(max(n, 16), dtype=torch.uint8, device=DEV)
+        pa.pa_varlen_fp8(out, w.q.to(DEV), kc, vc, ks, vs, bt, torch.from_numpy(w.seq_lens).to(DEV),
+                         torch.from_numpy(w.query_start_loc).to(DEV), mq, mc, w.scale,
+                         causal=w.causal if causal is None else causal, workspace=ws)
+        torch.cuda.synchronize()
+        pa.pa_device_status(clear=True)  # raises if a bounded wait ran out
+    finally:
+        pa.pa_set_option(pa.PA_OPT_VARLEN_KERNEL, 0)
     return out
+
+
+def varlen_fp8_kernels(w):
+    """(kernel, planned) pairs that apply to w: the CUDA-core kernel always;
+    the tcgen05 kernel (with and without the plan) for bf16/f16 queries,
+    head_dim 128 and block size 8 or a multiple of 16."""
+    runs = [(1, False)]
+    if w.dtype in ("bf16", "f16") and w.head_dim == 128 and (w.block_size == 8 or w.block_size % 16 == 0):
+        runs += [(2, False), (2, True)]
+    return runs
 
 
 def oracle_varlen_fp8(w, opools, causal):
@@ -486,9 +508,11 @@ def test_varlen_fp8_handbook_layout(pa, dtype):
     opools = oracle_fp8_caches(w)
     assert_pools_equal(pools[:4], opools)
     for causal in (True, False):
-        err = compare(w, run_varlen_fp8(pa, w, pools, causal=causal), oracle_varlen_fp8(w, opools, causal))
-        if dtype == "f32":
-            assert err < 1e-5
+        exact = oracle_varlen_fp8(w, opools, causal)
+        for kernel, planned in varlen_fp8_kernels(w):
+            err = compare(w, run_varlen_fp8(pa, w, pools, causal=causal, kernel=kernel, planned=planned), exact)
+            if dtype == "f32":
+                assert err < 1e-5
 
 
 def test_varlen_fp8_mixed_step_with_cow_full(pa):
@@ -501,7 +525,9 @@ def test_varlen_fp8_mixed_step_with_cow_full(pa):
     pools = device_fp8_caches(w, DEV)
     opools = oracle_fp8_caches(w)
     assert_pools_equal(pools[:4], opools)
-    compare(w, run_varlen_fp8(pa, w, pools), oracle_varlen_fp8(w, opools, True))
+    exact = oracle_varlen_fp8(w, opools, True)
+    for kernel, planned in varlen_fp8_kernels(w):
+        compare(w, run_varlen_fp8(pa, w, pools, kernel=kernel, planned=planned), exact)
 
 
 VARLEN_FP8_CASES = []
@@ -526,5 +552,49 @@ def test_random_varlen_fp8(pa, dt, bs, hd, g, hkv, lens, qlens, seed):
     opools = oracle_fp8_caches(w)
     assert_pools_equal(pools[:4], opools)
     for causal in (True, False):
-        compare(w, run_varlen_fp8(pa, w, pools, causal=causal), oracle_varlen_fp8(w, opools, causal))
+        exact = oracle_varlen_fp8(w, opools, causal)
+        for kernel, planned in varlen_fp8_kernels(w):
+            compare(w, run_varlen_fp8(pa, w, pools, causal=causal, kernel=kernel, planned=planned), exact)
+
+
+TC_VARLEN_FP8_CASES = []
+_r5 = np.random.default_rng(919)
+for _i in range(8):
+    _bs = int(_r5.choice([8, 16, 32, 64]))
+    _g = int(_r5.choice([1, 2, 3, 6, 8, 12]))
+    _hkv = int(_r5.choice([1, 2, 4]))
+    _dt = str(_r5.choice(["bf16", "f16"]))
+    _S = int(_r5.integers(1, 7))
+    _q = _r5.integers(1, 300, _S)
+    _q[_r5.random(_S) < 0.4] = 1  # decode rows mixed in
+    _cached = _r5.integers(0, 400, _S)
+    TC_VARLEN_FP8_CASES.append((_dt, _bs, _g, _hkv, (_cached + _q).tolist(), _q.tolist(), 970 + _i))
+
+
+@pytest.mark.parametrize("dt,bs,g,hkv,lens,qlens,seed", TC_VARLEN_FP8_CASES)
+def test_random_varlen_fp8_tensor_core(pa, dt, bs, g, hkv, lens, qlens, seed):
+    """head_dim 128 shapes the tcgen05 kernel takes over a code cache: several
+    128-key tiles, both query tiles of a pair, partial last tiles."""
+    w = W.varlen_workload("vfp8tc", dt, bs, g * hkv, hkv, 128, lens, qlens, seed=seed)
+    pools = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    for causal in (True, False):
+        exact = oracle_varlen_fp8(w, opools, causal)
+        for kernel, planned in varlen_fp8_kernels(w):
+            compare(w, run_varlen_fp8(pa, w, pools, causal=causal, kernel=kernel, planned=planned), exact)
+
+
+def test_varlen_fp8_permutation_bit_identical(pa):
+    w = W.varlen_workload("perm_vfp8", "bf16", 16, 12, 2, 128, [300, 81, 17, 1000], [1, 81, 5, 130], seed=3)
+    kc, vc, ks, vs, bt = device_fp8_caches(w, DEV)
+    base = run_varlen_fp8(pa, w, (kc, vc, ks, vs, bt), kernel=2, planned=True)
+    perm = torch.from_numpy(np.random.default_rng(5).permutation(w.num_blocks)).to(DEV)
+    pools2 = []
+    for t in (kc, vc, ks, vs):
+        t2 = torch.empty_like(t)
+        t2[perm] = t
+        pools2.append(t2)
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_varlen_fp8(pa, w, (*pools2, bt2), kernel=2, planned=True)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
 
