@@ -356,13 +356,18 @@ PA_API pa_status pa_varlen(void* out, const void* q, const void* k_cache, const 
  * and value element its code's value times its (token, KV head) row's scale
  * (the quantized cache of "KV cache：容量推导、分页与回收", §输入放得下，输出
  * 还要留空间).  Prefill chunks and decode rows mix as in pa_varlen; causal
- * as there.  Runs on the CUDA-core kernel (fp32 arithmetic, any head_dim up
- * to 256 and any block size), which reads each code row once for up to 8
- * query heads of its KV head.
+ * as there.  bf16/f16 queries with head_dim 128 and block_size 8 or a
+ * multiple of 16 up to 256 run on the tcgen05 kernel: code tiles are turned
+ * into f16 code x scale in shared memory and the MMAs run in f16 (q, and
+ * the keys and values, must lie inside the f16 range); the rest runs on the
+ * CUDA-core kernel (fp32 arithmetic, any head_dim up to 256 and any block
+ * size).
  *   out, q:             device [total_q, num_heads, head_dim] of dtype (PA_F32/BF16/F16)
  *   k_codes, v_codes:   device uint8 [num_blocks, block_size, num_kv_heads, head_dim]
  *   k_scales, v_scales: device fp32 [num_blocks, num_kv_heads, block_size], 16-byte aligned
- *   workspace:          pa_varlen_fp8_workspace_size(...) bytes (0 today: may be NULL)
+ *   workspace:          optional, pa_varlen_fp8_workspace_size(...) bytes: as
+ *                       for pa_varlen, the tcgen05 kernel then runs its work
+ *                       longest first
  * The other arguments and the error behaviour are pa_varlen's.
  */
 PA_API size_t pa_varlen_fp8_workspace_size(int32_t num_seqs, int32_t total_q, int32_t max_q, int32_t num_heads,
