@@ -85,9 +85,18 @@ def measured_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
 
 
+def traffic_key(workload, fp8, block_size):
+    """Key of a workload's record in the committed ncu traffic table: the
+    workload, then "_fp8" over a quantized cache, then "_bs<n>" for a block
+    size other than 16."""
+    return workload + ("_fp8" if fp8 else "") + ("" if block_size == 16 else "_bs%d" % block_size)
+
+
 def traffic_record(workload, kernel_file):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary of this workload, if it was taken on the current kernel source."""
+    if workload is None:
+        return None
     src = os.path.join(ROOT, "paged_kv_cache_116_gb300", "csrc", kernel_file)
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
@@ -818,6 +827,8 @@ def main():
                       "step i's copies overlap its neighbours' kernels; %d steps per CUDA graph replay" % GS}
 
     peaks, kind = measured_peaks()
+    # the committed DRAM counters hold for one GPU's whole batch only
+    tkey = traffic_key(args.workload, fp8, bs) if world == 1 else None
     if decode:
         nblk = int(sum((L + bs - 1) // bs for L in w.seq_lens.tolist()))
         alg = kv_bytes + 2 * S * hq * hd * w.elt + nblk * 4 + S * 4
@@ -827,7 +838,7 @@ def main():
                     "<FP8>" if fp8 else "", call) if tc_decode else "attn_simt_kernel (%s, CUDA-core path)" % call),
                 "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "peak_kind": kind + " hbm_gbs", "algorithmic_bytes": alg,
-                "traffic": traffic_record(args.workload + ("_fp8" if fp8 else ""), "pa_decode_tc.cu"),
+                "traffic": traffic_record(tkey, "pa_decode_tc.cu") if tc_decode else None,
                 "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
     elif fp8 and w.dtype in ("bf16", "f16") and hd == 128 and (bs == 8 or (bs % 16 == 0 and bs <= 256)):
         # the mixed step over a code cache on the tensor cores (codes turned
@@ -838,7 +849,8 @@ def main():
         roof = {"bound": "tensor", "kernel": "varlen_umma_kernel<FP8> (pa_varlen_fp8, tcgen05)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_kind": kind + " bf16_tflops (burst; f16 runs at the same rate)", "algorithmic_flops": fl,
-                "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9, "traffic": None,
+                "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
+                "traffic": traffic_record(tkey, "pa_varlen_umma.cu"),
                 "kernel_us": kern_ms * 1e3, "kernel_us_median_of_51": kern_med_us}
     elif fp8:
         # the mixed step over a code cache on the CUDA-core kernel: its
@@ -858,7 +870,7 @@ def main():
                 "unit": "TFLOP/s", "frac": achieved / peak, "peak_kind": kind + " bf16_tflops (burst)",
                 "algorithmic_flops": fl, "kv_bytes": kv_bytes, "kv_GBps_in_kernel": kv_bytes / (kern_ms / 1e3) / 1e9,
                 "unique_kv_bytes": unique_kv_bytes(w), "parts": parts,
-                "traffic": traffic_record(args.workload, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3,
+                "traffic": traffic_record(tkey, "pa_varlen_umma.cu"), "kernel_us": kern_ms * 1e3,
                 "kernel_us_median_of_51": kern_med_us}
 
     if rank == 0:
