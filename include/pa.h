@@ -403,8 +403,8 @@ PA_API pa_status pa_varlen_fp8(void* out, const void* q, const void* k_codes, co
  * Check mode (PA_OPT_CHECK_MODE) applies as for pa_decode: lengths and
  * tables are copied to the host and validated (PA_ERR_INDEX) before launch.
  * The array need not start at zero, and no call reads what an earlier one
- * left in it (each launch writes every split record and unit descriptor its
- * merge reads), so it never needs clearing -- not even after a bounded wait
+ * left in it (each launch writes every split record its merge reads, and
+ * the merge finds them from the lengths alone), so it never needs clearing -- not even after a bounded wait
  * ran out (PA_ERR_TIMEOUT).
  */
 PA_API pa_status pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,

@@ -19,8 +19,8 @@
 // Every call on a device shares the array, so two calls whose kernels
 // overlap on the GPU (different streams without ordering) race on it.
 // Nothing in it has to start at zero, and nothing a call leaves behind is
-// read by a later one: each launch writes every split record and unit
-// descriptor its merge reads before the merge runs.
+// read by a later one: each launch writes every split record its merge
+// reads before the merge runs, and the merge finds them from the lengths.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>

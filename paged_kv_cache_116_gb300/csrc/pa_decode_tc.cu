@@ -18,8 +18,9 @@
 //    programmatic dependent, merges them by their log-sum-exp in a fixed
 //    order once the grid has completed ("aiqz.cc PagedAttention", §工程实现
 //    要点: blocks computed apart and merged by the online-softmax rule).  The
-//    workspace never needs clearing.  The cut depends only on the lengths,
-//    never on physical block ids.
+//    cut depends only on the lengths, never on physical block ids, so the
+//    merge finds every piece from the lengths alone; the workspace holds
+//    nothing but the records and never needs clearing.
 //  * Each warp runs its own R-deep ring of shared-memory stages (one or two
 //    16-token tiles each).  Several lanes issue, in one instruction, the TMA
 //    loads (cp.async.bulk.tensor, 128-byte swizzle) of a stage's K and V
@@ -91,13 +92,10 @@ struct TcParams {
     int32_t num_kv_heads;
     int32_t group;
     float scale_log2;
-    // split merge: the number of tiles W (written by block 0), one
-    // descriptor per unit {first warp, last warp, the first warp's record
-    // slot or -1 when the unit needs no merge, 0}, and two records of
-    // group * (HD + 4) floats per warp
-    long long* ws_tiles;
-    int4* ws_desc;  // [num_seqs * num_kv_heads]
-    float* ws_part; // [total_warps][2]
+    // split merge: two records of group * (HD + 4) floats per warp (slot 0:
+    // the warp's first piece, 1: its last), each head's unnormalised o then
+    // its m and l
+    float* ws_part;  // [total_warps][2]
     // append mode (k_new != nullptr): each sequence's token at position L-1
     // arrives in k_new / v_new [num_seqs, Hkv, HD]; it is written to the pool
     // and attended from these rows, not from the pool
@@ -242,13 +240,11 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
     tile_prefix(p.context_lens, S, prefix, lens);
 
     const int64_t W = (int64_t)prefix[S] * Hkv;
-    if (blockIdx.x == 0 && threadIdx.x == 0) *p.ws_tiles = W;
     // sequences with no context get a zero row (and nothing to merge)
     for (int s = blockIdx.x; s < S; s += gridDim.x) {
         if (prefix[s + 1] == prefix[s]) {
             T* o = static_cast<T*>(p.out) + (int64_t)s * p.num_heads * HD;
             for (int e = threadIdx.x; e < p.num_heads * HD; e += blockDim.x) o[e] = Elt<T>::from_f(0.f);
-            for (int h = threadIdx.x; h < Hkv; h += blockDim.x) p.ws_desc[(int64_t)s * Hkv + h] = make_int4(0, 0, -1, 0);
         }
     }
 
@@ -502,9 +498,7 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 lt[nt][e] = l;
             }
         const bool complete = (seg_b0 == 0 && bend == nb);
-        int* desc = reinterpret_cast<int*>(p.ws_desc + (int64_t)cs * Hkv + ch);
         if (complete) {
-            if (lane == 0) *reinterpret_cast<int4*>(desc) = make_int4((int)gw, (int)gw, -1, 0);
             T* out = static_cast<T*>(p.out) + ((int64_t)cs * p.num_heads + (int64_t)ch * G) * HD;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -525,13 +519,6 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
             // this warp's record (slot 0: the warp's first piece, 1: its
             // last); decode_merge_kernel combines the pieces after this grid
             const int slot = first_seg ? 0 : 1;
-            if (lane == 0) {
-                if (seg_b0 == 0) {  // the unit's first piece: this warp is its first
-                    desc[0] = (int)gw;
-                    desc[2] = slot;
-                }
-                if (bend == nb) desc[1] = (int)gw;  // its last piece
-            }
             float* rec = p.ws_part + (gw * 2 + slot) * (int64_t)G * (HD + 4);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
@@ -950,52 +937,61 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 
 // The split merge ("aiqz.cc PagedAttention", §工程实现要点: blocks computed
 // apart, merged by the online-softmax rule).  Launched right after
-// decode_tc_kernel as its programmatic dependent: it waits for that grid
-// to complete, then half a warp per (sequence, KV head, query head of the
-// group) whose unit was cut between warps combines the unit's partial
-// records (m, l, unnormalised o) by their log-sum-exp, in warp order.  The
-// records are read in batches of up to four whose loads all go out
-// together (one memory round trip per batch, not one per record), each
-// batch folded into the running state by the same rule.  The unit's
-// descriptor names its first and last warp and the first warp's record
-// slot; every later warp holds the unit as its first piece (slot 0).  Warps
-// with empty ranges (only when the batch has fewer tiles than the decode
-// grid has warps) hold no record.
+// decode_tc_kernel as its programmatic dependent; half a warp per (sequence,
+// KV head, query head of the group).  Before it waits for the decode grid it
+// finds its unit's pieces from the lengths alone, with the decode's own cut
+// (warp w owns flat tiles [w W / TW, (w+1) W / TW)): the unit's first warp
+// holds it as its first piece (record slot 0) when the unit starts where
+// that warp's range starts, else as its last (slot 1); every later warp
+// holds it as its first piece.  A unit inside one warp's range was written
+// whole by that warp and is skipped.  The lengths were complete before the
+// decode grid started (it waited for them), so reading them early is safe.
+// After the wait the records are read in batches of up to B whose loads all
+// go out together (one memory round trip per batch), each batch folded into
+// the running state by the log-sum-exp rule, in warp order.  Warps with
+// empty ranges (only when the batch has fewer tiles than the decode grid
+// has warps) hold no record.
 template <typename T, int HD>
 __global__ void __launch_bounds__(256) decode_merge_kernel(const TcParams p, const int64_t TW) {
-    constexpr int E = HD / 16;  // output elements per lane
-    constexpr int B = 4;        // records per batch
-    pdl_wait_primary();
-    const int G = p.group;
+    constexpr int E = HD / 16;             // output elements per lane
+    constexpr int B = HD <= 128 ? 8 : 4;   // records per batch
+    extern __shared__ int32_t mprefix[];   // [num_seqs + 1]
+    const int S = p.num_seqs, Hkv = p.num_kv_heads, G = p.group;
+    tile_prefix(p.context_lens, S, mprefix, nullptr);
     const int64_t item = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4);
-    if (item >= (int64_t)p.num_seqs * p.num_kv_heads * G) return;
+    if (item >= (int64_t)S * Hkv * G) return;
     const int hl = threadIdx.x & 15;  // lane within the half warp
     const int j = (int)(item % G);
     const int64_t u = item / G;
-    const int4 d = __ldcg(p.ws_desc + u);
-    const int64_t W = __ldcg(p.ws_tiles);
-    if (d.z < 0) return;  // one warp held the unit whole and wrote the output
-    // every descriptor of a unit with context is rewritten by each launch;
-    // one outside this grid can only be a leftover after a warp gave up on
-    // a bounded wait (reported as PA_ERR_TIMEOUT), so it is not followed
-    if (d.x < 0 || d.x > d.y || (int64_t)d.y >= TW || d.z > 1) return;
+    const int s = (int)(u / Hkv), h = (int)(u - (int64_t)s * Hkv);
+    const int nb = mprefix[s + 1] - mprefix[s];
+    if (nb == 0) return;  // no context: the decode wrote the zero row
+    const int64_t W = (int64_t)mprefix[S] * Hkv;
+    const int64_t u0 = (int64_t)mprefix[s] * Hkv + (int64_t)h * nb, u1 = u0 + nb;
+    // the warp owning flat tile f: the last w with w W / TW <= f
+    auto owner = [&](int64_t f) -> int64_t { return ((f + 1) * TW + W - 1) / W - 1; };
+    const int64_t wf = owner(u0), wl = owner(u1 - 1);
+    if (wf == wl) return;  // held whole by one warp
+    const int slot0 = u0 == wf * W / TW ? 0 : 1;
     const float* rec0 = p.ws_part + (int64_t)j * (HD + 4) + hl * E;
     const int64_t rstride = (int64_t)G * (HD + 4);
+
+    pdl_wait_primary();  // the records are the decode grid's output
     float M = -INFINITY, L = 0.f, o[E];
 #pragma unroll
     for (int t = 0; t < E; ++t) o[t] = 0.f;
-    for (int64_t w0 = d.x; w0 <= d.y; w0 += B) {
+    for (int64_t w0 = wf; w0 <= wl; w0 += B) {
         float m[B], l[B];
         float4 a[B][E / 4];
 #pragma unroll
         for (int b = 0; b < B; ++b) {
             const int64_t w = w0 + b;
             // an absent record (past the unit, or an empty range) weighs nothing
-            const bool ok = w <= d.y && !(W < TW && w * W / TW == (w + 1) * W / TW);
+            const bool ok = w <= wl && !(W < TW && w * W / TW == (w + 1) * W / TW);
             m[b] = -INFINITY;
             l[b] = 0.f;
             if (ok) {
-                const float* r = rec0 + (w * 2 + (w == d.x ? d.z : 0)) * rstride;
+                const float* r = rec0 + (w * 2 + (w == wf ? slot0 : 0)) * rstride;
                 m[b] = __ldcg(r - hl * E + HD);
                 l[b] = __ldcg(r - hl * E + HD + 1);
 #pragma unroll
@@ -1027,7 +1023,6 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(const TcParams p, con
         M = Mn;
     }
     const float inv = 1.f / L;
-    const int s = (int)(u / p.num_kv_heads), h = (int)(u - (int64_t)s * p.num_kv_heads);
     T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + (int64_t)h * G + j) * HD + hl * E;
 #pragma unroll
     for (int t = 0; t < E; t += 4) {  // 4 outputs (8 bytes) per store
@@ -1086,13 +1081,6 @@ bool make_kv_map(CUtensorMap* m, const void* cache, int dtype, bool fp8, int num
     return true;
 }
 
-// Bytes of the workspace's unit descriptors (after a 256-byte header, ahead
-// of the split records).
-size_t desc_ws_bytes(int32_t num_seqs, int32_t num_kv_heads) {
-    const int s = num_seqs < kDecodeMaxSeqsPerLaunch ? num_seqs : kDecodeMaxSeqsPerLaunch;
-    return ((size_t)s * num_kv_heads * sizeof(int4) + 255) & ~(size_t)255;
-}
-
 template <typename T, int HD, int NT, bool FP8, bool PAIR = false, bool GATHER = false>
 const void* kernel_ptr() {
     return reinterpret_cast<const void*>(&decode_tc_kernel<T, HD, NT, FP8, PAIR, GATHER>);
@@ -1139,10 +1127,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     p.num_kv_heads = a.num_kv_heads;
     p.group = a.num_heads / a.num_kv_heads;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    p.ws_tiles = static_cast<long long*>(workspace);
-    p.ws_desc = reinterpret_cast<int4*>(static_cast<uint8_t*>(workspace) + 256);
-    p.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256 +
-                                         desc_ws_bytes(a.num_seqs, a.num_kv_heads));
+    p.ws_part = static_cast<float*>(workspace);
     p.k_new = a.k_new;
     p.v_new = a.v_new;
     p.k_pool = const_cast<void*>(a.k_cache);
@@ -1176,7 +1161,7 @@ cudaError_t launch_typed(const AttnArgs& a, int32_t num_blocks, int grid, void* 
     cudaLaunchConfig_t mcfg = cfg;
     mcfg.gridDim = dim3((unsigned)((items + 15) / 16));
     mcfg.blockDim = dim3(256);
-    mcfg.dynamicSmemBytes = 0;
+    mcfg.dynamicSmemBytes = (size_t)(a.num_seqs + 1) * sizeof(int32_t);
     return cudaLaunchKernelEx(&mcfg, decode_merge_kernel<T, HD>, p, tw);
 }
 
@@ -1263,8 +1248,7 @@ int decode_tc_warps_per_cta(int32_t head_dim, bool kv_fp8) {
 size_t decode_tc_workspace(int32_t num_seqs, int32_t num_kv_heads, int32_t group, int32_t head_dim, int grid_ctas,
                            bool kv_fp8) {
     const int nw = decode_tc_warps_per_cta(head_dim, kv_fp8);
-    return 256 + desc_ws_bytes(num_seqs, num_kv_heads) +
-           (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
+    return (size_t)grid_ctas * nw * 2 * group * (head_dim + 4) * sizeof(float);
 }
 
 cudaError_t launch_decode_tc(const AttnArgs& a, int32_t num_blocks, int grid_ctas, void* workspace,
