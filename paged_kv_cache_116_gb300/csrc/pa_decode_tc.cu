@@ -149,11 +149,6 @@ constexpr size_t smem_bytes(int num_seqs) {
            (size_t)(num_seqs + 1) * 4 + (size_t)num_seqs * 4;
 }
 
-// Two E4M3 codes (low byte first) -> two f16 values (low half first), exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two_codes & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
 
 
 // 16-token tiles per sequence and their exclusive prefix over the batch,
@@ -646,10 +641,14 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                         const int kk = 4 * u + q4;
                         const uint32_t a0w = (&wa[0].x)[q4], a1w = (&wa[1].x)[q4];
                         const uint32_t b0w = (&wb[0].x)[q4], b1w = (&wb[1].x)[q4];
-                        const uint32_t a0 = e4m3x2_to_f16x2(a0w), a2 = e4m3x2_to_f16x2(a0w >> 16);
-                        const uint32_t a1 = e4m3x2_to_f16x2(a1w), a3 = e4m3x2_to_f16x2(a1w >> 16);
-                        const uint32_t b0 = e4m3x2_to_f16x2(b0w), b2 = e4m3x2_to_f16x2(b0w >> 16);
-                        const uint32_t b1 = e4m3x2_to_f16x2(b1w), b3 = e4m3x2_to_f16x2(b1w >> 16);
+                        uint32_t a0, a2;
+                        e4m3x4_to_f16x2x2(a0w, a0, a2);
+                        uint32_t a1, a3;
+                        e4m3x4_to_f16x2x2(a1w, a1, a3);
+                        uint32_t b0, b2;
+                        e4m3x4_to_f16x2x2(b0w, b0, b2);
+                        uint32_t b1, b3;
+                        e4m3x4_to_f16x2x2(b1w, b1, b3);
 #pragma unroll
                         for (int nt = 0; nt < NT; ++nt) {
                             mma16816<__half>(sa[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
@@ -725,10 +724,14 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                         const uint32_t ha = __byte_perm((&va[2].x)[wi], (&va[3].x)[wi], sel);
                         const uint32_t lb = __byte_perm((&vb[0].x)[wi], (&vb[1].x)[wi], sel);
                         const uint32_t hb = __byte_perm((&vb[2].x)[wi], (&vb[3].x)[wi], sel);
-                        const uint32_t a0 = e4m3x2_to_f16x2(la), a1 = e4m3x2_to_f16x2(la >> 16);
-                        const uint32_t a2 = e4m3x2_to_f16x2(ha), a3 = e4m3x2_to_f16x2(ha >> 16);
-                        uint32_t b0 = e4m3x2_to_f16x2(lb), b1 = e4m3x2_to_f16x2(lb >> 16);
-                        uint32_t b2 = e4m3x2_to_f16x2(hb), b3 = e4m3x2_to_f16x2(hb >> 16);
+                        uint32_t a0, a1;
+                        e4m3x4_to_f16x2x2(la, a0, a1);
+                        uint32_t a2, a3;
+                        e4m3x4_to_f16x2x2(ha, a2, a3);
+                        uint32_t b0, b1;
+                        e4m3x4_to_f16x2x2(lb, b0, b1);
+                        uint32_t b2, b3;
+                        e4m3x4_to_f16x2x2(hb, b2, b3);
                         if (valid_b < BS) {
                             b0 &= m01;
                             b1 &= m01;
@@ -787,8 +790,10 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 const uint32_t w0 = (&kw[0][kk >> 2].x)[kk & 3], w1 = (&kw[1][kk >> 2].x)[kk & 3];
-                const uint32_t a0 = e4m3x2_to_f16x2(w0), a2 = e4m3x2_to_f16x2(w0 >> 16);
-                const uint32_t a1 = e4m3x2_to_f16x2(w1), a3 = e4m3x2_to_f16x2(w1 >> 16);
+                uint32_t a0, a2;
+                e4m3x4_to_f16x2x2(w0, a0, a2);
+                uint32_t a1, a3;
+                e4m3x4_to_f16x2x2(w1, a1, a3);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
                     mma16816<__half>(sc[nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
@@ -883,8 +888,10 @@ __global__ void __launch_bounds__(Pipe<HD, FP8>::NW * 32, Pipe<HD, FP8>::MINB)
                 const uint32_t w0 = (&vw[0][wi >> 2].x)[wi & 3], w1 = (&vw[1][wi >> 2].x)[wi & 3];
                 const uint32_t w8 = (&vw[2][wi >> 2].x)[wi & 3], w9 = (&vw[3][wi >> 2].x)[wi & 3];
                 const uint32_t lo = __byte_perm(w0, w1, sel), hi = __byte_perm(w8, w9, sel);
-                uint32_t a0 = e4m3x2_to_f16x2(lo), a1 = e4m3x2_to_f16x2(lo >> 16);
-                uint32_t a2 = e4m3x2_to_f16x2(hi), a3 = e4m3x2_to_f16x2(hi >> 16);
+                uint32_t a0, a1;
+                e4m3x4_to_f16x2x2(lo, a0, a1);
+                uint32_t a2, a3;
+                e4m3x4_to_f16x2x2(hi, a2, a3);
                 if (valid < BS) {
                     a0 &= m01;
                     a1 &= m01;

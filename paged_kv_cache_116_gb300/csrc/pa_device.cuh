@@ -169,6 +169,16 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
     return y;
 }
 
+// Four E4M3 codes (low byte first) -> two f16x2 words, exact: lo holds codes
+// 0 and 1, hi codes 2 and 3 (low half first).  The word is split into its
+// 16-bit halves as registers, so no shift or mask is spent on them.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_codes, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four_codes));
+}
+
 template <typename T>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1);

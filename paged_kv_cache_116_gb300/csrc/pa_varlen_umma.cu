@@ -306,9 +306,8 @@ __device__ __forceinline__ bool warp_decode(const CUtensorMap* tmK, const CUtens
                     uint32_t h[8];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const __half2_raw lo =
-                            __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[u] & 0xffffu), __NV_E4M3);
-                        const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[u] >> 16), __NV_E4M3);
+                        uint32_t lo, hi;
+                        e4m3x4_to_f16x2x2(w[u], lo, hi);
                         __half2 a, b;
                         memcpy(&a, &lo, 4);
                         memcpy(&b, &hi, 4);
@@ -433,8 +432,8 @@ __device__ __forceinline__ void dequant_tile_in_place(uint8_t* slot, const float
             uint32_t h[8];
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
-                const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[t] & 0xffffu), __NV_E4M3);
-                const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[t] >> 16), __NV_E4M3);
+                uint32_t lo, hi;
+                e4m3x4_to_f16x2x2(w[t], lo, hi);
                 __half2 a, b;
                 memcpy(&a, &lo, 4);
                 memcpy(&b, &hi, 4);
