@@ -47,13 +47,15 @@
 // exp2-domain online softmax over the tile, P^T moved into B-fragment
 // layout with movmatrix, O^T += V^T P^T in fp32 registers.
 //
-// The grid is [prefill tile pairs | decode groups | spare].  With a
-// workspace, a one-CTA plan kernel runs first and lists the prefill tile
-// pairs longest first (bucketed by the number of 128-key tiles tile A
-// reads) and the decode rows; the varlen kernel, its programmatic
-// dependent, takes item blockIdx.x / Hkv for KV head blockIdx.x % Hkv, so
-// the long pairs of every request and both heads start in the first waves
-// and the short ones fill the tail.  Each CTA's output is independent of
+// The grid is [decode groups | prefill tile pairs | spare]: the decode
+// CTAs go first, since each streams its requests at one warp's pace and,
+// dispatched last, they were the tail of the launch.  With a workspace, a
+// one-CTA plan kernel runs first and lists the prefill tile pairs longest
+// first (bucketed by the number of 128-key tiles tile A reads) and the
+// decode rows; the varlen kernel, its programmatic dependent, takes item
+// blockIdx.x / Hkv for KV head blockIdx.x % Hkv, so the long pairs of every
+// request and both heads start in the first waves and the short ones fill
+// the tail.  Each CTA's output is independent of
 // the others', so the order changes no result.  Without a workspace every
 // CTA scans the requests' pair counts and decode flags (one packed
 // exclusive prefix in shared memory) and finds its work, in request order,
@@ -119,6 +121,7 @@ struct UmParams {
     const int32_t* plan;
     const int2* items;
     const int32_t* dec_req;
+    int32_t dec_ctas;  // decode-CTA slots per KV head, at the front of the grid
     // quantized cache (FP8 mode): fp32 scales [num_blocks, num_kv_heads, block_size]
     const float* k_scales;
     const float* v_scales;
@@ -525,9 +528,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     n_pairs = pref[S] & kPairMask;
     n_dec = pref[S] >> kPairBits;
     }
-    if (bid >= n_pairs) {
-        // ---- a decode CTA (or a spare one): decode rows of ranks DG d .. DG d + 7
-        const int64_t d = bid - n_pairs;
+    if (bid < p.dec_ctas) {
+        // ---- a decode CTA (or a spare one): decode rows of ranks DG d .. DG d + 7.
+        // They lead the grid: each streams its requests' keys at one warp's
+        // pace and would otherwise be the tail of the launch.
+        const int64_t d = bid;
         if (d * DG >= n_dec) return;  // spare (uniform for the CTA)
         if (threadIdx.x == 0) {
             for (int w = 0; w < DG * DR; ++w) mbar_init(&bars[w], 1u);
@@ -556,6 +561,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
         return;
     }
+    bid -= p.dec_ctas;
+    if (bid >= n_pairs) return;  // spare (uniform for the CTA)
     // ---- a prefill CTA: tile pair p_rel of request req
     int req;
     int64_t p_rel;
@@ -1198,6 +1205,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
     }
     const bool dec_route = G <= kMaxDecodeGroupG;
     const int64_t dgroups = dec_route ? (a.num_seqs + DG - 1) / DG : 0;
+    p.dec_ctas = (int32_t)dgroups;
     const size_t smem = um_smem_bytes<HD>(workspace ? 0 : a.num_seqs);
     cudaError_t e = cudaFuncSetAttribute(varlen_umma_kernel<T, HD, FP8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
