@@ -116,10 +116,12 @@ struct UmParams {
     int32_t causal;
     float scale_log2;
     // planned order (workspace given): plan[0] = prefill pairs, plan[1] =
-    // decode rows; items[k] = (request, pair) of the k-th prefill CTA,
+    // decode rows; items[k] describes the k-th prefill CTA's tile pair in
+    // full -- {request, tile A's first query row, its position, L with bit
+    // 31 set when a tile B precedes it} -- so the CTA reads nothing else,
     // longest first; dec_req[r] = the request of decode rank r
     const int32_t* plan;
-    const int2* items;
+    const int4* items;
     const int32_t* dec_req;
     int32_t dec_ctas;  // decode-CTA slots per KV head, at the front of the grid
     // quantized cache (FP8 mode): fp32 scales [num_blocks, num_kv_heads, block_size]
@@ -142,13 +144,17 @@ struct UGeo {
     // per tile: s_full, p_full, o_done; v_zeroed;
     // code cache only: k_conv[R], v_conv[R] (a slot's codes turned into
     // f16), q_conv (the Q tiles in f16)
-    static constexpr int NBAR = 1 + 4 * R + 6 + 1 + 2 * R + 1;
+    // (a decode CTA's warps use DR each of the same barriers)
+    static constexpr int NBAR_PF = 1 + 4 * R + 6 + 1 + 2 * R + 1;
+    static constexpr int NBAR = NBAR_PF > DG * DR ? NBAR_PF : DG * DR;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TBL_OFF = TADDR_OFF + 16;                 // two producers' table windows
     static constexpr int TBL_INTS = 2 * kTableWindow;              // rows of each group's first and second box
     // code cache: K then V scales per slot (targets of 16-byte-aligned bulk copies)
     static constexpr int SCL_OFF = (TBL_OFF + 2 * TBL_INTS * 4 + 127) / 128 * 128;
-    static constexpr int CU_OFF = SCL_OFF + 2 * R * BK * 4;
+    // code cache: a prefill CTA's [2][R][BK] scales, or a decode CTA's [DG][DR][2][BS]
+    static constexpr int SCL_BYTES = 2 * R * BK * 4 > DG * DR * 2 * BS * 4 ? 2 * R * BK * 4 : DG * DR * 2 * BS * 4;
+    static constexpr int CU_OFF = SCL_OFF + SCL_BYTES;
 };
 
 static_assert(DG * DR <= UGeo<64>::NBAR, "a decode CTA's warps use the kernel's barriers");
@@ -563,13 +569,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     bid -= p.dec_ctas;
     if (bid >= n_pairs) return;  // spare (uniform for the CTA)
-    // ---- a prefill CTA: tile pair p_rel of request req
-    int req;
-    int64_t p_rel;
+    // ---- a prefill CTA: tile pair p_rel of request req.  Per tile x (A the
+    // later tokens, B the tile before it, if any): its first query row qrx,
+    // the position of its first token psx, and its rows tnx.
+    int req, L, ntiles, qrx[2], psx[2], tnx[2], nktx[2];
     if (planned) {
-        const int2 it = __ldcg(p.items + bid);
+        const int4 it = __ldcg(p.items + bid);
         req = it.x;
-        p_rel = it.y;
+        L = it.w & 0x7fffffff;
+        ntiles = it.w < 0 ? 2 : 1;
+        qrx[0] = it.y;
+        psx[0] = it.z;
+        tnx[0] = min(TT, L - it.z);  // tile A ends at the request's last token or is full
+        qrx[1] = it.y - TT;
+        psx[1] = it.z - TT;
+        tnx[1] = ntiles == 2 ? TT : 0;
     } else {
         int lo = 0, hi = S - 1;
         while (lo < hi) {
@@ -578,22 +592,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             else hi = mid - 1;
         }
         req = lo;
-        p_rel = bid - (pref[req] & kPairMask);
+        const int p_rel = (int)(bid - (pref[req] & kPairMask));
+        const int q0 = p.cu[req], n_new = p.cu[req + 1] - q0;
+        L = p.seq_lens[req];
+        // tile A = the later tokens (last pairs first); tile B the tile before it, if any
+        const int tile_a = (n_new + TT - 1) / TT - 1 - 2 * p_rel;
+        ntiles = tile_a >= 1 ? 2 : 1;
+        for (int x = 0; x < 2; ++x) {
+            const int t = tile_a - x, t0 = t >= 0 ? t * TT : 0;
+            qrx[x] = q0 + t0;
+            psx[x] = L - n_new + t0;
+            tnx[x] = t >= 0 ? min(TT, n_new - t0) : 0;
+        }
     }
-    const int q0 = p.cu[req], n_new = p.cu[req + 1] - q0;
-    const int ntile = (n_new + TT - 1) / TT;
-    const int L = p.seq_lens[req];
-    const int first_pos = L - n_new;
     const int nb_seq = (L + BS - 1) / BS;
-    // tile A = the later tokens (last pairs first); tile B the tile before it, if any
-    const int tile_a = ntile - 1 - 2 * (int)p_rel;
-    const int ntiles = tile_a >= 1 ? 2 : 1;
-    int t0x[2], tnx[2], nktx[2];
     for (int x = 0; x < 2; ++x) {
-        const int t = tile_a - x;
-        t0x[x] = t >= 0 ? t * TT : 0;
-        tnx[x] = t >= 0 ? min(TT, n_new - t0x[x]) : 0;
-        const int kv_end = p.causal ? first_pos + t0x[x] + tnx[x] : L;
+        const int kv_end = p.causal ? psx[x] + tnx[x] : L;
         nktx[x] = x < ntiles ? (kv_end + BK - 1) / BK : 0;
     }
     const int nkt = nktx[0];  // tile A reaches at least as far as tile B
@@ -655,7 +669,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                     for (int c = 0; c < Gm::CH; ++c)
                         tma_load_3d(base + Gm::Q_OFF + x * Gm::QT + c * Gm::QCH, &tmQ, q_full, 64 * c, kvh * G,
-                                    q0 + t0x[x], pol);
+                                    qrx[x], pol);
             }
         }
         const int ngrp = min(nb_seq, nkt * BPT);
@@ -832,7 +846,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int m = threadIdx.x - 128 * x;
         const bool valid = x < ntiles && m < tnx[x] * G;
         const int ti = valid ? m / G : 0, gh = valid ? m - (m / G) * G : 0;
-        const int prow = p.causal ? first_pos + t0x[x] + ti : L - 1;
+        const int prow = p.causal ? psx[x] + ti : L - 1;
         const uint32_t t_lane = tmem + ((uint32_t)(wq * 32) << 16) + 256u * x;
         const float sl = p.scale_log2;
         float m_used = -INFINITY, l = 0.f;
@@ -1009,7 +1023,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 tc_fence_after();
                 const float inv = 1.f / l;
                 T* orow = static_cast<T*>(p.out) +
-                          ((int64_t)(q0 + t0x[x] + ti) * p.num_heads + (int64_t)kvh * G + gh) * HD;
+                          ((int64_t)(qrx[x] + ti) * p.num_heads + (int64_t)kvh * G + gh) * HD;
 #pragma unroll 1
                 for (int c = 0; c < HD / 32; ++c) {
                     float o[32];
@@ -1047,7 +1061,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __restrict__ cu,
                                                            const int32_t* __restrict__ seq_lens, int S, int TT,
                                                            int causal, int dec_route, int nbuckets, int32_t* plan,
-                                                           int2* items, int32_t* dec_req) {
+                                                           int4* items, int32_t* dec_req) {
     extern __shared__ int32_t hist[];  // [nbuckets] counts, then [nbuckets] cursors
     __shared__ int32_t n_dec_s;
     int32_t* cursor = hist + nbuckets;
@@ -1095,7 +1109,12 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __rest
         const int n = cu[i + 1] - cu[i], L = seq_lens[i];
         if (dec_route && n == 1) continue;
         const int npair = (n + 2 * TT - 1) / (2 * TT);
-        for (int pr = 0; pr < npair; ++pr) items[atomicAdd(&cursor[tiles_of(n, L, pr)], 1)] = make_int2(i, pr);
+        const int q0 = cu[i], ntile = (n + TT - 1) / TT;
+        for (int pr = 0; pr < npair; ++pr) {
+            const int t0 = (ntile - 1 - 2 * pr) * TT;  // tile A's first new token
+            items[atomicAdd(&cursor[tiles_of(n, L, pr)], 1)] =
+                make_int4(i, q0 + t0, L - n + t0, L | (t0 >= TT ? (int)0x80000000u : 0));
+        }
     }
     if (threadIdx.x == 0) plan[1] = n_dec_s;
 }
@@ -1142,7 +1161,7 @@ bool um_encode(CUtensorMap* m, const void* base, int dtype, const cuuint64_t dim
 int64_t um_pairs_bound(int64_t total_q, int32_t num_seqs, int TT) { return total_q / (2 * TT) + num_seqs; }
 size_t um_round(size_t b) { return (b + 255) & ~(size_t)255; }
 size_t um_plan_bytes(int64_t total_q, int32_t num_seqs, int TT) {
-    return 256 + um_round((size_t)um_pairs_bound(total_q, num_seqs, TT) * sizeof(int2)) +
+    return 256 + um_round((size_t)um_pairs_bound(total_q, num_seqs, TT) * sizeof(int4)) +
            um_round((size_t)num_seqs * sizeof(int32_t));
 }
 
@@ -1216,8 +1235,8 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
     if (workspace) {
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         p.plan = reinterpret_cast<const int32_t*>(ws);
-        p.items = reinterpret_cast<const int2*>(ws + 256);
-        p.dec_req = reinterpret_cast<const int32_t*>(ws + 256 + um_round((size_t)pairs * sizeof(int2)));
+        p.items = reinterpret_cast<const int4*>(ws + 256);
+        p.dec_req = reinterpret_cast<const int32_t*>(ws + 256 + um_round((size_t)pairs * sizeof(int4)));
         const int nbuckets = (int)std::min<int64_t>(kMaxPlanBuckets, (int64_t)(a.max_context + BK - 1) / BK + 2);
         cudaLaunchConfig_t pc = {};
         pc.gridDim = dim3(1);
@@ -1228,7 +1247,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         pc.numAttrs = 1;
         e = cudaLaunchKernelEx(&pc, varlen_plan_kernel, a.cu_seqlens_q, a.seq_lens, a.num_seqs, TT, a.causal,
                                dec_route ? 1 : 0, nbuckets, const_cast<int32_t*>(p.plan),
-                               const_cast<int2*>(p.items), const_cast<int32_t*>(p.dec_req));
+                               const_cast<int4*>(p.items), const_cast<int32_t*>(p.dec_req));
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
