@@ -895,17 +895,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // exceeds it by more than 8 (P then stays below 2^8, far inside
             // its type's range).  So once every row of the warp has a
             // maximum, one pass over the scores gives the exponentials and
-            // the tile's maximum together; only the first tile, a tile that
-            // outgrows some row's maximum, or a non-positive scale takes the
-            // maximum first and then the exponentials.  Whether to redo is
-            // decided per warp (tensor-memory loads are warp-wide); a row
-            // whose maximum did not grow recomputes the same values.
+            // their sum, which bounds them; only the first tile, a tile whose
+            // sum says it may outgrow some row's maximum, or a non-positive
+            // scale takes the maximum and then the exponentials.  Whether to
+            // redo is decided per warp (tensor-memory loads are warp-wide); a
+            // row whose maximum did not grow recomputes the same values.
             // 64 scores per tensor-memory wait; P (two per column) is kept in
             // registers until it is final, then written over the low half of
             // the S columns; masked keys get exactly 0.
-            float sum = 0.f, mraw = -INFINITY;  // mraw: the tile's maximum raw score
+            float sum = 0.f;
             float pk[BK / 2];  // the tile's P, two per 32-bit column, stored once it is final
-            auto exp_pass = [&](float neg_m, bool track) {
+            auto exp_pass = [&](float neg_m) {
                 sum = 0.f;
 #pragma unroll
                 for (int q64 = 0; q64 < BK / 64; ++q64) {
@@ -916,7 +916,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     if (full) {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            if (track) mraw = fmaxf(mraw, fmaxf(a[2 * j], a[2 * j + 1]));
                             const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
                             const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
                             sum += e0 + e1;
@@ -927,7 +926,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
                             const bool v0 = 2 * j <= nv, v1 = 2 * j + 1 <= nv;
-                            if (track) mraw = fmaxf(mraw, fmaxf(v0 ? a[2 * j] : -INFINITY, v1 ? a[2 * j + 1] : -INFINITY));
                             const float e0 = v0 ? fast_exp2(fmaf(a[2 * j], sl, neg_m)) : 0.f;
                             const float e1 = v1 ? fast_exp2(fmaf(a[2 * j + 1], sl, neg_m)) : 0.f;
                             sum += e0 + e1;
@@ -953,25 +951,32 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 return sl > 0.f ? m_t * sl : m_t;
             };
             // a positive scale keeps the order, so the maximum is taken on raw scores
-            bool one_pass = sl > 0.f && __all_sync(0xffffffffu, m_used != -INFINITY);
-            float m_tile = -INFINITY;
-            if (one_pass) {
-                exp_pass(-m_used, true);
-                m_tile = mraw * sl;
-                one_pass = __all_sync(0xffffffffu, !(m_tile > m_used + 8.f));
-            } else {
-                m_tile = max_pass();
-            }
-            bool grow = false;
+            const bool have_max = sl > 0.f && __all_sync(0xffffffffu, m_used != -INFINITY);
+            float m_tile = have_max ? -INFINITY : max_pass();
+            bool grow = false, settled = !have_max;  // settled: this tile's exponent base is final
             float alpha = 1.f;
-            if (!one_pass) {
+            auto settle = [&]() {
                 const float m_new = fmaxf(m_used, m_tile);
                 grow = (m_used == -INFINITY) || (m_new > m_used + 8.f);
                 if (grow) {
                     alpha = fast_exp2(m_used - m_new);
                     m_used = m_new;
                 }
-                exp_pass(-m_used, false);
+            };
+            if (settled) settle();
+            // One call site of the pass.  A row's exponents sum to at least
+            // their maximum, so a sum of at most 2^8 proves that no score of
+            // the tile exceeded the row's maximum by more than 8: the pass
+            // stands.  Otherwise (rare: the tile outgrew some row's maximum,
+            // or many scores sit just above it) the tile's maximum is taken
+            // and the pass redone against it.
+#pragma unroll 1
+            for (;;) {
+                exp_pass(-m_used);
+                if (settled || __all_sync(0xffffffffu, !(sum > 256.f))) break;
+                m_tile = max_pass();
+                settled = true;
+                settle();
             }
             // P over the first 64 S columns, all of which have been read
             tmem_st32(t_lane + P_COL, *reinterpret_cast<float(*)[32]>(pk));
