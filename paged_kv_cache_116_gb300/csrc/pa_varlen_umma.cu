@@ -914,13 +914,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_ld32(t_lane + S_COL + 64 * q64 + 32, *reinterpret_cast<float(*)[32]>(a + 32));
                     tmem_wait_ld();
                     if (full) {
+                        // two scores per fma and two exponents per add (packed fp32x2)
+                        const unsigned long long slv = f32x2_pack(sl, sl), nmv = f32x2_pack(neg_m, neg_m);
+                        unsigned long long s2 = f32x2_pack(0.f, 0.f);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
-                            const float e0 = fast_exp2(fmaf(a[2 * j], sl, neg_m));
-                            const float e1 = fast_exp2(fmaf(a[2 * j + 1], sl, neg_m));
-                            sum += e0 + e1;
+                            float x0, x1;
+                            f32x2_unpack(fma_f32x2(f32x2_pack(a[2 * j], a[2 * j + 1]), slv, nmv), x0, x1);
+                            const float e0 = fast_exp2(x0), e1 = fast_exp2(x1);
+                            s2 = add_f32x2(s2, f32x2_pack(e0, e1));
                             pk[32 * q64 + j] = __uint_as_float(pack2<PT>(e0, e1));
                         }
+                        float s0, s1;
+                        f32x2_unpack(s2, s0, s1);
+                        sum += s0 + s1;
                     } else {
                         const int nv = vis - 64 * q64;  // columns j <= nv are visible
 #pragma unroll
