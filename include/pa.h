@@ -324,7 +324,10 @@ PA_API pa_status pa_decode_append_fp8(void* out, const void* q, const void* k_ne
  * request i is at position seq_lens[i] - n_i + j and, with causal != 0,
  * attends to positions 0..that position; with causal == 0 to all
  * seq_lens[i] positions.  Decode rows (n_i = 1) and prefill chunks mix
- * freely in one call.
+ * freely in one call.  bf16/f16 with head_dim 64, 128 or 256, at most 128
+ * query heads per KV head and block_size 8 or a multiple of 16 up to 256
+ * (head_dim 256: a multiple of 16) run on the tcgen05 (tensor-memory)
+ * kernel; the rest on the CUDA-core kernel.
  *   out, q:       device [total_q, num_heads, head_dim] of dtype (16-byte aligned)
  *   cu_seqlens_q: device int32 [num_seqs + 1], cu_seqlens_q[0] = 0,
  *                 non-decreasing, cu_seqlens_q[num_seqs] = total_q

@@ -606,8 +606,8 @@ static pa_status varlen_impl(void* out, const void* q, const void* k_cache, cons
     if (want == 2 && !um_ok)
         return fail(PA_ERR_UNSUPPORTED, fp8 ? "the tcgen05 varlen kernel over a code cache takes bf16/f16 "
                                               "queries, head_dim 128 and block_size 8 or a multiple of 16"
-                                            : "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128 and "
-                                              "block_size 8 or a multiple of 16");
+                                            : "the tcgen05 varlen kernel takes bf16/f16, head_dim 64/128/256 and "
+                                              "block_size a multiple of 16 (or 8, below head_dim 256)");
     const bool use_um = um_ok && (want == 2 || want == 0);
     cudaStream_t st = as_stream(stream);
     if (check_mode()) {

@@ -1,6 +1,10 @@
 // pa_varlen_umma.cu -- the varlen prefill/decode mix on the 5th-generation
 // tensor cores (tcgen05.mma, accumulators in tensor memory), bf16/f16,
-// head_dim 64 or 128, block_size 8 or a multiple of 16 up to 256.
+// head_dim 64, 128 or 256, block_size 8 or a multiple of 16 up to 256
+// (head_dim 256: a multiple of 16).  At head_dim 256 a CTA takes one query
+// tile instead of two (S and O use 384 of the 512 tensor-memory columns) and
+// its K and V rings have one slot (Q, K and V tiles of 64 KB each), and
+// decode rows take the prefill path.
 //
 // Same arithmetic as the handbook's paged_attention ("分页 KV Cache",
 // §分页注意力): request i owns query rows cu[i] .. cu[i+1]-1, its new token j
@@ -129,23 +133,28 @@ struct UmParams {
     const float* v_scales;
 };
 
+// Head dims up to 128: two query tiles per CTA and two-slot K and V rings.
+// Head dim 256: one query tile (S and O take 384 of the 512 tensor-memory
+// columns) and one-slot rings (Q, K and V tiles of 64 KB each).
 template <int HD>
 struct UGeo {
+    static constexpr int NQ = HD == 256 ? 1 : 2;  // query tiles per CTA (the pair width)
+    static constexpr int RK = HD == 256 ? 1 : 2;  // K and V ring slots
     static constexpr int CH = HD / 64;          // 128-byte chunks per head row
     static constexpr int QCH = TM * 128;        // bytes of one chunk of a Q tile
     static constexpr int KCH = BK * 128;        // bytes of one chunk of a K (or V) tile
     static constexpr int QT = CH * QCH;         // bytes of a Q tile
     static constexpr int Q_OFF = 0;             // Q tiles A, B
     static constexpr int TILE = CH * KCH;       // bytes of a K (or V) tile
-    static constexpr int K_OFF = 2 * QT;
-    static constexpr int V_OFF = K_OFF + R * TILE;
-    static constexpr int BAR_OFF = V_OFF + R * TILE;
+    static constexpr int K_OFF = NQ * QT;
+    static constexpr int V_OFF = K_OFF + RK * TILE;
+    static constexpr int BAR_OFF = V_OFF + RK * TILE;
     // q_full, k_full[R], k_empty[R], v_full[R], v_empty[R],
     // per tile: s_full, p_full, o_done; v_zeroed;
     // code cache only: k_conv[R], v_conv[R] (a slot's codes turned into
     // f16), q_conv (the Q tiles in f16)
     // (a decode CTA's warps use DR each of the same barriers)
-    static constexpr int NBAR_PF = 1 + 4 * R + 6 + 1 + 2 * R + 1;
+    static constexpr int NBAR_PF = 1 + 4 * RK + 6 + 1 + 2 * RK + 1;
     static constexpr int NBAR = NBAR_PF > DG * DR ? NBAR_PF : DG * DR;
     static constexpr int TADDR_OFF = BAR_OFF + NBAR * 8;
     static constexpr int TBL_OFF = TADDR_OFF + 16;                 // two producers' table windows
@@ -153,12 +162,14 @@ struct UGeo {
     // code cache: K then V scales per slot (targets of 16-byte-aligned bulk copies)
     static constexpr int SCL_OFF = (TBL_OFF + 2 * TBL_INTS * 4 + 127) / 128 * 128;
     // code cache: a prefill CTA's [2][R][BK] scales, or a decode CTA's [DG][DR][2][BS]
-    static constexpr int SCL_BYTES = 2 * R * BK * 4 > DG * DR * 2 * BS * 4 ? 2 * R * BK * 4 : DG * DR * 2 * BS * 4;
+    static constexpr int SCL_BYTES = 2 * RK * BK * 4 > DG * DR * 2 * BS * 4 ? 2 * RK * BK * 4 : DG * DR * 2 * BS * 4;
     static constexpr int CU_OFF = SCL_OFF + SCL_BYTES;
 };
 
 static_assert(DG * DR <= UGeo<64>::NBAR, "a decode CTA's warps use the kernel's barriers");
-static_assert(UGeo<128>::SCL_OFF % 128 == 0 && UGeo<64>::SCL_OFF % 128 == 0, "scale area aligned for bulk copies");
+static_assert(UGeo<128>::SCL_OFF % 128 == 0 && UGeo<64>::SCL_OFF % 128 == 0 && UGeo<256>::SCL_OFF % 128 == 0,
+              "scale area aligned for bulk copies");
+static_assert(UGeo<256>::CU_OFF + 1024 + (kMaxSeqsSmem + 1) * 4 <= 232448, "head_dim 256 fits in shared memory");
 static_assert(DG * DR * 2 * BS * 64 * 2 <= UGeo<64>::BAR_OFF && DG * DR * 2 * BS * 128 * 2 <= UGeo<128>::BAR_OFF,
               "decode warps' stages fit below the barriers");
 
@@ -467,6 +478,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                        const __grid_constant__ CUtensorMap tmV, const UmParams p) {
     using Gm = UGeo<HD>;
     static_assert(!FP8 || HD == 128, "the code cache is read at head_dim 128");
+    constexpr int R = Gm::RK;   // K and V ring slots at this head dim
+    constexpr int PW = Gm::NQ;  // query tiles per CTA (2: a tile pair; 1: one tile)
     // the MMA operand type: the query type, or f16 over a code cache
     constexpr bool kBF16 = std::is_same<T, __nv_bfloat16>::value && !FP8;
     using PT = typename std::conditional<FP8, __half, T>::type;
@@ -498,7 +511,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // for a decode row taken by a decode CTA) and whether it is such a
     // decode row; one packed exclusive prefix of both over the requests.
     int32_t* pref = reinterpret_cast<int32_t*>(base + Gm::CU_OFF);  // [S + 1]
-    const bool dec_route = G <= kMaxDecodeGroupG;
+    const bool dec_route = G <= kMaxDecodeGroupG && HD <= 128;
     int64_t bid = blockIdx.x;
     int n_pairs, n_dec;
     if (planned) {
@@ -509,7 +522,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         const int n = p.cu[i + 1] - p.cu[i];
         const bool dec = dec_route && n == 1;
-        pref[i + 1] = dec ? (1 << kPairBits) : (n + 2 * TT - 1) / (2 * TT);
+        pref[i + 1] = dec ? (1 << kPairBits) : (n + PW * TT - 1) / (PW * TT);
     }
     if (threadIdx.x == 0) pref[0] = 0;
     __syncthreads();
@@ -559,12 +572,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 else lo = mid + 1;
             }
         }
-        constexpr int kStage = 2 * BS * HD * 2;
-        uint8_t* wst = base + (size_t)warp * DR * kStage;
-        float* wscl = scl_s + warp * DR * 2 * BS;  // FP8: this warp's [DR][2][16] scales
-        const bool ok = G <= 8 ? warp_decode<T, HD, 1, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane)
-                               : warp_decode<T, HD, 2, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane);
-        if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
+        if constexpr (HD <= 128) {  // (no decode CTAs at head_dim 256: dec_ctas is 0 there)
+            constexpr int kStage = 2 * BS * HD * 2;
+            uint8_t* wst = base + (size_t)warp * DR * kStage;
+            float* wscl = scl_s + warp * DR * 2 * BS;  // FP8: this warp's [DR][2][16] scales
+            const bool ok = G <= 8
+                                ? warp_decode<T, HD, 1, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane)
+                                : warp_decode<T, HD, 2, FP8>(&tmK, &tmV, p, lo, kvh, wst, bars + warp * DR, wscl, lane);
+            if (!ok && lane == 0) atomicOr(&g_umma_status, kStatusTimeout);
+        }
         return;
     }
     bid -= p.dec_ctas;
@@ -596,8 +612,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int q0 = p.cu[req], n_new = p.cu[req + 1] - q0;
         L = p.seq_lens[req];
         // tile A = the later tokens (last pairs first); tile B the tile before it, if any
-        const int tile_a = (n_new + TT - 1) / TT - 1 - 2 * p_rel;
-        ntiles = tile_a >= 1 ? 2 : 1;
+        const int tile_a = (n_new + TT - 1) / TT - 1 - PW * p_rel;
+        ntiles = PW == 2 && tile_a >= 1 ? 2 : 1;
         for (int x = 0; x < 2; ++x) {
             const int t = tile_a - x, t0 = t >= 0 ? t * TT : 0;
             qrx[x] = q0 + t0;
@@ -630,7 +646,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // them so their scores are finite and their (never stored) rows
         // take the same unmasked path as the rest of their warp
         const int pad = TM - G * TT, per_tile = Gm::CH * pad * 8;
-        for (int e = threadIdx.x; e < 2 * per_tile; e += NTHREADS) {
+        for (int e = threadIdx.x; e < PW * per_tile; e += NTHREADS) {
             const int x = e / per_tile, r0 = e - x * per_tile, c = r0 / (pad * 8), r = r0 - c * pad * 8;
             *reinterpret_cast<uint4*>(base + Gm::Q_OFF + x * Gm::QT + c * Gm::QCH + (G * TT + r / 8) * 128 +
                                       (r & 7) * 16) = make_uint4(0, 0, 0, 0);
@@ -1072,8 +1088,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 // pairs, plan[1] = decode rows.
 __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __restrict__ cu,
                                                            const int32_t* __restrict__ seq_lens, int S, int TT,
-                                                           int causal, int dec_route, int nbuckets, int32_t* plan,
-                                                           int4* items, int32_t* dec_req) {
+                                                           int PW, int causal, int dec_route, int nbuckets,
+                                                           int32_t* plan, int4* items, int32_t* dec_req) {
     extern __shared__ int32_t hist[];  // [nbuckets] counts, then [nbuckets] cursors
     __shared__ int32_t n_dec_s;
     int32_t* cursor = hist + nbuckets;
@@ -1084,7 +1100,7 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __rest
     __syncthreads();
     // 128-key tiles tile A of pair pr of a request reads
     auto tiles_of = [&](int n, int L, int pr) -> int {
-        const int ntile = (n + TT - 1) / TT, ta = ntile - 1 - 2 * pr, t0 = ta * TT;
+        const int ntile = (n + TT - 1) / TT, ta = ntile - 1 - PW * pr, t0 = ta * TT;
         const int kv_end = causal ? L - n + t0 + min(TT, n - t0) : L;
         return min((kv_end + BK - 1) / BK, nbuckets - 1);
     };
@@ -1094,7 +1110,7 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __rest
             dec_req[atomicAdd(&n_dec_s, 1)] = i;
             continue;
         }
-        const int npair = (n + 2 * TT - 1) / (2 * TT);
+        const int npair = (n + PW * TT - 1) / (PW * TT);
         for (int pr = 0; pr < npair; ++pr) atomicAdd(&hist[tiles_of(n, L, pr)], 1);
     }
     __syncthreads();
@@ -1120,12 +1136,12 @@ __global__ void __launch_bounds__(1024) varlen_plan_kernel(const int32_t* __rest
     for (int i = threadIdx.x; i < S; i += blockDim.x) {
         const int n = cu[i + 1] - cu[i], L = seq_lens[i];
         if (dec_route && n == 1) continue;
-        const int npair = (n + 2 * TT - 1) / (2 * TT);
+        const int npair = (n + PW * TT - 1) / (PW * TT);
         const int q0 = cu[i], ntile = (n + TT - 1) / TT;
         for (int pr = 0; pr < npair; ++pr) {
-            const int t0 = (ntile - 1 - 2 * pr) * TT;  // tile A's first new token
+            const int t0 = (ntile - 1 - PW * pr) * TT;  // tile A's first new token
             items[atomicAdd(&cursor[tiles_of(n, L, pr)], 1)] =
-                make_int4(i, q0 + t0, L - n + t0, L | (t0 >= TT ? (int)0x80000000u : 0));
+                make_int4(i, q0 + t0, L - n + t0, L | (PW == 2 && t0 >= TT ? (int)0x80000000u : 0));
         }
     }
     if (threadIdx.x == 0) plan[1] = n_dec_s;
@@ -1169,8 +1185,9 @@ bool um_encode(CUtensorMap* m, const void* base, int dtype, const cuuint64_t dim
 }
 
 // Workspace layout of a planned launch: plan header, prefill items (one per
-// possible tile pair), decode-row requests.
-int64_t um_pairs_bound(int64_t total_q, int32_t num_seqs, int TT) { return total_q / (2 * TT) + num_seqs; }
+// possible tile pair, or tile at head_dim 256: the bound below covers both),
+// decode-row requests.
+int64_t um_pairs_bound(int64_t total_q, int32_t num_seqs, int TT) { return total_q / TT + num_seqs; }
 size_t um_round(size_t b) { return (b + 255) & ~(size_t)255; }
 size_t um_plan_bytes(int64_t total_q, int32_t num_seqs, int TT) {
     return 256 + um_round((size_t)um_pairs_bound(total_q, num_seqs, TT) * sizeof(int4)) +
@@ -1227,14 +1244,16 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
     p.dec_req = nullptr;
     p.k_scales = a.k_scales;
     p.v_scales = a.v_scales;
-    // prefill tile pairs (at most total_q / 2T + one per request), then
-    // decode CTAs of DG requests; CTAs past the work the kernel finds return
-    const int64_t pairs = (int64_t)a.total_q / (2 * TT) + a.num_seqs;
+    // prefill tile pairs (at most total_q / 2T + one per request; single
+    // tiles at head_dim 256), then decode CTAs of DG requests; CTAs past the
+    // work the kernel finds return
+    constexpr int PW = UGeo<HD>::NQ;
+    const int64_t pairs = (int64_t)a.total_q / (PW * TT) + a.num_seqs;
     if (pairs >= (1 << kPairBits)) {
         *err = "too many query rows for one varlen launch";
         return cudaErrorInvalidValue;
     }
-    const bool dec_route = G <= kMaxDecodeGroupG;
+    const bool dec_route = G <= kMaxDecodeGroupG && HD <= 128;
     const int64_t dgroups = dec_route ? (a.num_seqs + DG - 1) / DG : 0;
     p.dec_ctas = (int32_t)dgroups;
     const size_t smem = um_smem_bytes<HD>(workspace ? 0 : a.num_seqs);
@@ -1248,7 +1267,8 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         uint8_t* ws = static_cast<uint8_t*>(workspace);
         p.plan = reinterpret_cast<const int32_t*>(ws);
         p.items = reinterpret_cast<const int4*>(ws + 256);
-        p.dec_req = reinterpret_cast<const int32_t*>(ws + 256 + um_round((size_t)pairs * sizeof(int4)));
+        const int64_t items_cap = um_pairs_bound(a.total_q, a.num_seqs, TT);  // the workspace's layout
+        p.dec_req = reinterpret_cast<const int32_t*>(ws + 256 + um_round((size_t)items_cap * sizeof(int4)));
         const int nbuckets = (int)std::min<int64_t>(kMaxPlanBuckets, (int64_t)(a.max_context + BK - 1) / BK + 2);
         cudaLaunchConfig_t pc = {};
         pc.gridDim = dim3(1);
@@ -1257,7 +1277,7 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
         pc.stream = stream;
         pc.attrs = attr;
         pc.numAttrs = 1;
-        e = cudaLaunchKernelEx(&pc, varlen_plan_kernel, a.cu_seqlens_q, a.seq_lens, a.num_seqs, TT, a.causal,
+        e = cudaLaunchKernelEx(&pc, varlen_plan_kernel, a.cu_seqlens_q, a.seq_lens, a.num_seqs, TT, PW, a.causal,
                                dec_route ? 1 : 0, nbuckets, const_cast<int32_t*>(p.plan),
                                const_cast<int4*>(p.items), const_cast<int32_t*>(p.dec_req));
         if (e != cudaSuccess) return e;
@@ -1276,9 +1296,11 @@ cudaError_t um_launch(const AttnArgs& a, int32_t num_blocks, void* workspace, st
 }  // namespace
 
 bool varlen_umma_supported(int dtype, int head_dim, int block_size, int group, bool kv_fp8) {
-    return (dtype == 1 || dtype == 2) && (kv_fp8 ? head_dim == 128 : (head_dim == 64 || head_dim == 128)) &&
-           (block_size == 8 || (block_size % BS == 0 && block_size <= 256)) && group >= 1 &&
-           group <= TM;
+    // head_dim 256: block sizes whose 16-token groups are single boxes (a
+    // 64-box tile of 8-token blocks would exceed the lanes that issue boxes)
+    const bool hd_ok = kv_fp8 ? head_dim == 128 : (head_dim == 64 || head_dim == 128 || head_dim == 256);
+    const bool bs_ok = (block_size == 8 && head_dim <= 128) || (block_size % BS == 0 && block_size <= 256);
+    return (dtype == 1 || dtype == 2) && hd_ok && bs_ok && group >= 1 && group <= TM;
 }
 
 size_t varlen_umma_workspace(int32_t num_seqs, int64_t total_q, int32_t group) {
@@ -1294,10 +1316,12 @@ cudaError_t launch_varlen_umma(const AttnArgs& a, int32_t num_blocks, void* work
             return a.dtype == 1 ? um_launch<__nv_bfloat16, 128, true>(c, num_blocks, ws, err, stream)
                                 : um_launch<__half, 128, true>(c, num_blocks, ws, err, stream);
         if (a.dtype == 1)
-            return a.head_dim == 64 ? um_launch<__nv_bfloat16, 64>(c, num_blocks, ws, err, stream)
-                                    : um_launch<__nv_bfloat16, 128>(c, num_blocks, ws, err, stream);
-        return a.head_dim == 64 ? um_launch<__half, 64>(c, num_blocks, ws, err, stream)
-                                : um_launch<__half, 128>(c, num_blocks, ws, err, stream);
+            return a.head_dim == 64    ? um_launch<__nv_bfloat16, 64>(c, num_blocks, ws, err, stream)
+                   : a.head_dim == 128 ? um_launch<__nv_bfloat16, 128>(c, num_blocks, ws, err, stream)
+                                       : um_launch<__nv_bfloat16, 256>(c, num_blocks, ws, err, stream);
+        return a.head_dim == 64    ? um_launch<__half, 64>(c, num_blocks, ws, err, stream)
+               : a.head_dim == 128 ? um_launch<__half, 128>(c, num_blocks, ws, err, stream)
+                                   : um_launch<__half, 256>(c, num_blocks, ws, err, stream);
     };
     if (workspace) return one(a, workspace);  // planned: any number of requests in one launch
     // unplanned: a launch scans at most kMaxSeqsSmem requests in shared

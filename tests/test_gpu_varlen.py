@@ -177,3 +177,50 @@ def test_varlen_tcgen05_block_sizes(pa, bs):
         exact = oracle_attention(w, causal=causal)
         for routed in (False, True):
             compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2, routed=routed), exact)
+
+
+HD256_CASES = []
+_r3 = np.random.default_rng(256)
+for _i in range(8):
+    _g = int(_r3.choice([1, 2, 3, 4, 8, 12, 16]))
+    _hkv = int(_r3.choice([1, 2]))
+    _dt = str(_r3.choice(["bf16", "f16"]))
+    _bs = int(_r3.choice([16, 32]))
+    _S = int(_r3.integers(1, 7))
+    _q = _r3.integers(1, 200, _S)
+    _q[_r3.random(_S) < 0.4] = 1  # decode rows (the prefill path takes them at this head dim)
+    _cached = _r3.integers(0, 300, _S)
+    HD256_CASES.append((_dt, _bs, _g, _hkv, (_cached + _q).tolist(), _q.tolist(), _i))
+
+
+@pytest.mark.parametrize("dt,bs,g,hkv,lens,qlens,seed", HD256_CASES)
+def test_varlen_tcgen05_head_dim_256(pa, dt, bs, g, hkv, lens, qlens, seed):
+    """head_dim 256 on the tensor cores: one query tile per CTA (S and O take
+    384 tensor-memory columns) and one-slot K / V rings."""
+    w = W.varlen_workload("hd256", dt, bs, g * hkv, hkv, 256, lens, qlens, seed=300 + seed)
+    kc, vc, bt = device_caches(w, DEV)
+    for causal in (True, False):
+        exact = oracle_attention(w, causal=causal)
+        for routed in (False, True):
+            compare(w, run_varlen(pa, w, kc, vc, bt, causal=causal, kernel=2, routed=routed), exact)
+    pa.pa_device_status(clear=True)  # raises if a kernel recorded a timeout
+
+
+def test_varlen_head_dim_256_relabelling_bit_identical(pa):
+    w = W.varlen_workload("perm_256", "bf16", 16, 8, 2, 256, [300, 81, 17, 700], [1, 81, 5, 130], seed=7)
+    kc, vc, bt = device_caches(w, DEV)
+    base = run_varlen(pa, w, kc, vc, bt, kernel=2, routed=True)
+    compare(w, base, oracle_attention(w))
+    perm = torch.from_numpy(np.random.default_rng(8).permutation(w.num_blocks)).to(DEV)
+    kc2, vc2 = torch.empty_like(kc), torch.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = torch.where(bt >= 0, perm[bt.clamp(min=0).long()].int(), bt)
+    again = run_varlen(pa, w, kc2, vc2, bt2, kernel=2, routed=True)
+    assert torch.equal(base.view(torch.int16), again.view(torch.int16))
+
+
+def test_varlen_head_dim_256_block_size_8_takes_the_cuda_core_path(pa):
+    w = W.varlen_workload("hd256_bs8", "bf16", 8, 4, 2, 256, [40, 9, 70], [12, 1, 30], seed=9)
+    kc, vc, bt = device_caches(w, DEV)
+    compare(w, run_varlen(pa, w, kc, vc, bt, kernel=0), oracle_attention(w))
