@@ -96,46 +96,64 @@ __global__ void __launch_bounds__(kWarps * 32) attn_simt_kernel(AttnArgs a) {
             acc[h][k] = 0.f;
         }
     }
-    for (int t = warp; t < visible; t += kWarps) {
-        const int64_t blk = table[t / a.block_size], off_in = t % a.block_size;
-        const int64_t slot = blk * a.block_size + off_in;
-        float ks = 1.f, vs = 1.f;
-        if constexpr (FP8) {
-            const int64_t si = (blk * a.num_kv_heads + kvh) * a.block_size + off_in;
-            ks = a.k_scales[si];
-            vs = a.v_scales[si];
+    // U tokens per warp in flight: their table entries load together, then
+    // their K/V rows, so a warp waits for two memory round trips per U
+    // tokens rather than per token; they are then folded in in order (as
+    // many as the registers hold without spilling)
+    constexpr int U = DPL <= 2 ? 4 : (DPL * GH <= 16 ? 2 : 1);
+    for (int t0 = warp; t0 < visible; t0 += U * kWarps) {
+        int64_t slot[U];
+        float ks[U], vs[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int t = min(t0 + u * kWarps, visible - 1);  // in range; unused past `visible`
+            const int64_t blk = table[t / a.block_size], off_in = t % a.block_size;
+            slot[u] = blk * a.block_size + off_in;
+            ks[u] = vs[u] = 1.f;
+            if constexpr (FP8) {
+                const int64_t si = (blk * a.num_kv_heads + kvh) * a.block_size + off_in;
+                ks[u] = a.k_scales[si];
+                vs[u] = a.v_scales[si];
+            }
         }
-        const typename C::S* kr = kc + slot * row_elts;
-        const typename C::S* vr = vc + slot * row_elts;
-        float kx[DPL], vx[DPL];
+        float kx[U][DPL], vx[U][DPL];
 #pragma unroll
-        for (int k = 0; k < DPL; ++k) {
-            const int d = lane + 32 * k;
-            kx[k] = d < hd ? C::to_f(kr[d]) : 0.f;
-            vx[k] = d < hd ? C::to_f(vr[d]) : 0.f;
-        }
-        float dot[GH];
+        for (int u = 0; u < U; ++u) {
+            const typename C::S* kr = kc + slot[u] * row_elts;
+            const typename C::S* vr = vc + slot[u] * row_elts;
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            dot[h] = 0.f;
-#pragma unroll
-            for (int k = 0; k < DPL; ++k) dot[h] = fmaf(qv[h][k], kx[k], dot[h]);
+            for (int k = 0; k < DPL; ++k) {
+                const int d = lane + 32 * k;
+                kx[u][k] = d < hd ? C::to_f(kr[d]) : 0.f;
+                vx[u][k] = d < hd ? C::to_f(vr[d]) : 0.f;
+            }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1)
+        for (int u = 0; u < U; ++u) {
+            if (t0 + u * kWarps >= visible) break;  // warp-uniform
+            float dot[GH];
 #pragma unroll
-            for (int h = 0; h < GH; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+            for (int h = 0; h < GH; ++h) {
+                dot[h] = 0.f;
 #pragma unroll
-        for (int h = 0; h < GH; ++h) {
-            const float x = dot[h] * ks * scale_log2;
-            const float m_new = fmaxf(m[h], x);
-            const float corr = exp2f(m[h] - m_new);
-            const float p = exp2f(x - m_new);
-            l[h] = l[h] * corr + p;
-            const float pv = p * vs;
+                for (int k = 0; k < DPL; ++k) dot[h] = fmaf(qv[h][k], kx[u][k], dot[h]);
+            }
 #pragma unroll
-            for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(pv, vx[k], acc[h][k] * corr);
-            m[h] = m_new;
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int h = 0; h < GH; ++h) dot[h] += __shfl_xor_sync(0xffffffffu, dot[h], off);
+#pragma unroll
+            for (int h = 0; h < GH; ++h) {
+                const float x = dot[h] * ks[u] * scale_log2;
+                const float m_new = fmaxf(m[h], x);
+                const float corr = exp2f(m[h] - m_new);
+                const float p = exp2f(x - m_new);
+                l[h] = l[h] * corr + p;
+                const float pv = p * vs[u];
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) acc[h][k] = fmaf(pv, vx[u][k], acc[h][k] * corr);
+                m[h] = m_new;
+            }
         }
     }
 
