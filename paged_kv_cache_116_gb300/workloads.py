@@ -316,6 +316,79 @@ def mixed_varlen(seed: int = 0, num_chunks: int = 16, num_groups: int = 60, grou
               f"{num_groups}x{group_size} samples share a {prompt_len}-token prompt")
 
 
+def forked_decode_mix(layout, dtype="bf16", block_size=16, num_heads=12, num_kv_heads=2, head_dim=128,
+                      seed=0, device="cpu") -> Workload:
+    """A varlen step whose decode rows include parallel-sampling groups.
+
+    layout: a list of requests in order, each
+      ("chunk", n_new, cached)        a prefill chunk after `cached` tokens;
+      ("single", L)                   a decode row over L tokens (own blocks);
+      ("group", prompt_len, extras)   len(extras) samples forked from one
+                                      prompt: they share its full blocks, each
+                                      has its own blocks from the prompt's
+                                      partial tail on, holding extras[j] more
+                                      cached tokens of its own, and appends
+                                      one token (L = prompt_len + extras[j] + 1).
+    Cached rows are written before the step (the shared prompt rows once,
+    through the first sample's table); the new rows by the step.  Physical
+    blocks come from a shuffled free list."""
+    bs = block_size
+    rng = np.random.default_rng(seed)
+    lens, qlens, cached_of, tables, pre_rows = [], [], [], [], []
+    need = 0
+    for item in layout:
+        if item[0] == "chunk":
+            need += _blocks_for(int(item[1]) + int(item[2]), bs)
+        elif item[0] == "single":
+            need += _blocks_for(int(item[1]), bs)
+        else:
+            shared = int(item[1]) // bs
+            need += shared + sum(_blocks_for(int(item[1]) + int(e) + 1, bs) - shared for e in item[2])
+    num_blocks = max(1, int(math.ceil(need * 1.1)) + 4)
+    free = list(rng.permutation(num_blocks))
+    for item in layout:
+        if item[0] in ("chunk", "single"):
+            L = int(item[1]) + int(item[2]) if item[0] == "chunk" else int(item[1])
+            n = int(item[1]) if item[0] == "chunk" else 1
+            t = [int(free.pop()) for _ in range(_blocks_for(L, bs))]
+            lens.append(L)
+            qlens.append(n)
+            tables.append(t)
+            pre_rows.append((len(tables) - 1, 0, L - n))
+        else:
+            prompt, extras = int(item[1]), [int(e) for e in item[2]]
+            shared = [int(free.pop()) for _ in range(prompt // bs)]
+            for j, e in enumerate(extras):
+                L = prompt + e + 1
+                t = shared + [int(free.pop()) for _ in range(_blocks_for(L, bs) - len(shared))]
+                lens.append(L)
+                qlens.append(1)
+                tables.append(t)
+                # the shared rows once (first sample), every sample's own rows
+                pre_rows.append((len(tables) - 1, 0 if j == 0 else len(shared) * bs, L - 1))
+    S = len(lens)
+    seq_lens, query_lens = np.asarray(lens, np.int32), np.asarray(qlens, np.int32)
+    bt = _pad_tables(tables)
+    pre_seq = np.concatenate([np.full(b - a, i, np.int32) for i, a, b in pre_rows])
+    pre_pos = np.concatenate([np.arange(a, b, dtype=np.int64) for i, a, b in pre_rows])
+    new_seq = np.repeat(np.arange(S, dtype=np.int32), query_lens.astype(np.int64))
+    new_pos = np.concatenate([np.arange(int(seq_lens[i] - query_lens[i]), int(seq_lens[i]), dtype=np.int64)
+                              for i in range(S)])
+    g = _gen(seed + 1, device)
+    N = int(query_lens.sum())
+    q = _normal(g, (N, num_heads, head_dim), 1.0, dtype)
+    pre_k = _normal(g, (pre_pos.shape[0], num_kv_heads, head_dim), 1.0, dtype)
+    pre_v = _normal(g, (pre_pos.shape[0], num_kv_heads, head_dim), 1.0, dtype)
+    new_k = _normal(g, (N, num_kv_heads, head_dim), 1.0, dtype)
+    new_v = _normal(g, (N, num_kv_heads, head_dim), 1.0, dtype)
+    return Workload(
+        name="forked_decode_mix", dtype=dtype, block_size=bs, num_blocks=num_blocks, num_heads=num_heads,
+        num_kv_heads=num_kv_heads, head_dim=head_dim, scale=head_dim ** -0.5, causal=True, seq_lens=seq_lens,
+        query_lens=query_lens, block_tables=bt, pre_block_tables=bt, pre_seq_idx=pre_seq, pre_pos=pre_pos,
+        pre_k=pre_k, pre_v=pre_v, new_seq_idx=new_seq, new_pos=new_pos, new_k=new_k, new_v=new_v, q=q, seed=seed,
+        notes="layout %r" % (layout,))
+
+
 def handbook_check(seed: int = 0, dtype: str = "f32") -> Workload:
     """The handbook's verification layout: contexts [37, 5, 20] with [1, 5, 8]
     new tokens (a decode, a full prefill, the second half of a chunked

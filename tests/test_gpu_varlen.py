@@ -224,3 +224,61 @@ def test_varlen_head_dim_256_block_size_8_takes_the_cuda_core_path(pa):
     w = W.varlen_workload("hd256_bs8", "bf16", 8, 4, 2, 256, [40, 9, 70], [12, 1, 30], seed=9)
     kc, vc, bt = device_caches(w, DEV)
     compare(w, run_varlen(pa, w, kc, vc, bt, kernel=0), oracle_attention(w))
+
+
+# Parallel-sampling layouts: runs of decode rows forked from one prompt
+# (their tables share the prompt's full blocks, each has its own blocks from
+# the partial tail on, some with more cached tokens of their own), lone decode
+# rows and prefill chunks between them.  (dtype, block size, head dim, G, Hkv)
+FORK_CASES = [
+    ("bf16", 16, 128, 6, 2),
+    ("f16", 16, 128, 4, 2),
+    ("bf16", 8, 64, 2, 3),
+    ("bf16", 8, 128, 4, 1),
+    ("bf16", 32, 128, 8, 1),
+    ("f16", 16, 64, 1, 4),
+    ("bf16", 64, 128, 3, 2),
+    ("bf16", 16, 128, 12, 1),
+]
+FORK_LAYOUT = [("chunk", 40, 20), ("group", 37, [0, 5, 21, 3]), ("single", 50), ("group", 16, [0, 0, 17]),
+               ("group", 7, [2, 9]), ("chunk", 3, 0), ("group", 300, [0, 0, 0, 0, 0]),
+               ("group", 130, [40, 0, 77, 1, 2, 3, 4]), ("single", 1), ("group", 33, [0, 1])]
+
+
+def decode_rows(w):
+    return torch.from_numpy(w.query_start_loc[:-1][w.query_lens == 1].astype(np.int64)).to(DEV)
+
+
+@pytest.mark.parametrize("dt,bs,hd,g,hkv", FORK_CASES)
+def test_varlen_forked_decode_rows(pa, dt, bs, hd, g, hkv):
+    """Forked samples' decode rows against the oracle with the plan
+    (workspace given), and bit for bit against the same launch without it:
+    the plan changes which CTA works a row, not its arithmetic."""
+    w = W.forked_decode_mix(FORK_LAYOUT, dt, bs, g * hkv, hkv, hd, seed=bs + hd + g)
+    kc, vc, bt = device_caches(w, DEV)
+    planned = run_varlen(pa, w, kc, vc, bt, kernel=2, routed=True)
+    compare(w, planned, oracle_attention(w))
+    unplanned = run_varlen(pa, w, kc, vc, bt, kernel=2, routed=False)
+    rows = decode_rows(w)
+    assert torch.equal(planned[rows].view(torch.int16), unplanned[rows].view(torch.int16))
+    pa.pa_device_status(clear=True)
+
+
+def test_varlen_forked_decode_rows_many_requests(pa):
+    """Over a thousand decode rows in runs of forked samples, with chunks and
+    lone rows between runs (more requests than the plan kernel's threads)."""
+    rng = np.random.default_rng(7)
+    layout = [("chunk", 70, 30)]
+    while sum(len(x[2]) if x[0] == "group" else 1 for x in layout) < 1300:
+        k = int(rng.integers(1, 8))
+        layout.append(("group", int(rng.integers(1, 60)), rng.integers(0, 20, k).tolist()))
+        if rng.random() < 0.1:
+            layout.append(("single", int(rng.integers(1, 40))))
+    w = W.forked_decode_mix(layout, "bf16", 16, 4, 1, 64, seed=11)
+    kc, vc, bt = device_caches(w, DEV)
+    planned = run_varlen(pa, w, kc, vc, bt, kernel=2, routed=True)
+    compare(w, planned, oracle_attention(w))
+    unplanned = run_varlen(pa, w, kc, vc, bt, kernel=2, routed=False)
+    rows = decode_rows(w)
+    assert torch.equal(planned[rows].view(torch.int16), unplanned[rows].view(torch.int16))
+    pa.pa_device_status(clear=True)
