@@ -598,3 +598,17 @@ def test_varlen_fp8_permutation_bit_identical(pa):
     again = run_varlen_fp8(pa, w, (*pools2, bt2), kernel=2, planned=True)
     assert torch.equal(base.view(torch.int16), again.view(torch.int16))
 
+
+
+def test_varlen_fp8_long_contexts(pa):
+    """Over the quantized cache: a chunk after 20,000 cached tokens and
+    decode rows over 17,000 and 33,000 tokens (several table windows of the
+    producers and of a decode warp), every kernel that applies."""
+    w = W.varlen_workload("long_vfp8", "bf16", 16, 12, 2, 128, [20032, 17000, 33000, 150], [32, 1, 1, 150],
+                          seed=77)
+    pools = device_fp8_caches(w, DEV)
+    opools = oracle_fp8_caches(w)
+    assert_pools_equal(pools[:4], opools)
+    exact = oracle_varlen_fp8(w, opools, True)
+    for kernel, planned in varlen_fp8_kernels(w):
+        compare(w, run_varlen_fp8(pa, w, pools, kernel=kernel, planned=planned), exact)

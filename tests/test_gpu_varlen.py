@@ -282,3 +282,19 @@ def test_varlen_forked_decode_rows_many_requests(pa):
     rows = decode_rows(w)
     assert torch.equal(planned[rows].view(torch.int16), unplanned[rows].view(torch.int16))
     pa.pa_device_status(clear=True)
+
+
+@pytest.mark.parametrize("bs", [8, 16, 256])
+def test_varlen_long_contexts(pa, bs):
+    """Contexts past one block-table window of the prefill producers (512
+    16-token groups, 8,192 tokens) and of a decode warp (32 tiles): a chunk
+    of 32 after 20,000 cached tokens, decode rows over 17,000 and 33,000
+    tokens, a short full prefill; with and without the plan, and on the
+    CUDA-core kernel."""
+    w = W.varlen_workload("long_vl", "bf16", bs, 12, 2, 128, [20032, 17000, 33000, 150], [32, 1, 1, 150],
+                          seed=40 + bs)
+    kc, vc, bt = device_caches(w, DEV)
+    exact = oracle_attention(w)
+    for kernel, routed in ((2, False), (2, True), (1, False)):
+        compare(w, run_varlen(pa, w, kc, vc, bt, kernel=kernel, routed=routed), exact)
+    pa.pa_device_status(clear=True)
