@@ -89,7 +89,6 @@ constexpr int BS = 16;          // keys per group (one TMA box of 16 rows, or tw
 constexpr int BK = 128;         // keys per tile
 constexpr int BPT = BK / BS;    // groups per key tile
 constexpr int TM = 128;         // rows of the MMA tile
-constexpr int R = 2;            // K and V stages
 constexpr int NWARPS = 11;      // 2 x 4 softmax warps, K producer, V producer, MMA issuer
 constexpr int NTHREADS = NWARPS * 32;
 constexpr int W_KPROD = 8, W_VPROD = 9, W_MMA = 10;
