@@ -504,6 +504,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool planned = p.plan != nullptr;
     const int Hkv = p.num_heads / G;
     const int kvh = planned ? (int)(blockIdx.x % Hkv) : (int)blockIdx.y;
+    // the tensor maps are kernel parameters: their descriptors are fetched
+    // while this grid waits for the previous kernel (a first TMA through a
+    // descriptor not yet fetched stalls its issuing thread)
+    if (threadIdx.x == 32 * W_KPROD) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
     pdl_wait_primary();
 
     // ---- work of this CTA.  Per request: its tile pairs (ceil(n / 2T); none
@@ -513,8 +521,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const bool dec_route = G <= kMaxDecodeGroupG && HD <= 128;
     int64_t bid = blockIdx.x;
     int n_pairs, n_dec;
+    int4 item = make_int4(0, 0, 0, 0);
     if (planned) {
         bid = blockIdx.x / Hkv;
+        // a prefill slot's item is read with the plan's counts, not after
+        // them: slots past the pairs read an unused entry (the item array
+        // holds one per slot) and return below
+        if (bid >= p.dec_ctas) item = __ldcg(p.items + (bid - p.dec_ctas));
         n_pairs = __ldcg(p.plan);
         n_dec = __ldcg(p.plan + 1);
     } else {
@@ -589,7 +602,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // the position of its first token psx, and its rows tnx.
     int req, L, ntiles, qrx[2], psx[2], tnx[2], nktx[2];
     if (planned) {
-        const int4 it = __ldcg(p.items + bid);
+        const int4 it = item;
         req = it.x;
         L = it.w & 0x7fffffff;
         ntiles = it.w < 0 ? 2 : 1;
@@ -676,9 +689,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint64_t* emps = is_v ? v_empty : k_empty;
         int32_t* tbl_s = reinterpret_cast<int32_t*>(base + Gm::TBL_OFF) + is_v * Gm::TBL_INTS;
         if (lane == 0) {
-            prefetch_tmap(tm);
             if (!is_v) {
-                prefetch_tmap(&tmQ);
                 mbar_arrive_expect_tx(q_full, (uint32_t)(ntiles * Gm::CH * 128 * G * TT));
                 for (int x = 0; x < ntiles; ++x)
 #pragma unroll
