@@ -78,3 +78,26 @@ def test_argument_errors_need_no_gpu(lib):
     assert lib.pa_write_kv(None, None, None, 0, None, None, 10, 16, 2, 128, 1, None) == 0
     assert lib.pa_decode(None, None, None, None, None, 4, None, 0, 8, 2, 128, 10, 16, 64, 1.0, 1, None, 0,
                          None) == 0
+
+
+def test_varlen_workspace_holds_an_item_for_every_prefill_slot(lib):
+    """The tensor-core varlen kernel reads the plan item of every prefill
+    slot of its grid (total_q / (P T) + num_seqs slots; P query tiles per
+    CTA, T = 128 / G tokens per tile) before it knows how many hold work, so
+    the workspace must hold that many 16-byte items after its 256-byte
+    header, and the decode-row list (4 bytes per request) after them."""
+    import numpy as np
+
+    bf16 = 1
+    rng = np.random.default_rng(5)
+    lib.pa_varlen_workspace_size.restype = ctypes.c_size_t
+    for _ in range(300):
+        hd = int(rng.choice([64, 128, 256]))
+        g = int(rng.choice([1, 2, 3, 4, 6, 8, 12, 16]))
+        hkv = int(rng.integers(1, 5))
+        S = int(rng.integers(1, 5000))
+        total_q = int(rng.integers(S, 40 * S + 2))
+        ws = lib.pa_varlen_workspace_size(S, total_q, total_q, g * hkv, hkv, hd, 16, 4096, bf16)
+        P, T = (1 if hd == 256 else 2), 128 // g
+        slots = total_q // (P * T) + S
+        assert ws >= 256 + 16 * slots + 4 * S, (hd, g, S, total_q, ws)
